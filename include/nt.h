@@ -1,0 +1,244 @@
+/*
+ * nt.h -- C ABI of the packed ternary-weight decode library (libnt).
+ *
+ * What the library computes comes from "The Neutrino Engine" (Fermion Research):
+ *
+ *   - § "A 104 microsecond floor inside a 694 microsecond step": at batch one each weight
+ *     feeds a single multiply-accumulate per token and nearly all of them are touched, so
+ *     the weight bytes divided by the memory bandwidth give a floor on the time per token.
+ *     Weights are consumed in their packed form: no floating-point copy of them exists,
+ *     nothing is converted per token and each tensor is read at most once per token. The
+ *     final projection covers every vocabulary row.
+ *   - § "The file is not the traffic": per token, all ternary projection matrices (q, k, v,
+ *     o, gate, up and down of every layer) are streamed, each row carrying a scale; the
+ *     vocabulary tables hold int8 values in 151,936 rows of 4,096 columns, and every row of
+ *     the output table is scored.
+ *   - § "One changed token fails the release" and § "The 0.6B model does not get to decide":
+ *     the emitted token is the greedy (arg-max) choice.
+ *   - § "The same weights take four execution paths": the values are rearranged for each
+ *     device once, when the model is loaded (here: nt_repack_ternary).
+ *
+ * The pages publish no kernel and no format, so the bit layout, the activation quantizer,
+ * the epilogue rounding order and the tie rule below are this library's stated readings.
+ *
+ * Conventions (every call):
+ *   - Returns nt_status; NT_OK is 0. No C++ exception crosses this boundary.
+ *     nt_last_error_string() gives a detail string for the calling host thread.
+ *   - Every tensor argument is a DEVICE pointer (CUDA global memory) owned by the caller,
+ *     unless the argument says "host". The library never frees or retains caller memory
+ *     beyond the call, except a decode plan, which keeps the pointers its descriptor named.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ *     default stream) and never synchronize the device. Argument errors are detected on the
+ *     host before any launch; launch errors return NT_ERR_CUDA; faults inside a kernel
+ *     surface at the caller's next synchronization.
+ *   - Inputs are never modified. Outputs are written in full.
+ *   - Hot calls allocate nothing. Where scratch is needed the caller passes a workspace of
+ *     the size the matching *_workspace_size call reports.
+ *   - Sizes are int; every product that addresses memory is computed in 64-bit.
+ *
+ * Data formats:
+ *   - Plain ternary layout (NT_LAYOUT_PLAIN), the exchange format: row-major uint32
+ *     W[N][K/16]; trit k of row n is the 2-bit field at bits [2(k%16), 2(k%16)+1] of word
+ *     W[n][k/16] (least-significant field first). Field codes: 00 -> 0, 01 -> +1,
+ *     11 -> -1; 10 is invalid (decoded as 0 by every kernel, counted by
+ *     nt_repack_ternary). K must be a multiple of 16.
+ *   - Tiled ternary layout (NT_LAYOUT_TILED), made by nt_repack_ternary: rows are padded
+ *     to Np = roundup(N, 4) and columns to Kp = roundup(K, 512) with zero trits. Tile t
+ *     holds rows 4t..4t+3 as Kp/16 consecutive 16-byte groups; group j holds, for each of
+ *     the 4 rows r (in order), one 32-bit word with trits 16j..16j+15 of row 4t+r. Inside
+ *     a word, nibble i (i = 0..3) codes the pair (trit 16j+i, trit 16j+4+i) and nibble 4+i
+ *     codes (trit 16j+8+i, trit 16j+12+i) with the pair codes
+ *        (0,0)=0 (+1,0)=1 (-1,0)=2 (0,+1)=3 (+1,+1)=4 (-1,+1)=5 (+1,-1)=6 (-1,-1)=7
+ *        (0,-1)=14
+ *     -- the code the byte-permute decode in the kernels reads directly. Same 2 bits per
+ *     trit as the plain layout; only padding adds bytes.
+ *   - Activations: int8 q[B][K] row-major with one fp32 scale s_x[b] per vector.
+ *   - Output table (lm-head): int8 T[V][K] row-major with fp32 row scales s_T[V].
+ *
+ * Arithmetic (the reading every kernel and the oracle follow):
+ *   quantize:  m = max_k |x_k|; if m == 0 then s = 0 and q = 0; else s = m / 127 (fp32
+ *              division, round to nearest even) and q_k = clamp(rint(x_k / s), -127, 127)
+ *              with an fp32 division and round-half-to-even.
+ *   project:   acc[n] = sum_k t[n][k] * q[k] (exact int32);
+ *              y[n] = fl(fl(float(acc[n]) * s_w[n]) * s_x) -- int-to-float round to nearest,
+ *              then two fp32 products, each rounded to nearest, no fused multiply-add.
+ *   lm-head:   logit[v] = fl(fl(float(acc[v]) * s_T[v]) * s_x) the same way; argmax is the
+ *              lowest v whose logit is maximal (+0 and -0 compare equal).
+ */
+#ifndef NT_H_
+#define NT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NT_ABI_VERSION 1
+
+typedef enum nt_status {
+  NT_OK = 0,
+  NT_ERR_INVALID_ARG = 1, /* a size, enum or pointer argument is out of range or NULL */
+  NT_ERR_ALIGNMENT = 2,   /* a pointer is not aligned as the call requires */
+  NT_ERR_UNSUPPORTED = 3, /* the current device is not compute capability 10.3 (GB300) */
+  NT_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed (detail string has it) */
+  NT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (decode plan status) */
+  NT_ERR_WORKSPACE = 6    /* the workspace is NULL or smaller than the size call reported */
+} nt_status;
+
+enum nt_layout { NT_LAYOUT_PLAIN = 0, NT_LAYOUT_TILED = 1 };
+
+/* Version of this header's ABI; equals NT_ABI_VERSION of the library that was built. */
+int nt_abi_version(void);
+
+/* Static English text for a status code. Never NULL. */
+const char* nt_status_string(nt_status s);
+
+/* Detail of the last error returned to the calling host thread ("" if none). The pointer
+ * stays valid until the next nt_* call on the same thread. */
+const char* nt_last_error_string(void);
+
+/* Checks that the current CUDA device is a GB300 (compute capability 10.3) and reports its
+ * SM count (host int*, may be NULL). Every other call performs the same check once per
+ * device and returns NT_ERR_UNSUPPORTED on any other device. */
+nt_status nt_device_check(int* sm_count_opt);
+
+/* ---------------------------------------------------------------------------------------
+ * Activation quantization (int8, one absmax scale per vector).
+ * The pages state the int8 tables but not how activations reach int8; this call is the
+ * plain symmetric absmax reading given at the top of this header.
+ *   x    [B][K] fp32, 4-byte aligned         q   [B][K] int8
+ *   s_x  [B] fp32 (output)                   B >= 1, K >= 1
+ * Non-finite inputs give unspecified (but memory-safe) results.
+ */
+nt_status nt_quantize_act(const float* x, int B, int K, int8_t* q, float* s_x, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Load-time arrangement ("The same weights take four execution paths": values are
+ * rearranged per device once, at load). Converts a plain ternary matrix into the
+ * tiled layout. Run once per matrix; not part of a decode step.
+ *   w_plain     [N][K/16] uint32, 4-byte aligned; K % 16 == 0, N >= 1
+ *   w_tiled     nt_repack_size(N, K) bytes, 16-byte aligned (output)
+ *   n_invalid_opt  device uint32 counter or NULL; when given, the call ADDS the number of
+ *                  invalid 10 fields it met (each decoded as 0).
+ */
+nt_status nt_repack_size(int N, int K, size_t* bytes);
+nt_status nt_repack_ternary(const uint32_t* w_plain, int N, int K, void* w_tiled,
+                            uint32_t* n_invalid_opt, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Ternary projection, batch 1 ("A 104 microsecond floor ...": each weight feeds one
+ * multiply-accumulate per token; "The file is not the traffic": ternary projection
+ * matrices with a scale per row).
+ *   w        layout NT_LAYOUT_PLAIN ([N][K/16] uint32, 4-byte aligned) or
+ *            NT_LAYOUT_TILED (nt_repack_ternary output, 16-byte aligned)
+ *   s_w      [N] fp32 row scales            q  [K] int8      s_x  [1] fp32
+ *   y        [N] fp32 (output)              acc_opt [N] int32 (output) or NULL
+ *   K % 16 == 0, N >= 1.
+ */
+nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, int K,
+                          const int8_t* q, const float* s_x, float* y, int32_t* acc_opt,
+                          void* stream);
+
+/* Ternary projection of B activation vectors that share the weights (the batched verify
+ * pass in "The 0.6B model does not get to decide" scores several positions in one pass).
+ *   q [B][K] int8, s_x [B], y [B][N] fp32 (output), acc_opt [B][N] int32 or NULL.
+ * Results equal B independent nt_ternary_gemv calls, bit for bit. Any B >= 1 is accepted.
+ */
+nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,
+                          const int8_t* q, const float* s_x, int B, float* y,
+                          int32_t* acc_opt, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * int8 output projection with fused greedy arg-max ("A 104 microsecond floor ...": the
+ * last projection turns the final hidden vector into a score for every vocabulary entry;
+ * "The file is not the traffic": int8 tables, 151,936 x 4,096, every output row scored;
+ * greedy decode per "One changed token fails the release").
+ *   T [V][K] int8 (16-byte aligned, K % 16 == 0)   s_T [V] fp32
+ *   q [B][K] int8 (16-byte aligned)                s_x [B] fp32
+ *   logits_opt [B][V] fp32 (output) or NULL        argmax [B] int32 (output)
+ *   ws: nt_int8_logits_workspace_size(V, K, B) bytes of device memory that is zero-filled
+ *       before its first use; every call returns it to that state. Calls that share one
+ *       workspace must not overlap on the device.
+ */
+nt_status nt_int8_logits_workspace_size(int V, int K, int B, size_t* bytes);
+nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
+                                const int8_t* q, const float* s_x, int B, float* logits_opt,
+                                int32_t* argmax, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Decode step: every projection of every layer, then optionally the output projection, in
+ * one submission ("A 104 microsecond floor ...": on the instrumented A100 step, roughly
+ * 590 of 694 microseconds were spent across about 120 kernel boundaries rather than in
+ * DRAM transfers, and a single fused kernel's software barriers brought similar waits back).
+ */
+enum nt_step_mode {
+  NT_STEP_INDEPENDENT = 0, /* every projection has its own supplied input; no ordering */
+  NT_STEP_ORDERED = 1      /* per layer {q,k,v} -> {o} -> {gate,up} -> {down}, layer by
+                              layer, each stage complete before the next one starts */
+};
+enum nt_launcher {
+  NT_LAUNCH_PERSISTENT = 0, /* one cooperative kernel streams the whole step */
+  NT_LAUNCH_GRAPH = 1,      /* a CUDA graph of one launch per stage, replayed per step */
+  NT_LAUNCH_STREAM = 2      /* the same launches issued one by one (the launch-gap case) */
+};
+
+/* One projection. All pointers device; the weights in NT_LAYOUT_TILED. */
+typedef struct nt_proj {
+  int N, K;
+  const void* w;     /* nt_repack_ternary output for an N x K matrix */
+  const float* s_w;  /* [N] */
+  const float* x;    /* [B][K] fp32 input to quantize inside the step, or NULL */
+  int8_t* q;         /* [B][K] int8: written by the step when x != NULL, else read */
+  float* s_x;        /* [B]: written when x != NULL, else read */
+  float* y;          /* [B][N] fp32 output */
+} nt_proj;
+
+typedef struct nt_decode_desc {
+  int n_layers;          /* >= 1 */
+  int batch;             /* B, 1..16 */
+  const nt_proj* proj;   /* host array of n_layers * 7 entries, per layer in the order
+                            q, k, v, o, gate, up, down; copied at plan creation */
+  /* Output projection; head_T == NULL leaves it out. */
+  const int8_t* head_T;  /* [V][K] int8 */
+  const float* head_s;   /* [V] */
+  int head_V, head_K;
+  const float* head_x;   /* [B][K] fp32 hidden to quantize in the step, or NULL */
+  int8_t* head_q;        /* [B][K] int8 (written when head_x != NULL, else read) */
+  float* head_sx;        /* [B] */
+  float* head_logits;    /* [B][V] fp32 or NULL */
+  int32_t* head_argmax;  /* [B] int32 */
+  int mode;              /* enum nt_step_mode */
+  int launcher;          /* enum nt_launcher */
+  double timeout_ms;     /* bound on every device-side wait of the persistent kernel;
+                            <= 0 selects 250 ms */
+} nt_decode_desc;
+
+typedef struct nt_decode_plan nt_decode_plan;
+
+/* Validates the descriptor, allocates the plan's own small device state (schedule, barrier
+ * counters, workspace) and, for NT_LAUNCH_GRAPH, builds the graph. Not a hot call. */
+nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** plan);
+
+/* Runs one decode step on `stream`. Allocates nothing. Steps of one plan must not overlap
+ * on the device (issue them on one stream). NT_LAUNCH_PERSISTENT needs every CTA of its
+ * grid resident at once and returns NT_ERR_CUDA if the device cannot provide that. */
+nt_status nt_decode_step(nt_decode_plan* plan, void* stream);
+
+/* After the caller has synchronized with the last step: NT_OK, or NT_ERR_TIMEOUT when a
+ * bounded wait inside the persistent kernel ran out (the step's outputs are then invalid
+ * and the plan must be reset before reuse). Reads 4 bytes from the device (synchronous). */
+nt_status nt_decode_step_status(nt_decode_plan* plan, nt_status* device_status);
+
+/* Clears the plan's device-side error word and barrier counters (synchronous). */
+nt_status nt_decode_plan_reset(nt_decode_plan* plan);
+
+/* Releases the plan and everything it allocated. NULL is ignored. */
+void nt_decode_plan_destroy(nt_decode_plan* plan);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NT_H_ */
