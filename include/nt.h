@@ -213,6 +213,10 @@ typedef struct nt_decode_desc {
   int launcher;          /* enum nt_launcher */
   double timeout_ms;     /* bound on every device-side wait of the persistent kernel;
                             <= 0 selects 250 ms */
+  int test_fault;        /* 0 in normal use. 1 makes the first grid barrier of the
+                            persistent kernel wait for one arrival more than the grid makes,
+                            so that wait runs out after timeout_ms and the step reports
+                            NT_ERR_TIMEOUT: the hook the tests of the timeout path use. */
 } nt_decode_desc;
 
 typedef struct nt_decode_plan nt_decode_plan;

@@ -1,0 +1,250 @@
+// nt_step.cu -- the decode plan: every projection of every layer, then the output projection,
+// submitted as one step ("The Neutrino Engine", § "A 104 microsecond floor inside a 694
+// microsecond step": on the instrumented step most of the time went to about 120 kernel
+// boundaries, and one fused kernel's software barriers brought the waits back).
+//
+// Launchers:
+//   NT_LAUNCH_STREAM     one launch per stage issued on the caller's stream every step;
+//   NT_LAUNCH_GRAPH      the same launches captured once into a CUDA graph, replayed per step;
+//   NT_LAUNCH_PERSISTENT one cooperative kernel streams the whole step (nt_persist.cu).
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "nt_kernels.cuh"
+#include "nt_step.cuh"
+
+using namespace nt;
+
+namespace {
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+nt_status validate_desc(const nt_decode_desc* d) {
+  if (!d) return set_error(NT_ERR_INVALID_ARG, "NULL descriptor");
+  if (d->n_layers < 1 || !d->proj) return set_error(NT_ERR_INVALID_ARG, "need n_layers >= 1 and a projection array");
+  if (d->batch < 1 || d->batch > kStepMaxBatch) return set_error(NT_ERR_INVALID_ARG, "batch must be in [1, 16]");
+  if (d->mode != NT_STEP_INDEPENDENT && d->mode != NT_STEP_ORDERED)
+    return set_error(NT_ERR_INVALID_ARG, "mode must be NT_STEP_INDEPENDENT or NT_STEP_ORDERED");
+  if (d->launcher != NT_LAUNCH_PERSISTENT && d->launcher != NT_LAUNCH_GRAPH && d->launcher != NT_LAUNCH_STREAM)
+    return set_error(NT_ERR_INVALID_ARG, "unknown launcher");
+  for (int i = 0; i < d->n_layers * kProjPerLayer; ++i) {
+    const nt_proj& p = d->proj[i];
+    if (p.N < 1 || p.K < 16 || p.K % 16 != 0)
+      return set_error(NT_ERR_INVALID_ARG, "projection " + std::to_string(i) + ": need N >= 1 and K a positive multiple of 16");
+    if (!p.w || !p.s_w || !p.q || !p.s_x || !p.y)
+      return set_error(NT_ERR_INVALID_ARG, "projection " + std::to_string(i) + ": NULL pointer");
+    if (!aligned(p.w, 16) || !aligned(p.q, 16) || !aligned(p.s_w, 4) || !aligned(p.s_x, 4) ||
+        !aligned(p.y, 4) || (p.x && !aligned(p.x, 4)))
+      return set_error(NT_ERR_ALIGNMENT, "projection " + std::to_string(i) + ": misaligned pointer");
+  }
+  if (d->head_T) {
+    if (d->head_V < 1 || d->head_K < 16 || d->head_K % 16 != 0)
+      return set_error(NT_ERR_INVALID_ARG, "head: need V >= 1 and K a positive multiple of 16");
+    if (!d->head_s || !d->head_q || !d->head_sx || !d->head_argmax)
+      return set_error(NT_ERR_INVALID_ARG, "head: NULL pointer");
+    if (!aligned(d->head_T, 16) || !aligned(d->head_q, 16) || (d->head_x && !aligned(d->head_x, 4)))
+      return set_error(NT_ERR_ALIGNMENT, "head: misaligned pointer");
+  }
+  return NT_OK;
+}
+
+// Issues the per-stage launches of one step on `st` (stream and graph launchers).
+nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
+  if (p->n_qjobs) NT_TRY(launch_quantize_jobs(p->d_qjobs, p->n_qjobs, p->B, st));
+  for (const PlanStage& s : p->stages)
+    NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
+                                   s.total_tiles, p->B, st));
+  if (p->has_head)
+    NT_TRY(launch_head(p->head_T, p->head_s, p->head_V, p->head_K, p->head_q, p->head_sx, p->B,
+                       p->head_logits, p->head_argmax, p->d_head_ws, st));
+  return NT_OK;
+}
+
+void free_plan(nt_decode_plan* p) {
+  if (!p) return;
+  if (p->exec) cudaGraphExecDestroy(p->exec);
+  if (p->graph) cudaGraphDestroy(p->graph);
+  cudaFree(p->d_mats);
+  cudaFree(p->d_prefix);
+  cudaFree(p->d_qjobs);
+  cudaFree(p->d_head_ws);
+  cudaFree(p->d_ctrl);
+  cudaFree(p->d_sched);
+  delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
+  clear_error();
+  if (!out) return set_error(NT_ERR_INVALID_ARG, "NULL plan pointer");
+  *out = nullptr;
+  NT_TRY(validate_desc(d));
+  int sms = 0;
+  NT_TRY(check_device(&sms));
+  nt_decode_plan* p = new nt_decode_plan();
+  p->sm_count = sms;
+  cudaGetDevice(&p->device);
+  p->n_layers = d->n_layers;
+  p->B = d->batch;
+  p->mode = d->mode;
+  p->launcher = d->launcher;
+  p->timeout_ns = (uint64_t)((d->timeout_ms > 0 ? d->timeout_ms : 250.0) * 1e6);
+  p->test_fault = d->test_fault;
+
+  // Matrices in step order, and the stages that group them.
+  const int n_proj = d->n_layers * kProjPerLayer;
+  std::vector<MatDesc> mats(n_proj);
+  std::vector<QuantJob> jobs;
+  for (int i = 0; i < n_proj; ++i) {
+    const nt_proj& pr = d->proj[i];
+    MatDesc& m = mats[i];
+    m.w = static_cast<const uint8_t*>(pr.w);
+    m.s_w = pr.s_w;
+    m.q = pr.q;
+    m.s_x = pr.s_x;
+    m.y = pr.y;
+    m.acc = nullptr;
+    m.N = pr.N;
+    m.K = pr.K;
+    m.B = d->batch;
+    if (pr.x) jobs.push_back(QuantJob{pr.x, pr.q, pr.s_x, pr.K, d->batch});
+  }
+  p->mats = mats;
+  std::vector<int64_t> prefix;
+  auto add_stage = [&](int first, int n) {
+    PlanStage s{first, n, (int64_t)prefix.size(), 0};
+    int64_t acc = 0;
+    for (int i = 0; i < n; ++i) {
+      prefix.push_back(acc);
+      acc += padded_rows(mats[first + i].N) / 4;
+    }
+    prefix.push_back(acc);
+    s.total_tiles = acc;
+    p->stages.push_back(s);
+  };
+  if (d->mode == NT_STEP_INDEPENDENT) {
+    add_stage(0, n_proj);
+  } else {
+    for (int l = 0; l < d->n_layers; ++l) {
+      const int b = l * kProjPerLayer;
+      add_stage(b + 0, 3);  // q, k, v
+      add_stage(b + 3, 1);  // o
+      add_stage(b + 4, 2);  // gate, up
+      add_stage(b + 6, 1);  // down
+    }
+  }
+
+  p->has_head = d->head_T != nullptr;
+  if (p->has_head) {
+    p->head_T = d->head_T;
+    p->head_s = d->head_s;
+    p->head_V = d->head_V;
+    p->head_K = d->head_K;
+    p->head_q = d->head_q;
+    p->head_sx = d->head_sx;
+    p->head_logits = d->head_logits;
+    p->head_argmax = d->head_argmax;
+    if (d->head_x) jobs.push_back(QuantJob{d->head_x, d->head_q, d->head_sx, d->head_K, d->batch});
+  }
+  p->n_qjobs = (int)jobs.size();
+
+  auto fail = [&](nt_status s) { free_plan(p); return s; };
+  auto cuda_fail = [&](cudaError_t e, const char* what) {
+    set_error(NT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    free_plan(p);
+    return NT_ERR_CUDA;
+  };
+  cudaError_t e;
+  if ((e = cudaMalloc(&p->d_mats, sizeof(MatDesc) * mats.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  if ((e = cudaMemcpy(p->d_mats, mats.data(), sizeof(MatDesc) * mats.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy");
+  if ((e = cudaMalloc(&p->d_prefix, sizeof(int64_t) * prefix.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  if ((e = cudaMemcpy(p->d_prefix, prefix.data(), sizeof(int64_t) * prefix.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy");
+  if (!jobs.empty()) {
+    if ((e = cudaMalloc(&p->d_qjobs, sizeof(QuantJob) * jobs.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemcpy(p->d_qjobs, jobs.data(), sizeof(QuantJob) * jobs.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy");
+  }
+  if (p->has_head) {
+    const size_t ws = head_ws_bytes(p->B);
+    if ((e = cudaMalloc(&p->d_head_ws, ws)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_head_ws, 0, ws)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
+  if ((e = cudaMalloc(&p->d_ctrl, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  if ((e = cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+
+  if (p->launcher == NT_LAUNCH_PERSISTENT) {
+    const nt_status s = persist_prepare(p);
+    if (s != NT_OK) return fail(s);
+  } else if (p->launcher == NT_LAUNCH_GRAPH) {
+    cudaStream_t cs;
+    if ((e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking)) != cudaSuccess) return cuda_fail(e, "cudaStreamCreate");
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) { cudaStreamDestroy(cs); return cuda_fail(e, "cudaStreamBeginCapture"); }
+    const nt_status s = issue_launches(p, cs);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    p->graph = g;
+    if (s != NT_OK) return fail(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+    if ((e = cudaGraphInstantiate(&p->exec, p->graph, 0)) != cudaSuccess) return cuda_fail(e, "cudaGraphInstantiate");
+  }
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  *out = p;
+  return NT_OK;
+}
+
+nt_status nt_decode_step(nt_decode_plan* p, void* stream) {
+  clear_error();
+  if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
+  const cudaStream_t st = as_stream(stream);
+  switch (p->launcher) {
+    case NT_LAUNCH_GRAPH:
+      NT_CUDA_TRY(cudaGraphLaunch(p->exec, st));
+      return NT_OK;
+    case NT_LAUNCH_STREAM:
+      return issue_launches(p, st);
+    default:
+      return persist_launch(p, st);
+  }
+}
+
+nt_status nt_decode_step_status(nt_decode_plan* p, nt_status* device_status) {
+  clear_error();
+  if (!p || !device_status) return set_error(NT_ERR_INVALID_ARG, "NULL argument");
+  StepCtrl c;
+  NT_CUDA_TRY(cudaMemcpy(&c, p->d_ctrl, sizeof c, cudaMemcpyDeviceToHost));
+  *device_status = c.error ? NT_ERR_TIMEOUT : NT_OK;
+  if (c.error) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "persistent step: a bounded wait ran out (code %u, CTA %u)", c.error,
+             c.error_cta);
+    set_error(NT_ERR_TIMEOUT, buf);
+  }
+  return NT_OK;
+}
+
+nt_status nt_decode_plan_reset(nt_decode_plan* p) {
+  clear_error();
+  if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
+  NT_CUDA_TRY(cudaDeviceSynchronize());
+  NT_CUDA_TRY(cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl)));
+  if (p->d_head_ws) NT_CUDA_TRY(cudaMemset(p->d_head_ws, 0, head_ws_bytes(p->B)));
+  p->launches = 0;
+  NT_CUDA_TRY(cudaDeviceSynchronize());
+  return NT_OK;
+}
+
+void nt_decode_plan_destroy(nt_decode_plan* p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  free_plan(p);
+}
+
+}  // extern "C"

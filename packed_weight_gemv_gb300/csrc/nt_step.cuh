@@ -1,0 +1,76 @@
+// nt_step.cuh -- the decode plan's host state and the persistent launcher's schedule.
+#pragma once
+
+#include <vector>
+
+#include "nt_kernels.cuh"
+
+namespace nt {
+
+constexpr int kProjPerLayer = 7;   // q, k, v, o, gate, up, down
+constexpr int kStepMaxBatch = 16;
+
+struct PlanStage {
+  int first_mat, n_mats;
+  int64_t prefix_off;   // into the plan's prefix array
+  int64_t total_tiles;
+};
+
+// Device control word of a plan: error word of the bounded waits and the grid-barrier
+// arrival counter of the persistent kernel.
+struct StepCtrl {
+  unsigned int error;      // 0 = fine; otherwise the code of the wait that ran out
+  unsigned int error_cta;
+  unsigned int arrive;     // grid-barrier arrivals (wraps; compared modulo 2^32)
+  unsigned int head_done;  // CTAs finished with the output projection's arg-max
+};
+
+// One contiguous run of work for one CTA of the persistent kernel.
+enum : int { kItemTernary = 0, kItemHead = 1 };
+enum : int { kFlagStage = 1 };  // a grid-wide barrier precedes this item (ordered mode)
+struct WorkItem {
+  int kind;      // kItemTernary (begin/end count tiles of mats[mat]) or kItemHead (rows)
+  int mat;
+  int flags;
+  int pad_;
+  int64_t begin, end;
+};
+
+}  // namespace nt
+
+struct nt_decode_plan {
+  int device = 0, sm_count = 0;
+  int n_layers = 0, B = 1, mode = 0, launcher = 0;
+  uint64_t timeout_ns = 0;
+  int test_fault = 0;
+  std::vector<nt::MatDesc> mats;
+  std::vector<nt::PlanStage> stages;
+  nt::MatDesc* d_mats = nullptr;
+  int64_t* d_prefix = nullptr;
+  nt::QuantJob* d_qjobs = nullptr;
+  int n_qjobs = 0;
+  bool has_head = false;
+  const int8_t* head_T = nullptr;
+  const float* head_s = nullptr;
+  int head_V = 0, head_K = 0;
+  const int8_t* head_q = nullptr;
+  const float* head_sx = nullptr;
+  float* head_logits = nullptr;
+  int32_t* head_argmax = nullptr;
+  nt::HeadWs* d_head_ws = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  nt::StepCtrl* d_ctrl = nullptr;
+  // persistent launcher
+  nt::WorkItem* d_sched = nullptr;  // items, then (grid + 1) int offsets
+  size_t sched_item_bytes = 0;
+  int grid = 0, n_barriers = 0;
+  size_t smem_bytes = 0;
+  int act_stride = 0;               // bytes of one activation buffer in shared memory
+  uint64_t launches = 0;
+};
+
+namespace nt {
+nt_status persist_prepare(nt_decode_plan* p);
+nt_status persist_launch(nt_decode_plan* p, cudaStream_t st);
+}  // namespace nt

@@ -1,0 +1,241 @@
+"""Thin ctypes binding of the C ABI in include/nt.h (libnt.so), with the same call names.
+
+Argument marshalling only: every call passes device pointers of torch tensors (and the
+current torch CUDA stream unless one is given) to the library, and raises :class:`NtError`
+when the library returns a non-zero status. There is no fallback of any kind: if
+``libnt.so`` has not been built, importing a call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libnt.so")
+
+NT_OK = 0
+NT_ERR_INVALID_ARG = 1
+NT_ERR_ALIGNMENT = 2
+NT_ERR_UNSUPPORTED = 3
+NT_ERR_CUDA = 4
+NT_ERR_TIMEOUT = 5
+NT_ERR_WORKSPACE = 6
+
+NT_LAYOUT_PLAIN = 0
+NT_LAYOUT_TILED = 1
+NT_STEP_INDEPENDENT = 0
+NT_STEP_ORDERED = 1
+NT_LAUNCH_PERSISTENT = 0
+NT_LAUNCH_GRAPH = 1
+NT_LAUNCH_STREAM = 2
+
+# Every symbol include/nt.h declares.
+EXPORTS = (
+    "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
+    "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
+    "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
+    "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
+    "nt_decode_plan_destroy",
+)
+
+
+class NtError(RuntimeError):
+    def __init__(self, status: int, call: str, detail: str):
+        self.status = status
+        super().__init__(f"{call}: status {status} ({detail})")
+
+
+class nt_proj(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("K", ctypes.c_int), ("w", ctypes.c_void_p),
+                ("s_w", ctypes.c_void_p), ("x", ctypes.c_void_p), ("q", ctypes.c_void_p),
+                ("s_x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class nt_decode_desc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("batch", ctypes.c_int),
+                ("proj", ctypes.POINTER(nt_proj)),
+                ("head_T", ctypes.c_void_p), ("head_s", ctypes.c_void_p),
+                ("head_V", ctypes.c_int), ("head_K", ctypes.c_int),
+                ("head_x", ctypes.c_void_p), ("head_q", ctypes.c_void_p),
+                ("head_sx", ctypes.c_void_p), ("head_logits", ctypes.c_void_p),
+                ("head_argmax", ctypes.c_void_p), ("mode", ctypes.c_int),
+                ("launcher", ctypes.c_int), ("timeout_ms", ctypes.c_double),
+                ("test_fault", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libnt.so (once). Raises if it is missing: there is no other implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        i, vp, sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        sig = {
+            "nt_abi_version": ([], i),
+            "nt_status_string": ([i], ctypes.c_char_p),
+            "nt_last_error_string": ([], ctypes.c_char_p),
+            "nt_device_check": ([ctypes.POINTER(i)], i),
+            "nt_quantize_act": ([vp, i, i, vp, vp, vp], i),
+            "nt_repack_size": ([i, i, ctypes.POINTER(sz)], i),
+            "nt_repack_ternary": ([vp, i, i, vp, vp, vp], i),
+            "nt_ternary_gemv": ([vp, i, vp, i, i, vp, vp, vp, vp, vp], i),
+            "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp], i),
+            "nt_int8_logits_workspace_size": ([i, i, i, ctypes.POINTER(sz)], i),
+            "nt_int8_logits_argmax": ([vp, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
+            "nt_decode_plan_create": ([ctypes.POINTER(nt_decode_desc), ctypes.POINTER(vp)], i),
+            "nt_decode_step": ([vp, vp], i),
+            "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
+            "nt_decode_plan_reset": ([vp], i),
+            "nt_decode_plan_destroy": ([vp], None),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int, call: str):
+    if status != NT_OK:
+        lib = load_library()
+        detail = lib.nt_last_error_string().decode() or lib.nt_status_string(status).decode()
+        raise NtError(status, call, detail)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def nt_abi_version() -> int:
+    return load_library().nt_abi_version()
+
+
+def nt_device_check() -> int:
+    n = ctypes.c_int(0)
+    _check(load_library().nt_device_check(ctypes.byref(n)), "nt_device_check")
+    return n.value
+
+
+def nt_quantize_act(x: torch.Tensor, q: torch.Tensor, s_x: torch.Tensor, stream=None):
+    B, K = (1, x.numel()) if x.dim() == 1 else x.shape
+    _check(load_library().nt_quantize_act(_ptr(x), B, K, _ptr(q), _ptr(s_x), _stream(stream)),
+           "nt_quantize_act")
+
+
+def nt_repack_size(N: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().nt_repack_size(N, K, ctypes.byref(n)), "nt_repack_size")
+    return n.value
+
+
+def nt_repack_ternary(w_plain: torch.Tensor, N: int, K: int, w_tiled: torch.Tensor,
+                      n_invalid: Optional[torch.Tensor] = None, stream=None):
+    _check(load_library().nt_repack_ternary(_ptr(w_plain), N, K, _ptr(w_tiled), _ptr(n_invalid),
+                                            _stream(stream)), "nt_repack_ternary")
+
+
+def nt_ternary_gemv(w: torch.Tensor, layout: int, s_w: torch.Tensor, N: int, K: int,
+                    q: torch.Tensor, s_x: torch.Tensor, y: torch.Tensor,
+                    acc: Optional[torch.Tensor] = None, stream=None):
+    _check(load_library().nt_ternary_gemv(_ptr(w), layout, _ptr(s_w), N, K, _ptr(q), _ptr(s_x),
+                                          _ptr(y), _ptr(acc), _stream(stream)), "nt_ternary_gemv")
+
+
+def nt_ternary_gemm(w: torch.Tensor, layout: int, s_w: torch.Tensor, N: int, K: int,
+                    q: torch.Tensor, s_x: torch.Tensor, B: int, y: torch.Tensor,
+                    acc: Optional[torch.Tensor] = None, stream=None):
+    _check(load_library().nt_ternary_gemm(_ptr(w), layout, _ptr(s_w), N, K, _ptr(q), _ptr(s_x), B,
+                                          _ptr(y), _ptr(acc), _stream(stream)), "nt_ternary_gemm")
+
+
+def nt_int8_logits_workspace_size(V: int, K: int, B: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().nt_int8_logits_workspace_size(V, K, B, ctypes.byref(n)),
+           "nt_int8_logits_workspace_size")
+    return n.value
+
+
+def nt_int8_logits_argmax(T: torch.Tensor, s_T: torch.Tensor, V: int, K: int, q: torch.Tensor,
+                          s_x: torch.Tensor, B: int, logits: Optional[torch.Tensor],
+                          argmax: torch.Tensor, ws: torch.Tensor, stream=None):
+    _check(load_library().nt_int8_logits_argmax(
+        _ptr(T), _ptr(s_T), V, K, _ptr(q), _ptr(s_x), B, _ptr(logits), _ptr(argmax), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)), "nt_int8_logits_argmax")
+
+
+class DecodePlan:
+    """Owns an nt_decode_plan and keeps every tensor it names alive.
+
+    ``projs`` is a sequence of dicts with keys N, K, w, s_w, q, s_x, y and optionally x
+    (torch tensors on the current device), n_layers * 7 of them in q, k, v, o, gate, up, down
+    order per layer. ``head`` is None or a dict with T, s, V, K, q, sx, argmax and optionally
+    x and logits.
+    """
+
+    def __init__(self, n_layers: int, batch: int, projs: Sequence[dict], head: Optional[dict],
+                 mode: int = NT_STEP_INDEPENDENT, launcher: int = NT_LAUNCH_PERSISTENT,
+                 timeout_ms: float = 0.0, test_fault: int = 0):
+        lib = load_library()
+        self._keep = [projs, head]
+        arr = (nt_proj * len(projs))()
+        for i, p in enumerate(projs):
+            arr[i] = nt_proj(p["N"], p["K"], p["w"].data_ptr(), p["s_w"].data_ptr(),
+                             p["x"].data_ptr() if p.get("x") is not None else None,
+                             p["q"].data_ptr(), p["s_x"].data_ptr(), p["y"].data_ptr())
+        d = nt_decode_desc()
+        d.n_layers, d.batch, d.proj = n_layers, batch, ctypes.cast(arr, ctypes.POINTER(nt_proj))
+        if head is not None:
+            d.head_T, d.head_s = head["T"].data_ptr(), head["s"].data_ptr()
+            d.head_V, d.head_K = head["V"], head["K"]
+            d.head_x = head["x"].data_ptr() if head.get("x") is not None else None
+            d.head_q, d.head_sx = head["q"].data_ptr(), head["sx"].data_ptr()
+            d.head_logits = head["logits"].data_ptr() if head.get("logits") is not None else None
+            d.head_argmax = head["argmax"].data_ptr()
+        d.mode, d.launcher, d.timeout_ms, d.test_fault = mode, launcher, timeout_ms, test_fault
+        self._arr = arr
+        handle = ctypes.c_void_p(None)
+        _check(lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(handle)),
+               "nt_decode_plan_create")
+        self._h = handle
+
+    def nt_decode_step(self, stream=None):
+        _check(load_library().nt_decode_step(self._h, _stream(stream)), "nt_decode_step")
+
+    def nt_decode_step_status(self) -> int:
+        s = ctypes.c_int(0)
+        _check(load_library().nt_decode_step_status(self._h, ctypes.byref(s)),
+               "nt_decode_step_status")
+        return s.value
+
+    def nt_decode_plan_reset(self):
+        _check(load_library().nt_decode_plan_reset(self._h), "nt_decode_plan_reset")
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            load_library().nt_decode_plan_destroy(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

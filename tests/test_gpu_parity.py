@@ -1,0 +1,258 @@
+"""GPU parity: every C ABI call against the CPU oracle, element by element, on the same seeded
+inputs. Integer results (int8 codes, int32 accumulators, arg-max indices, repacked bytes) must
+match bit for bit; fp32 outputs within a relative error of 1e-6."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from packed_weight_gemv_gb300 import nt
+from synth import workloads as wl
+from tests._gpu import DEV, assert_close, dev, host, plan_inputs, tiled
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def device():
+    torch.cuda.set_device(DEV)
+    nt.nt_device_check()
+
+
+# ---- quantization ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,K,kind", [(1, 512, "normal"), (3, 4096, "normal"), (2, 12288, "normal"),
+                                      (1, 17, "normal"), (5, 1, "normal"), (2, 64, "zero"),
+                                      (2, 256, "constant"), (1, 4096, "tiny"), (4, 1000, "heavy")])
+def test_quantize(B, K, kind):
+    x = synth.normal(B * K, 3, 100 + K).reshape(B, K)
+    if kind == "zero":
+        x[:] = 0
+    elif kind == "constant":
+        x[:] = -2.5
+    elif kind == "tiny":
+        x *= np.float32(1e-30)
+    elif kind == "heavy":
+        x = (x ** 3).astype(np.float32)
+    q = torch.empty((B, K), dtype=torch.int8, device=DEV)
+    s = torch.empty(B, dtype=torch.float32, device=DEV)
+    nt.nt_quantize_act(dev(x), q, s)
+    oq, os_ = oracle.quantize(x)
+    assert np.array_equal(host(q), oq)
+    assert np.array_equal(host(s), os_)
+
+
+# ---- load-time repack ------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(1536, 512), (5, 48), (7, 528), (13, 1040), (1024, 4096), (4, 12288)])
+def test_repack(N, K):
+    w = synth.ternary_plain(N, K, 4, N + K)
+    got = host(tiled(w, N, K))
+    assert np.array_equal(got, oracle.repack_tiled(w, N, K))
+
+
+def test_repack_counts_invalid_fields():
+    N, K = 9, 64
+    w = synth.ternary_plain(N, K, 5, 1)
+    w[0, 0] = (w[0, 0] & ~np.uint32(0x3)) | np.uint32(0x2)        # field 0 of row 0 -> 10
+    w[8, 3] = (w[8, 3] & ~np.uint32(0xC0000000)) | np.uint32(0x80000000)  # field 15
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = torch.empty(nt.nt_repack_size(N, K), dtype=torch.uint8, device=DEV)
+    nt.nt_repack_ternary(dev(w), N, K, out, cnt)
+    assert int(cnt.item()) == oracle.count_invalid(w) == 2
+
+
+# ---- ternary projection ----------------------------------------------------------------
+
+SHAPES = [(1536, 512), (5, 48), (7, 528), (33, 1040), (4096, 4096), (1024, 12288), (1, 16)]
+
+
+@pytest.mark.parametrize("layout", [nt.NT_LAYOUT_PLAIN, nt.NT_LAYOUT_TILED])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_gemv(layout, N, K):
+    p = wl.projection(8, 0, 0, N, K, 1, seed=1)
+    q, s = oracle.quantize(p.x)
+    acc, y, _ = oracle.gemv(p.w_plain, p.s_w, N, K, q[0], s)
+    w = dev(p.w_plain) if layout == nt.NT_LAYOUT_PLAIN else tiled(p.w_plain, N, K)
+    gy = torch.full((N,), float("nan"), device=DEV)
+    gacc = torch.empty(N, dtype=torch.int32, device=DEV)
+    nt.nt_ternary_gemv(w, layout, dev(p.s_w), N, K, dev(q), dev(s), gy, gacc)
+    assert np.array_equal(host(gacc), acc)
+    assert_close(host(gy), y, f"gemv {N}x{K}")
+
+
+def test_single_gemv_workload():
+    # The single ternary GEMV: W 1536 x 512, seed 0, batch 1, through both layouts.
+    p = wl.single_gemv()
+    q, s = oracle.quantize(p.x)
+    acc, y, _ = oracle.gemv(p.w_plain, p.s_w, p.N, p.K, q[0], s)
+    for layout in (nt.NT_LAYOUT_PLAIN, nt.NT_LAYOUT_TILED):
+        w = dev(p.w_plain) if layout == nt.NT_LAYOUT_PLAIN else tiled(p.w_plain, p.N, p.K)
+        gq = torch.empty((1, p.K), dtype=torch.int8, device=DEV)
+        gs = torch.empty(1, dtype=torch.float32, device=DEV)
+        nt.nt_quantize_act(dev(p.x), gq, gs)
+        gy = torch.empty(p.N, device=DEV)
+        gacc = torch.empty(p.N, dtype=torch.int32, device=DEV)
+        nt.nt_ternary_gemv(w, layout, dev(p.s_w), p.N, p.K, gq, gs, gy, gacc)
+        assert np.array_equal(host(gacc), acc)
+        assert np.array_equal(host(gy), y)  # the fp32 epilogue order is fixed, so bit-equal
+
+
+def test_gemv_closed_forms():
+    N, K = 8, 512
+    q = synth.int8_uniform(K, 9, 9)
+    sq = int(q.astype(np.int64).sum())
+    for word, expect in [(0, 0), (0x55555555, sq), (0xFFFFFFFF, -sq)]:
+        w = np.full((N, K // 16), word, dtype=np.uint32)
+        for layout in (nt.NT_LAYOUT_PLAIN, nt.NT_LAYOUT_TILED):
+            ww = dev(w) if layout == nt.NT_LAYOUT_PLAIN else tiled(w, N, K)
+            gy = torch.empty(N, device=DEV)
+            gacc = torch.empty(N, dtype=torch.int32, device=DEV)
+            nt.nt_ternary_gemv(ww, layout, dev(np.ones(N, np.float32)), N, K, dev(q),
+                               dev(np.ones(1, np.float32)), gy, gacc)
+            assert (host(gacc) == expect).all()
+
+
+@pytest.mark.parametrize("layout", [nt.NT_LAYOUT_PLAIN, nt.NT_LAYOUT_TILED])
+@pytest.mark.parametrize("B", [2, 3, 16, 17])
+def test_gemm(layout, B):
+    N, K = 260, 1024
+    p = wl.projection(8, 1, B, N, K, B, seed=2)
+    q, s = oracle.quantize(p.x)
+    acc, y, _ = oracle.gemm(p.w_plain, p.s_w, N, K, q, s)
+    w = dev(p.w_plain) if layout == nt.NT_LAYOUT_PLAIN else tiled(p.w_plain, N, K)
+    gy = torch.empty((B, N), device=DEV)
+    gacc = torch.empty((B, N), dtype=torch.int32, device=DEV)
+    nt.nt_ternary_gemm(w, layout, dev(p.s_w), N, K, dev(q), dev(s), B, gy, gacc)
+    assert np.array_equal(host(gacc), acc)
+    assert_close(host(gy), y, f"gemm B={B}")
+
+
+# ---- int8 output projection ------------------------------------------------------------
+
+def _head_call(T, s_T, V, K, q, s, B, ws=None):
+    logits = torch.full((B, V), float("nan"), device=DEV)
+    am = torch.full((B,), -1, dtype=torch.int32, device=DEV)
+    if ws is None:
+        ws = torch.zeros(nt.nt_int8_logits_workspace_size(V, K, B), dtype=torch.uint8, device=DEV)
+    nt.nt_int8_logits_argmax(dev(T), dev(s_T), V, K, dev(q), dev(s), B, logits, am, ws)
+    return host(logits), host(am), ws
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_head_small(B):
+    h = wl.head(V=5000, K=4096, B=B, seed=3)
+    q, s = oracle.quantize(h.x)
+    logits, am, _ = oracle.logits_argmax(h.T, h.s_T, h.V, h.K, q, s)
+    gl, ga, ws = _head_call(h.T, h.s_T, h.V, h.K, q, s, B)
+    assert_close(gl, logits, "head logits")
+    assert np.array_equal(ga, am)
+    gl2, ga2, _ = _head_call(h.T, h.s_T, h.V, h.K, q, s, B, ws)  # workspace reused as left
+    assert np.array_equal(ga2, am) and np.array_equal(gl2, gl)
+
+
+@pytest.mark.parametrize("plant", [0, 4999, 511, 512, 2048, 2049])
+def test_head_planted_max_and_ties(plant):
+    V, K = 5000, 256
+    T = (synth.int8_uniform(V * K, 6, 7).reshape(V, K) // 4).astype(np.int8)
+    T[plant] = 127
+    tie = (plant * 7 + 13) % V
+    T[tie] = 127
+    q = np.full(K, 1, dtype=np.int8)
+    s_T = np.ones(V, dtype=np.float32)
+    s = np.ones(1, dtype=np.float32)
+    logits, am, _ = oracle.logits_argmax(T, s_T, V, K, q, s)
+    assert am[0] == min(plant, tie)
+    _, ga, _ = _head_call(T, s_T, V, K, q, s, 1)
+    assert ga[0] == am[0]
+
+
+def test_head_full_table():
+    # The int8 output projection at its full size: 151,936 x 4,096, batch 1.
+    h = wl.head()
+    q, s = oracle.quantize(h.x)
+    logits, am, _ = oracle.logits_argmax(h.T, h.s_T, h.V, h.K, q, s)
+    gl, ga, _ = _head_call(h.T, h.s_T, h.V, h.K, q, s, 1)
+    assert_close(gl, logits, "head full")
+    assert ga[0] == am[0]
+
+
+# ---- decode step -----------------------------------------------------------------------
+
+SMALL = {"q": (512, 512), "k": (128, 512), "v": (128, 512), "o": (512, 512),
+         "gate": (1536, 512), "up": (1536, 512), "down": (512, 1536)}
+
+
+def _check_step(projs, head, dp, hd, B=1):
+    for p, d in zip(projs, dp):
+        q, s = oracle.quantize(p.x[:B])
+        assert np.array_equal(host(d["q"]), q), p.name
+        assert np.array_equal(host(d["s_x"]), s), p.name
+        _, y, _ = oracle.gemm(p.w_plain, p.s_w, p.N, p.K, q, s)
+        assert_close(host(d["y"]), y, p.name)
+    if head is not None:
+        q, s = oracle.quantize(head.x[:B])
+        logits, am, _ = oracle.logits_argmax(head.T, head.s_T, head.V, head.K, q, s)
+        assert_close(host(hd["logits"]), logits, "head")
+        assert np.array_equal(host(hd["argmax"]), am)
+
+
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_PERSISTENT, nt.NT_LAUNCH_GRAPH, nt.NT_LAUNCH_STREAM])
+@pytest.mark.parametrize("mode", [nt.NT_STEP_INDEPENDENT, nt.NT_STEP_ORDERED])
+def test_decode_step_small(launcher, mode):
+    projs = wl.decoder_projections(2, SMALL, seed=4, workload=10)
+    head = wl.head(V=3001, K=512, seed=4, workload=10)
+    dp, hd = plan_inputs(projs, head)
+    plan = nt.DecodePlan(2, 1, dp, hd, mode, launcher)
+    for _ in range(3):  # repeated steps reuse the plan's counters and workspace
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, head, dp, hd)
+    plan.close()
+
+
+@pytest.mark.parametrize("B", [2, 4])
+def test_decode_step_batched_graph(B):
+    projs = wl.decoder_projections(1, SMALL, B=B, seed=5, workload=11)
+    head = wl.head(V=2000, K=512, B=B, seed=5, workload=11)
+    dp, hd = plan_inputs(projs, head, B=B)
+    plan = nt.DecodePlan(1, B, dp, hd, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_GRAPH)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    _check_step(projs, head, dp, hd, B=B)
+    plan.close()
+
+
+def test_decode_step_prequantized_inputs():
+    projs = wl.decoder_projections(1, SMALL, seed=6, workload=12)
+    dp, _ = plan_inputs(projs, None, quantize_in_step=False)
+    for p, d in zip(projs, dp):
+        q, s = oracle.quantize(p.x)
+        d["q"].copy_(dev(q))
+        d["s_x"].copy_(dev(s))
+    plan = nt.DecodePlan(1, 1, dp, None, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    _check_step(projs, None, dp, None)
+    plan.close()
+
+
+def test_persistent_timeout_is_reported_and_recoverable():
+    # A grid barrier that waits for one arrival more than the grid makes runs out after
+    # timeout_ms; the step reports NT_ERR_TIMEOUT and the context stays usable.
+    projs = wl.decoder_projections(1, SMALL, seed=7, workload=13)
+    dp, _ = plan_inputs(projs, None)
+    plan = nt.DecodePlan(1, 1, dp, None, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_PERSISTENT,
+                         timeout_ms=20.0, test_fault=1)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_ERR_TIMEOUT
+    plan.close()
+    good = nt.DecodePlan(1, 1, dp, None, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_PERSISTENT)
+    good.nt_decode_step()
+    torch.cuda.synchronize()
+    assert good.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, None, dp, None)
+    good.close()
