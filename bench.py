@@ -41,14 +41,14 @@ KERNEL_SOURCES = ["packed_weight_gemv_gb300/csrc/nt_persist.cu",
                   "packed_weight_gemv_gb300/csrc/nt_kernels.cuh"]
 
 
-def step_bytes(B: int = 1) -> int:
+def step_bytes(B: int = 1, n_layers: int = wl.DECODER_8B_LAYERS) -> int:
     """Algorithmic bytes of one decode token: the projection stream (packed trits, row scales,
     int8 activations, fp32 outputs, activation scales), the fp32 inputs the step quantizes
     (read once, int8 written once -- counted in the activations), and the output projection
     (table, row scales, hidden, logits, arg-max)."""
-    fp32_inputs = 4 * B * sum(K for (_, K) in wl.DECODER_8B.values()) * wl.DECODER_8B_LAYERS
+    fp32_inputs = 4 * B * sum(K for (_, K) in wl.DECODER_8B.values()) * n_layers
     fp32_inputs += 4 * B * wl.HEAD_K
-    return wl.packed_bytes_per_token(B=B) + wl.head_bytes(B=B) + fp32_inputs
+    return wl.packed_bytes_per_token(n_layers=n_layers, B=B) + wl.head_bytes(B=B) + fp32_inputs
 
 
 def kernel_source_hash() -> str:
@@ -136,9 +136,9 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------------------
 
-def build_inputs(torch, nt, dev):
+def build_inputs(torch, nt, dev, n_layers=wl.DECODER_8B_LAYERS):
     """Device-resident model: tiled weights, scales; fp32 inputs in one buffer."""
-    projs = wl.decoder_projections()
+    projs = wl.decoder_projections(n_layers)
     head = wl.head()
     K_total = sum(p.K for p in projs) + head.K
     x_all = torch.empty(K_total, dtype=torch.float32, device=dev)
@@ -240,15 +240,16 @@ def run_ours(args, rank, world):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     nt.nt_device_check()
-    projs, head, dp, hd, x_all = build_inputs(torch, nt, dev)
+    L = args.layers
+    projs, head, dp, hd, x_all = build_inputs(torch, nt, dev, L)
     stream = torch.cuda.current_stream()
-    plan = nt.DecodePlan(36, 1, dp, hd, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+    plan = nt.DecodePlan(L, 1, dp, hd, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
     for _ in range(args.warmup):
         plan.nt_decode_step(stream)
     torch.cuda.synchronize()
     if plan.nt_decode_step_status() != nt.NT_OK:
         raise RuntimeError("persistent step reported a timeout during warm-up")
-    parity = parity_gate(oracle, projs, head, dp, hd) if rank == 0 else "pass"
+    parity = parity_gate(oracle, projs, head, dp, hd, layers=(0, L - 1)) if rank == 0 else "pass"
     if parity != "pass":
         raise RuntimeError(f"parity gate failed: {parity}")
 
@@ -299,17 +300,17 @@ def run_ours(args, rank, world):
                                  ("independent_graph", nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_GRAPH),
                                  ("ordered_graph", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_GRAPH),
                                  ("ordered_stream", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_STREAM)]:
-        pl = nt.DecodePlan(36, 1, dp, hd, mode, launcher)
+        pl = nt.DecodePlan(L, 1, dp, hd, mode, launcher)
         for _ in range(3):
             pl.nt_decode_step(stream)
         extra[name + "_us_per_token"] = round(time_steps(torch, pl, n_extra, stream) / n_extra, 2)
         if pl.nt_decode_step_status() != nt.NT_OK:
             raise RuntimeError(f"{name}: step reported a timeout")
         pl.close()
-    parity_after = parity_gate(oracle, projs, head, dp, hd, layers=(17,)) if rank == 0 else "pass"
+    parity_after = parity_gate(oracle, projs, head, dp, hd, layers=(L // 2,)) if rank == 0 else "pass"
 
     peak, peak_kind = measured_peak()
-    nbytes = step_bytes()
+    nbytes = step_bytes(n_layers=L)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     cpu = cpu_baseline(oracle) if (rank == 0 and world == 1) else None
     line = {
@@ -325,7 +326,9 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "int8 x ternary -> int32, fp32 epilogue",
         "data": "synthetic (seeded SplitMix64; workload shapes and value mixes)",
-        "config": {"workload": WORKLOAD, "batch": 1, "mode": "independent",
+        "config": {"workload": WORKLOAD if L == wl.DECODER_8B_LAYERS else
+                   WORKLOAD.replace("36 layers", f"{L} of 36 layers (profiling case)"),
+                   "batch": 1, "mode": "independent",
                    "launcher": "persistent", "bytes_per_step": nbytes,
                    "l2": "inputs larger than L2 (2.37 GB streamed per step vs 129 MB L2)",
                    "parallelism": f"replicas x{world}"},
@@ -410,6 +413,9 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=wl.DECODER_8B_LAYERS,
+                    help="decoder layers in the step (36 = the 8B-shaped workload; fewer only "
+                         "for small profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

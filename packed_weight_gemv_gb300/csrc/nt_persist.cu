@@ -7,10 +7,10 @@
 // do not depend on activations, so the producer warp of every CTA keeps its shared-memory
 // ring full across stage boundaries while the consumer warps wait.
 //
-// CTA layout (one CTA per SM): warps 0..7 consume, warp 8 produces.
-//   producer (one thread): walks the CTA's schedule and issues one cp.async.bulk per chunk
-//     (<= 4 KB of a tile or of an output-table row) into the ring of the consumer warp that
-//     owns the unit (units are dealt round-robin), completing on that slot's mbarrier;
+// CTA layout (one CTA per SM): warps 0..15 consume, warp 16 produces.
+//   producer (lane w feeds consumer warp w): walks the CTA's schedule and issues one
+//     cp.async.bulk per chunk (<= 4 KB of a tile or of an output-table row) of the units warp
+//     w owns (units are dealt round-robin) into w's ring, completing on the slot's mbarrier;
 //   consumers: wait for a chunk, decode + dp4a it against the activation held in shared
 //     memory, release the slot; per unit (4 rows of a tiled matrix, or one output-table row)
 //     a warp reduction and the fp32 epilogue.
@@ -30,10 +30,10 @@
 namespace nt {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreadsP = kConsumerThreads + 32;
-constexpr int kSlots = 6;
+constexpr int kSlots = 3;
 constexpr int kSlotBytes = 4096;
 constexpr int kRingBytes = kConsumerWarps * kSlots * kSlotBytes;  // 192 KB
 constexpr int kBars = kConsumerWarps * kSlots;                     // full (and empty) barriers
@@ -179,58 +179,51 @@ __device__ __forceinline__ void unit_geometry(const PersistParams& P, const Work
 }
 
 // ---- producer ------------------------------------------------------------------------
+// Lane w of the producer warp feeds consumer warp w's ring: it walks the CTA's schedule and
+// issues the chunks of the units that warp w owns (units are dealt round-robin), so the 8
+// lanes issue copies independently of each other.
 __device__ void producer(const PersistParams& P, const WorkItem* items, int n_items, uint8_t* ring,
-                         uint32_t full0, uint32_t empty0, volatile int* s_abort) {
-  uint32_t cnt[kConsumerWarps];
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) cnt[w] = 0;
+                         uint32_t full0, uint32_t empty0, volatile int* s_abort, int w) {
   const uint64_t pol = evict_first_policy();
-  const uint32_t ring0 = smem_addr(ring);
-  uint32_t seq = 0;
+  const uint32_t ring_w = smem_addr(ring) + (uint32_t)w * kSlots * kSlotBytes;
+  const uint32_t full_w = full0 + 8u * w * kSlots, empty_w = empty0 + 8u * w * kSlots;
+  uint32_t cnt = 0, seq = 0;
   bool ok = true;
   for (int i = 0; i < n_items && ok; ++i) {
     const WorkItem it = items[i];
     const uint8_t* base;
     int ub;
     unit_geometry(P, it, base, ub);
-    for (int64_t u = it.begin; u < it.end && ok; ++u, ++seq) {
-      const int w = (int)(seq % kConsumerWarps);
+    const int64_t first = it.begin + (int64_t)((w - (int)(seq % kConsumerWarps) + kConsumerWarps) % kConsumerWarps);
+    for (int64_t u = first; u < it.end && ok; u += kConsumerWarps) {
       const uint8_t* src = base + u * (int64_t)ub;
       for (int off = 0; off < ub; off += kSlotBytes) {
         const uint32_t bytes = (uint32_t)min(kSlotBytes, ub - off);
-        uint32_t c = 0;
-#pragma unroll
-        for (int x = 0; x < kConsumerWarps; ++x) if (x == w) c = cnt[x];
-        const uint32_t slot = c % kSlots, phase = (c / kSlots) & 1u;
-        const uint32_t idx = (uint32_t)w * kSlots + slot;
-        if (!wait_phase(empty0 + 8 * idx, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
+        const uint32_t slot = cnt % kSlots, phase = (cnt / kSlots) & 1u;
+        if (!wait_phase(empty_w + 8 * slot, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
           if (!*s_abort) record_error(P.ctrl, kErrEmptyWait, s_abort);
           ok = false;
           break;
         }
-        mbar_expect_tx(full0 + 8 * idx, bytes);
-        bulk_load(ring0 + idx * kSlotBytes, src + off, bytes, full0 + 8 * idx, pol);
-#pragma unroll
-        for (int x = 0; x < kConsumerWarps; ++x) if (x == w) cnt[x] = c + 1;
+        mbar_expect_tx(full_w + 8 * slot, bytes);
+        bulk_load(ring_w + slot * kSlotBytes, src + off, bytes, full_w + 8 * slot, pol);
+        ++cnt;
       }
     }
+    seq += (uint32_t)(it.end - it.begin);
   }
   // Drain: every slot's last copy must have landed before this thread (and so the CTA)
   // may exit, whatever happened to the consumers.
-#pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) {
-    for (uint32_t s = 0; s < kSlots; ++s) {
-      if (cnt[w] <= s) continue;
-      const uint32_t last = (cnt[w] - 1 - s) / kSlots * kSlots + s;
-      const uint32_t idx = (uint32_t)w * kSlots + s;
-      const uint32_t bar = full0 + 8 * idx;
-      if (mbar_try_wait(bar, (last / kSlots) & 1u)) continue;
-      const uint64_t deadline = globaltimer_ns() + P.timeout_ns;
-      while (!mbar_try_wait(bar, (last / kSlots) & 1u)) {
-        if (globaltimer_ns() > deadline) {
-          record_error(P.ctrl, kErrDrain, s_abort);
-          break;
-        }
+  for (uint32_t s = 0; s < kSlots; ++s) {
+    if (cnt <= s) continue;
+    const uint32_t last = (cnt - 1 - s) / kSlots * kSlots + s;
+    const uint32_t bar = full_w + 8 * s;
+    if (mbar_try_wait(bar, (last / kSlots) & 1u)) continue;
+    const uint64_t deadline = globaltimer_ns() + P.timeout_ns;
+    while (!mbar_try_wait(bar, (last / kSlots) & 1u)) {
+      if (globaltimer_ns() > deadline) {
+        record_error(P.ctrl, kErrDrain, s_abort);
+        break;
       }
     }
   }
@@ -317,66 +310,86 @@ __device__ __forceinline__ bool wait_chunk(uint32_t bar, uint32_t phase, const P
   return ok;
 }
 
-// One tile (4 rows) of a tiled ternary matrix.
-__device__ bool consume_tile(const PersistParams& P, const MatDesc& m, int64_t tile, const uint8_t* act,
-                             uint8_t* ring, uint32_t full0, uint32_t empty0, ConsumerState& st,
-                             int cw, int lane, volatile int* s_abort) {
+// 16 bytes of one lane in one 512-byte piece: 4 rows x 16 trits against 16 activations.
+__device__ __forceinline__ void tile_piece(const uint8_t* sb, const uint8_t* ab, int& a0, int& a1,
+                                           int& a2, int& a3) {
+  const uint4 wv = lds128(sb);
+  const uint4 a = lds128(ab);
+  a0 = tiled_word_dot(wv.x, a.x, a.y, a.z, a.w, a0);
+  a1 = tiled_word_dot(wv.y, a.x, a.y, a.z, a.w, a1);
+  a2 = tiled_word_dot(wv.z, a.x, a.y, a.z, a.w, a2);
+  a3 = tiled_word_dot(wv.w, a.x, a.y, a.z, a.w, a3);
+}
+
+// One tile (4 rows) of a tiled ternary matrix. The row scale is loaded before the first
+// chunk so its latency hides behind the chunk work; sx is the item's activation scale.
+__device__ bool consume_tile(const PersistParams& P, const MatDesc& m, float sx, int64_t tile,
+                             const uint8_t* act, uint8_t* ring, uint32_t full0, uint32_t empty0,
+                             ConsumerState& st, int cw, int lane, volatile int* s_abort) {
+  constexpr int kPieces = kSlotBytes / 512;
   const int pieces = (int)(padded_k(m.K) / 512);
+  const int64_t n = tile * 4 + (lane >> 3);
+  const float sw = ((lane & 7) == 0 && n < m.N) ? __ldg(m.s_w + n) : 0.0f;
   int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (int p0 = 0; p0 < pieces; p0 += kSlotBytes / 512) {
-    const int np = min(kSlotBytes / 512, pieces - p0);
+  for (int p0 = 0; p0 < pieces; p0 += kPieces) {
     const uint32_t slot = st.cnt % kSlots, phase = (st.cnt / kSlots) & 1u;
     const uint32_t idx = (uint32_t)cw * kSlots + slot;
     if (!wait_chunk(full0 + 8 * idx, phase, P, lane, s_abort)) return false;
     const uint8_t* sb = ring + idx * kSlotBytes + lane * 16;
     const uint8_t* ab = act + (p0 * 32 + lane) * 16;
-#pragma unroll 8
-    for (int p = 0; p < np; ++p) {
-      const uint4 wv = lds128(sb + p * 512);
-      const uint4 a = lds128(ab + p * 512);
-      a0 = tiled_word_dot(wv.x, a.x, a.y, a.z, a.w, a0);
-      a1 = tiled_word_dot(wv.y, a.x, a.y, a.z, a.w, a1);
-      a2 = tiled_word_dot(wv.z, a.x, a.y, a.z, a.w, a2);
-      a3 = tiled_word_dot(wv.w, a.x, a.y, a.z, a.w, a3);
+    if (pieces - p0 >= kPieces) {
+#pragma unroll
+      for (int p = 0; p < kPieces; ++p) tile_piece(sb + p * 512, ab + p * 512, a0, a1, a2, a3);
+    } else {
+      for (int p = 0; p < pieces - p0; ++p) tile_piece(sb + p * 512, ab + p * 512, a0, a1, a2, a3);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * idx);
     ++st.cnt;
   }
   const int total = warp_sum4(a0, a1, a2, a3, lane);
-  if ((lane & 7) == 0) {
-    const int64_t n = tile * 4 + (lane >> 3);
-    if (n < m.N) m.y[n] = scale_out(total, m.s_w[n], m.s_x[0]);
-  }
+  if ((lane & 7) == 0 && n < m.N) m.y[n] = scale_out(total, sw, sx);
   return true;
 }
 
 // One row of the int8 output table.
-__device__ bool consume_head_row(const PersistParams& P, int64_t v, const uint8_t* act, uint8_t* ring,
-                                 uint32_t full0, uint32_t empty0, ConsumerState& st, int cw, int lane,
-                                 volatile int* s_abort) {
-  int acc = 0;
+__device__ __forceinline__ void row_piece(const uint8_t* sb, const uint8_t* ab, int& acc) {
+  const uint4 t = lds128(sb);
+  const uint4 a = lds128(ab);
+  acc = dp4a(t.x, a.x, acc);
+  acc = dp4a(t.y, a.y, acc);
+  acc = dp4a(t.z, a.z, acc);
+  acc = dp4a(t.w, a.w, acc);
+}
+
+__device__ bool consume_head_row(const PersistParams& P, float sx, int64_t v, const uint8_t* act,
+                                 uint8_t* ring, uint32_t full0, uint32_t empty0, ConsumerState& st,
+                                 int cw, int lane, volatile int* s_abort) {
+  const float sv = lane == 0 ? __ldg(P.head_s + v) : 0.0f;
+  int acc = 0, acc2 = 0;
   for (int off = 0; off < P.head_K; off += kSlotBytes) {
     const int cb = min(kSlotBytes, P.head_K - off);
     const uint32_t slot = st.cnt % kSlots, phase = (st.cnt / kSlots) & 1u;
     const uint32_t idx = (uint32_t)cw * kSlots + slot;
     if (!wait_chunk(full0 + 8 * idx, phase, P, lane, s_abort)) return false;
-    const uint8_t* sb = ring + idx * kSlotBytes;
-    for (int o = lane * 16; o < cb; o += 512) {
-      const uint4 t = lds128(sb + o);
-      const uint4 a = lds128(act + off + o);
-      acc = dp4a(t.x, a.x, acc);
-      acc = dp4a(t.y, a.y, acc);
-      acc = dp4a(t.z, a.z, acc);
-      acc = dp4a(t.w, a.w, acc);
+    const uint8_t* sb = ring + idx * kSlotBytes + lane * 16;
+    const uint8_t* ab = act + off + lane * 16;
+    if (cb == kSlotBytes) {
+#pragma unroll
+      for (int o = 0; o < kSlotBytes; o += 1024) {
+        row_piece(sb + o, ab + o, acc);
+        row_piece(sb + o + 512, ab + o + 512, acc2);
+      }
+    } else {
+      for (int o = 0; o + lane * 16 < cb; o += 512) row_piece(sb + o, ab + o, acc);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * idx);
     ++st.cnt;
   }
-  const int total = warp_sum(acc);
+  const int total = warp_sum(acc + acc2);
   if (lane == 0) {
-    const float lg = scale_out(total, P.head_s[v], P.head_sx[0]);
+    const float lg = scale_out(total, sv, sx);
     if (P.head_logits) P.head_logits[v] = lg;
     if (lg > st.best_v) { st.best_v = lg; st.best_i = (int)v; }  // rows rise per warp
   }
@@ -412,7 +425,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) persist_kernel(const PersistPara
   const WorkItem* items = P.items + i0;
 
   if (warp == kConsumerWarps) {
-    if (lane == 0) producer(P, items, n_items, ring, full0, empty0, s_abort);
+    if (lane < kConsumerWarps) producer(P, items, n_items, ring, full0, empty0, s_abort, lane);
     return;
   }
 
@@ -452,16 +465,20 @@ __global__ void __launch_bounds__(kThreadsP, 1) persist_kernel(const PersistPara
       prefetched = true;
     }
     // The abort flag is read by lane 0 and broadcast, so the whole warp takes one branch.
+    const int64_t first = it.begin + (int64_t)((cw - (int)(st.seq % kConsumerWarps) + kConsumerWarps) % kConsumerWarps);
     if (it.kind == kItemTernary) {
       const MatDesc m = P.mats[it.mat];
-      for (int64_t u = it.begin; u < it.end; ++u, ++st.seq)
-        if ((int)(st.seq % kConsumerWarps) == cw && !__shfl_sync(0xffffffffu, *s_abort, 0))
-          consume_tile(P, m, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
+      const float sx = __ldcg(m.s_x);
+      for (int64_t u = first; u < it.end; u += kConsumerWarps)
+        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+          consume_tile(P, m, sx, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
     } else {
-      for (int64_t u = it.begin; u < it.end; ++u, ++st.seq)
-        if ((int)(st.seq % kConsumerWarps) == cw && !__shfl_sync(0xffffffffu, *s_abort, 0))
-          consume_head_row(P, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
+      const float sx = __ldcg(P.head_sx);
+      for (int64_t u = first; u < it.end; u += kConsumerWarps)
+        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+          consume_head_row(P, sx, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
     }
+    st.seq += (uint32_t)(it.end - it.begin);
     buf ^= 1;
   }
   if (prefetched) cp_async_wait_all();
@@ -557,10 +574,12 @@ nt_status persist_prepare(nt_decode_plan* p) {
   const Unitset head{kItemHead, 0, p->head_V, p->head_K};
   int barriers = p->n_qjobs > 0 ? 1 : 0;
   if (p->mode == NT_STEP_INDEPENDENT) {
+    // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table, so every
+    // CTA has the same mix of decode-heavy and decode-free work.
     std::vector<Unitset> all;
     for (int i = 0; i < n_proj; ++i) all.push_back(ternary(i));
-    if (p->has_head) all.push_back(head);
     partition_stage(all, grid, false, per_cta);
+    if (p->has_head) partition_stage({head}, grid, false, per_cta);
   } else {
     bool first = true;
     for (int l = 0; l < p->n_layers; ++l) {
