@@ -167,6 +167,25 @@ nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
                                 const int8_t* q, const float* s_x, int B, float* logits_opt,
                                 int32_t* argmax, void* ws, size_t ws_bytes, void* stream);
 
+/* The same output projection and arg-max for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it is a convenience of this library. Some
+ * callers cannot obtain a workspace: a plugin whose host process owns every device
+ * allocation, a serving loop that must not call cudaMalloc (it can synchronize the device),
+ * or code under a fixed memory budget. This call takes only the inputs and outputs of
+ * nt_int8_logits_argmax (same meaning, layout and alignment) and allocates nothing: its
+ * scratch is a fixed ~128 KiB array in the library's device globals, present on every device
+ * that loads the library until the process exits.
+ *   B must be <= 16 (the scratch's size); larger B returns NT_ERR_INVALID_ARG.
+ *   The first call on a device looks up that device's scratch address (once, with the
+ *   device current); make that first call before any stream capture.
+ *   Every call on a device shares the one scratch array, so calls that overlap on that
+ *   device (e.g. from two streams) race and give wrong results; serialize them. Each call
+ *   clears the part of the scratch that must start at zero.
+ */
+nt_status nt_int8_logits_argmax_noalloc(const int8_t* T, const float* s_T, int V, int K,
+                                        const int8_t* q, const float* s_x, int B,
+                                        float* logits_opt, int32_t* argmax, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * Decode step: every projection of every layer, then optionally the output projection, in
  * one submission ("A 104 microsecond floor ...": on the instrumented A100 step, roughly

@@ -38,6 +38,7 @@ EXPORTS = (
     "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
     "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
+    "nt_int8_logits_argmax_noalloc",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
     "nt_decode_plan_destroy",
 )
@@ -94,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp], i),
             "nt_int8_logits_workspace_size": ([i, i, i, ctypes.POINTER(sz)], i),
             "nt_int8_logits_argmax": ([vp, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
+            "nt_int8_logits_argmax_noalloc": ([vp, vp, i, i, vp, vp, i, vp, vp, vp], i),
             "nt_decode_plan_create": ([ctypes.POINTER(nt_decode_desc), ctypes.POINTER(vp)], i),
             "nt_decode_step": ([vp, vp], i),
             "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
@@ -180,6 +182,17 @@ def nt_int8_logits_argmax(T: torch.Tensor, s_T: torch.Tensor, V: int, K: int, q:
     _check(load_library().nt_int8_logits_argmax(
         _ptr(T), _ptr(s_T), V, K, _ptr(q), _ptr(s_x), B, _ptr(logits), _ptr(argmax), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)), "nt_int8_logits_argmax")
+
+
+def nt_int8_logits_argmax_noalloc(T: torch.Tensor, s_T: torch.Tensor, V: int, K: int,
+                                  q: torch.Tensor, s_x: torch.Tensor, B: int,
+                                  logits: Optional[torch.Tensor], argmax: torch.Tensor,
+                                  stream=None):
+    """nt_int8_logits_argmax without a workspace, for callers that cannot allocate device
+    memory; B <= 16, and calls on one device must not overlap (they share fixed scratch)."""
+    _check(load_library().nt_int8_logits_argmax_noalloc(
+        _ptr(T), _ptr(s_T), V, K, _ptr(q), _ptr(s_x), B, _ptr(logits), _ptr(argmax),
+        _stream(stream)), "nt_int8_logits_argmax_noalloc")
 
 
 class DecodePlan:
