@@ -193,14 +193,20 @@ def parity_gate(oracle, projs, head, dp, hd, layers=(0, 35)):
     return "pass"
 
 
-def time_steps(torch, plan, steps, stream):
+def time_steps(torch, plan, steps, stream, nvtx_name=None):
+    """Device time of `steps` consecutive steps (CUDA events on the launching stream). The
+    NVTX range lets `ncu --nvtx --nvtx-include <name>/` list exactly these launches."""
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    if nvtx_name:
+        torch.cuda.nvtx.range_push(nvtx_name)
     ev0.record(stream)
     for _ in range(steps):
         plan.nt_decode_step(stream)
     ev1.record(stream)
     torch.cuda.synchronize()
+    if nvtx_name:
+        torch.cuda.nvtx.range_pop()
     return ev0.elapsed_time(ev1) * 1e3  # microseconds
 
 
@@ -260,7 +266,7 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.mark(True)
-    us = time_steps(torch, plan, args.steps, stream)
+    us = time_steps(torch, plan, args.steps, stream, nvtx_name="nt_timed")
     clocks.mark(False)
     if world > 1:
         torch.distributed.barrier()
