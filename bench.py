@@ -413,6 +413,75 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------------------
+# Batched sweep (not the headline line): the same 36-layer projection set and output table
+# with B independent activation vectors per step
+# ---------------------------------------------------------------------------------------
+
+def run_sweep(args):
+    import torch
+
+    import oracle
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    L = args.layers
+    projs, head, dp, hd, _ = build_inputs(torch, nt, dev, L)
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peak()
+    for B in (1, 2, 4, 8, 16):
+        dpB, hosts = [], []
+        for p, d in zip(projs, dp):
+            layer, name = p.name.split(".")
+            x = wl.projection_x(wl.WL_DECODE, int(layer[1:]), wl.PROJ_NAMES.index(name), p.K, B)
+            hosts.append(x)
+            dpB.append(dict(N=p.N, K=p.K, w=d["w"], s_w=d["s_w"], x=torch.from_numpy(x).to(dev),
+                            q=torch.empty((B, p.K), dtype=torch.int8, device=dev),
+                            s_x=torch.empty(B, dtype=torch.float32, device=dev),
+                            y=torch.empty((B, p.N), dtype=torch.float32, device=dev)))
+        hx = wl.head_x(B=B)
+        hdB = dict(T=hd["T"], s=hd["s"], V=head.V, K=head.K, x=torch.from_numpy(hx).to(dev),
+                   q=torch.empty((B, head.K), dtype=torch.int8, device=dev),
+                   sx=torch.empty(B, dtype=torch.float32, device=dev),
+                   logits=torch.empty((B, head.V), dtype=torch.float32, device=dev),
+                   argmax=torch.empty(B, dtype=torch.int32, device=dev))
+        plan = nt.DecodePlan(L, B, dpB, hdB, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+        for _ in range(args.warmup):
+            plan.nt_decode_step(stream)
+        torch.cuda.synchronize()
+        parity = "pass"
+        for i in range(len(wl.PROJ_NAMES)):  # every projection of layer 0
+            p = projs[i]
+            full = wl.projection(wl.WL_DECODE, 0, i, p.N, p.K)
+            q, s = oracle.quantize(hosts[i])
+            _, y, _ = oracle.gemm(full.w_plain, full.s_w, p.N, p.K, q, s)
+            got = dpB[i]["y"].cpu().numpy().astype(np.float64)
+            if np.any(np.abs(got - y) > 1e-6 * np.abs(y.astype(np.float64))):
+                parity = f"{p.name} differs"
+        q, s = oracle.quantize(hx)
+        logits, am, _ = oracle.logits_argmax(head.T, head.s_T, head.V, head.K, q, s)
+        if not np.array_equal(hdB["argmax"].cpu().numpy(), am):
+            parity = "arg-max differs"
+        got = hdB["logits"].cpu().numpy().astype(np.float64)
+        if np.any(np.abs(got - logits) > 1e-6 * np.abs(logits.astype(np.float64))):
+            parity = "logits differ"
+        steps = max(3, min(args.steps, 500))
+        us = time_steps(torch, plan, steps, stream) / steps
+        if plan.nt_decode_step_status() != nt.NT_OK:
+            parity = "timeout reported"
+        nbytes = step_bytes(B=B, n_layers=L)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"metric": "batched decode sweep", "batch": B, "steps": steps,
+                          "us_per_step": round(us, 2), "us_per_token": round(us / B, 2),
+                          "achieved_GBps": round(gbs, 1), "peak_GBps": peak,
+                          "frac": round(gbs / peak, 4), "peak_source": peak_kind,
+                          "bytes_per_step": nbytes, "passes_over_weights": -(-B // 4),
+                          "parity": parity}), flush=True)
+        plan.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,6 +491,8 @@ def main():
     ap.add_argument("--layers", type=int, default=wl.DECODER_8B_LAYERS,
                     help="decoder layers in the step (36 = the 8B-shaped workload; fewer only "
                          "for small profiling captures)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="batched sweep B = 1, 2, 4, 8, 16 (one JSON line per batch)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -430,6 +501,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if world > 1:
         import torch

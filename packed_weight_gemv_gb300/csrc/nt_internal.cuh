@@ -76,15 +76,28 @@ constexpr uint32_t kPoolA_hi = 0xFF01FF01u;  // codes 4..7 -> +1, -1, +1, -1
 constexpr uint32_t kPoolB_lo = 0x01000000u;  // codes 0..3 -> 0, 0, 0, +1
 constexpr uint32_t kPoolB_hi = 0xFFFF0101u;  // codes 4..7 -> +1, +1, -1, -1
 
+// One tiled word (16 trits) as four int8x4 words, trits 0-3, 4-7, 8-11 and 12-15.
+struct Trits16 {
+  uint32_t t0, t1, t2, t3;
+};
+__device__ __forceinline__ Trits16 tiled_word_decode(uint32_t w) {
+  const uint32_t hi = w >> 16;
+  return Trits16{prmt(kPoolA_lo, kPoolA_hi, w), prmt(kPoolB_lo, kPoolB_hi, w),
+                 prmt(kPoolA_lo, kPoolA_hi, hi), prmt(kPoolB_lo, kPoolB_hi, hi)};
+}
+__device__ __forceinline__ int trits16_dot(const Trits16& t, uint32_t a0, uint32_t a1, uint32_t a2,
+                                           uint32_t a3, int acc) {
+  acc = dp4a(t.t0, a0, acc);
+  acc = dp4a(t.t1, a1, acc);
+  acc = dp4a(t.t2, a2, acc);
+  acc = dp4a(t.t3, a3, acc);
+  return acc;
+}
+
 // Dot product of one tiled word (16 trits) with its 16 activation bytes a0..a3.
 __device__ __forceinline__ int tiled_word_dot(uint32_t w, uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, int acc) {
-  const uint32_t hi = w >> 16;
-  acc = dp4a(prmt(kPoolA_lo, kPoolA_hi, w), a0, acc);
-  acc = dp4a(prmt(kPoolB_lo, kPoolB_hi, w), a1, acc);
-  acc = dp4a(prmt(kPoolA_lo, kPoolA_hi, hi), a2, acc);
-  acc = dp4a(prmt(kPoolB_lo, kPoolB_hi, hi), a3, acc);
-  return acc;
+  return trits16_dot(tiled_word_decode(w), a0, a1, a2, a3, acc);
 }
 
 // Plain-layout decode: field codes 00, 01, 11 (10 reads as 0) through a 4-entry byte table.

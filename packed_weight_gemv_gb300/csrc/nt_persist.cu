@@ -1,27 +1,32 @@
-// nt_persist.cu -- the persistent decode-step kernel.
+// nt_persist.cu -- the persistent streaming kernel: the decode step, and the standalone output
+// projection.
 //
 // "The Neutrino Engine" (§ "A 104 microsecond floor inside a 694 microsecond step") reports
 // that a decode step spent most of its time across ~120 kernel boundaries, and that a single
-// fused kernel with software barriers brought similar waits back. Here one cooperative
-// launch streams the whole step, and the weight stream never waits for a barrier: weights
-// do not depend on activations, so the producer warp of every CTA keeps its shared-memory
-// ring full across stage boundaries while the consumer warps wait.
+// fused kernel with software barriers brought similar waits back. Here one launch streams the
+// whole step, and the weight stream never waits for a barrier: weights do not depend on
+// activations, so the producer warp of every CTA keeps its shared-memory ring full across
+// stage boundaries while only the consumer warps wait.
 //
-// CTA layout (one CTA per SM): warps 0..15 consume, warp 16 produces.
+// CTA layout (one CTA per SM): CW consumer warps (16 for batch 1, 15 for batched plans) and
+// one producer warp after them.
 //   producer (lane w feeds consumer warp w): walks the CTA's schedule and issues one
 //     cp.async.bulk per chunk (<= 4 KB of a tile or of an output-table row) of the units warp
 //     w owns (units are dealt round-robin) into w's ring, completing on the slot's mbarrier;
-//   consumers: wait for a chunk, decode + dp4a it against the activation held in shared
-//     memory, release the slot; per unit (4 rows of a tiled matrix, or one output-table row)
-//     a warp reduction and the fp32 epilogue.
-// Ordered mode puts a grid-wide barrier before each stage; only consumers wait at it.
-// Every wait is bounded by a %globaltimer deadline; on expiry the CTA records an error code,
-// stops, and the producer waits (bounded) for its own copies in flight before exiting.
+//   consumers: wait for a chunk, decode it once and dp4a it against up to 4 activation
+//     vectors held in shared memory, release the slot; per unit (4 rows of a tiled matrix, or
+//     one output-table row) a warp reduction and the fp32 epilogue.
+// Batches above 4 vectors take several passes over the weights (the decode + dp4a work, not
+// the memory, bounds those batches). Ordered mode puts a grid-wide barrier before each stage;
+// only consumers wait at it. Every wait is bounded by a %globaltimer deadline; on expiry the
+// CTA records an error code, consumers walk the remaining barriers without work, and the
+// producer waits (bounded) for its own copies in flight before exiting.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -30,21 +35,34 @@
 namespace nt {
 namespace {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreadsP = kConsumerThreads + 32;
-constexpr int kSlots = 3;
+constexpr int kMaxSlots = 3;
 constexpr int kSlotBytes = 4096;
-constexpr int kRingBytes = kConsumerWarps * kSlots * kSlotBytes;  // 192 KB
-constexpr int kBars = kConsumerWarps * kSlots;                     // full (and empty) barriers
-constexpr int kConsumerBarrier = 1;                                // named barrier id
+constexpr int kPiecesPerSlot = kSlotBytes / 512;
+constexpr int kChunkBatch = 4;                       // activation vectors per pass (batched)
+constexpr int kConsumerBarrier = 1;                  // named barrier id
+constexpr int kMaxSmem = 232448;                     // 227 KB per CTA on sm_103
+
+// Kernel configuration: CW consumer warps and up to NBMAX activation vectors per pass. Batch 1
+// runs 16 consumer warps (17 warps, registers capped at 96 by the 5 warps one SM
+// sub-partition holds); batched plans need more registers for 4 vectors' accumulators and run
+// 15 (16 warps, up to 128 registers).
+template <int CW_, int NBMAX_>
+struct KCfg {
+  static constexpr int CW = CW_;
+  static constexpr int CT = CW * 32;       // consumer threads
+  static constexpr int THREADS = CT + 32;  // + the producer warp
+  static constexpr int NBMAX = NBMAX_;
+  static constexpr int BARS = CW * kMaxSlots;
+};
+using Cfg1 = KCfg<16, 1>;
+using CfgB = KCfg<15, kChunkBatch>;
 
 enum : unsigned int { kErrFullWait = 1, kErrEmptyWait = 2, kErrGridBarrier = 3, kErrDrain = 4 };
 
 struct PersistParams {
   const MatDesc* mats;
-  const WorkItem* items;
-  const int* item_off;  // [grid + 1]
+  const WorkItem* items;  // NULL: implicit schedule (standalone output projection)
+  const int* item_off;    // [grid + 1]
   const QuantJob* qjobs;
   int n_qjobs;
   int n_barriers;
@@ -58,11 +76,31 @@ struct PersistParams {
   HeadWs* head_ws;
   int head_V, head_K;
   int has_head;
-  int act_stride;
+  int B;         // activation vectors
+  int chunk_b;   // vectors per pass (<= kChunkBatch)
+  int nslots;    // ring slots per consumer warp (<= kMaxSlots)
+  int act_k;     // bytes per activation vector in shared memory
   uint32_t launch_idx;
-  uint32_t barrier_extra;  // added to the first grid barrier's target (timeout-path tests)
+  uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
   uint64_t timeout_ns;
 };
+
+struct SmemLayout {
+  int ring, act, bars, hbest, red, abort_flag, total;
+};
+
+template <class C>
+__host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int act_k) {
+  SmemLayout L;
+  L.ring = 0;
+  L.act = L.ring + C::CW * nslots * kSlotBytes;
+  L.bars = L.act + 2 * chunk_b * act_k;
+  L.hbest = L.bars + 2 * C::BARS * 8;
+  L.red = L.hbest + C::CW * kStepMaxBatch * (int)sizeof(HeadPartial);
+  L.abort_flag = L.red + C::CW * 4;
+  L.total = L.abort_flag + 16;
+  return L;
+}
 
 // ---- PTX wrappers --------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -105,8 +143,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <class C>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(kConsumerThreads) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"n"(kConsumerBarrier), "n"(C::CT) : "memory");
 }
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
@@ -149,7 +188,7 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-// Sum of 4 per-lane values across the warp; row r's total lands in lane 8r.
+// Sum of 4 per-lane values across the warp; row r's total lands in lanes 8r..8r+7.
 __device__ __forceinline__ int warp_sum4(int a0, int a1, int a2, int a3, int lane) {
   const bool h16 = lane & 16;
   int k0 = h16 ? a2 : a0, k1 = h16 ? a3 : a1;
@@ -165,7 +204,30 @@ __device__ __forceinline__ int warp_sum4(int a0, int a1, int a2, int a3, int lan
   return k;
 }
 
-// Unit geometry of a work item: bytes per unit and the source base address.
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// ---- schedule --------------------------------------------------------------------------
+__device__ __forceinline__ int item_count(const PersistParams& P) {
+  if (P.items) return P.item_off[blockIdx.x + 1] - P.item_off[blockIdx.x];
+  return (P.B + P.chunk_b - 1) / P.chunk_b;  // implicit: one item per pass
+}
+
+// Item i of this CTA. The implicit schedule (standalone output projection) gives CTA c the
+// rows [c V / grid, (c+1) V / grid) once per pass of chunk_b vectors.
+__device__ __forceinline__ WorkItem get_item(const PersistParams& P, int i) {
+  if (P.items) return P.items[P.item_off[blockIdx.x] + i];
+  WorkItem w;
+  w.kind = kItemHead;
+  w.mat = 0;
+  w.flags = 0;
+  w.b0 = i * P.chunk_b;
+  w.begin = (int64_t)blockIdx.x * P.head_V / gridDim.x;
+  w.end = (int64_t)(blockIdx.x + 1) * P.head_V / gridDim.x;
+  return w;
+}
+
 __device__ __forceinline__ void unit_geometry(const PersistParams& P, const WorkItem& it,
                                               const uint8_t*& base, int& unit_bytes) {
   if (it.kind == kItemTernary) {
@@ -178,28 +240,32 @@ __device__ __forceinline__ void unit_geometry(const PersistParams& P, const Work
   }
 }
 
+// First unit of an item that consumer warp w owns (units are dealt round-robin by their
+// sequence number within the CTA).
+template <class C>
+__device__ __forceinline__ int64_t first_unit(const WorkItem& it, uint32_t seq, int w) {
+  return it.begin + (int64_t)((w - (int)(seq % C::CW) + C::CW) % C::CW);
+}
+
 // ---- producer ------------------------------------------------------------------------
-// Lane w of the producer warp feeds consumer warp w's ring: it walks the CTA's schedule and
-// issues the chunks of the units that warp w owns (units are dealt round-robin), so the 8
-// lanes issue copies independently of each other.
-__device__ void producer(const PersistParams& P, const WorkItem* items, int n_items, uint8_t* ring,
-                         uint32_t full0, uint32_t empty0, volatile int* s_abort, int w) {
+// Lane w of the producer warp feeds consumer warp w's ring.
+template <class C>
+__device__ void producer(const PersistParams& P, int n_items, uint8_t* ring, uint32_t full0,
+                         uint32_t empty0, volatile int* s_abort, int w) {
   const uint64_t pol = evict_first_policy();
-  const uint32_t ring_w = smem_addr(ring) + (uint32_t)w * kSlots * kSlotBytes;
-  const uint32_t full_w = full0 + 8u * w * kSlots, empty_w = empty0 + 8u * w * kSlots;
-  uint32_t cnt = 0, seq = 0;
+  const uint32_t ring_w = smem_addr(ring) + (uint32_t)(w * P.nslots * kSlotBytes);
+  const uint32_t full_w = full0 + 8u * w * kMaxSlots, empty_w = empty0 + 8u * w * kMaxSlots;
+  uint32_t slot = 0, phase = 0, issued = 0, seq = 0;
   bool ok = true;
   for (int i = 0; i < n_items && ok; ++i) {
-    const WorkItem it = items[i];
+    const WorkItem it = get_item(P, i);
     const uint8_t* base;
     int ub;
     unit_geometry(P, it, base, ub);
-    const int64_t first = it.begin + (int64_t)((w - (int)(seq % kConsumerWarps) + kConsumerWarps) % kConsumerWarps);
-    for (int64_t u = first; u < it.end && ok; u += kConsumerWarps) {
+    for (int64_t u = first_unit<C>(it, seq, w); u < it.end && ok; u += C::CW) {
       const uint8_t* src = base + u * (int64_t)ub;
       for (int off = 0; off < ub; off += kSlotBytes) {
         const uint32_t bytes = (uint32_t)min(kSlotBytes, ub - off);
-        const uint32_t slot = cnt % kSlots, phase = (cnt / kSlots) & 1u;
         if (!wait_phase(empty_w + 8 * slot, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
           if (!*s_abort) record_error(P.ctrl, kErrEmptyWait, s_abort);
           ok = false;
@@ -207,20 +273,21 @@ __device__ void producer(const PersistParams& P, const WorkItem* items, int n_it
         }
         mbar_expect_tx(full_w + 8 * slot, bytes);
         bulk_load(ring_w + slot * kSlotBytes, src + off, bytes, full_w + 8 * slot, pol);
-        ++cnt;
+        ++issued;
+        if (++slot == (uint32_t)P.nslots) { slot = 0; phase ^= 1u; }
       }
     }
     seq += (uint32_t)(it.end - it.begin);
   }
   // Drain: every slot's last copy must have landed before this thread (and so the CTA)
   // may exit, whatever happened to the consumers.
-  for (uint32_t s = 0; s < kSlots; ++s) {
-    if (cnt <= s) continue;
-    const uint32_t last = (cnt - 1 - s) / kSlots * kSlots + s;
+  for (uint32_t s = 0; s < (uint32_t)P.nslots; ++s) {
+    if (issued <= s) continue;
+    const uint32_t parity = ((issued - 1 - s) / (uint32_t)P.nslots) & 1u;
     const uint32_t bar = full_w + 8 * s;
-    if (mbar_try_wait(bar, (last / kSlots) & 1u)) continue;
+    if (mbar_try_wait(bar, parity)) continue;
     const uint64_t deadline = globaltimer_ns() + P.timeout_ns;
-    while (!mbar_try_wait(bar, (last / kSlots) & 1u)) {
+    while (!mbar_try_wait(bar, parity)) {
       if (globaltimer_ns() > deadline) {
         record_error(P.ctrl, kErrDrain, s_abort);
         break;
@@ -230,42 +297,64 @@ __device__ void producer(const PersistParams& P, const WorkItem* items, int n_it
 }
 
 // ---- consumers -----------------------------------------------------------------------
-struct ConsumerState {
-  uint32_t cnt;  // chunks this warp consumed
-  uint32_t seq;  // units seen by the CTA (for the round-robin owner)
-  float best_v;  // output projection: this warp's best logit / row (lane 0)
-  int best_i;
+struct Ring {
+  uint8_t* base;  // this warp's first slot
+  uint32_t full, empty;
+  uint32_t slot, phase;
+  int nslots;
 };
 
-// Quantize one fp32 vector with the 256 consumer threads.
-__device__ void quantize_consumers(const QuantJob& j, float* red) {
+// A consumer warp's wait for its next chunk: every lane waits (each observes the mbarrier
+// phase, which makes the bulk copy's bytes visible to it) and the outcome is made
+// warp-uniform, so no lane leaves while others go on to warp-wide shuffles.
+__device__ __forceinline__ const uint8_t* wait_chunk(const PersistParams& P, Ring& r, int lane,
+                                                     volatile int* s_abort) {
+  const bool ok = __all_sync(0xffffffffu, wait_phase(r.full + 8 * r.slot, r.phase, P.timeout_ns,
+                                                     P.ctrl, s_abort));
+  if (!ok) {
+    if (lane == 0 && !*s_abort) record_error(P.ctrl, kErrFullWait, s_abort);
+    return nullptr;
+  }
+  return r.base + r.slot * kSlotBytes;
+}
+
+__device__ __forceinline__ void release_chunk(Ring& r, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(r.empty + 8 * r.slot);
+  if (++r.slot == (uint32_t)r.nslots) { r.slot = 0; r.phase ^= 1u; }
+}
+
+// Quantize one fp32 vector with the consumer threads.
+template <class C>
+__device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_out, float* red) {
   const int t = threadIdx.x;
   float m = 0.0f;
-  for (int k = t; k < j.K; k += kConsumerThreads) m = fmaxf(m, fabsf(j.x[k]));
+  for (int k = t; k < K; k += C::CT) m = fmaxf(m, fabsf(x[k]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((t & 31) == 0) red[t >> 5] = m;
-  consumer_sync();
+  consumer_sync<C>();
   m = red[0];
 #pragma unroll
-  for (int i = 1; i < kConsumerWarps; ++i) m = fmaxf(m, red[i]);
+  for (int i = 1; i < C::CW; ++i) m = fmaxf(m, red[i]);
   const float s = (m == 0.0f) ? 0.0f : __fdiv_rn(m, 127.0f);
-  if (t == 0) *j.s = s;
-  for (int k = t; k < j.K; k += kConsumerThreads) {
+  if (t == 0) *s_out = s;
+  for (int k = t; k < K; k += C::CT) {
     int v = 0;
     if (m != 0.0f) {
-      v = __float2int_rn(__fdiv_rn(j.x[k], s));
+      v = __float2int_rn(__fdiv_rn(x[k], s));
       v = v > 127 ? 127 : (v < -127 ? -127 : v);
     }
-    j.q[k] = (int8_t)v;
+    q[k] = (int8_t)v;
   }
-  consumer_sync();  // red[] reuse
+  consumer_sync<C>();  // red[] reuse
 }
 
 // Grid-wide barrier among the consumers of all CTAs; `target` counts arrivals modulo 2^32.
-__device__ bool grid_barrier(const PersistParams& P, uint32_t target, volatile int* s_abort) {
+template <class C>
+__device__ void grid_barrier(const PersistParams& P, uint32_t target, volatile int* s_abort) {
   target += P.barrier_extra;
-  consumer_sync();
+  consumer_sync<C>();
   if (threadIdx.x == 0 && !*s_abort) {
     __threadfence();
     red_release_add(&P.ctrl->arrive, 1u);
@@ -278,154 +367,181 @@ __device__ bool grid_barrier(const PersistParams& P, uint32_t target, volatile i
       }
     }
   }
-  consumer_sync();
-  return !*s_abort;
+  consumer_sync<C>();
 }
 
-// Copies K activation bytes (K % 16 == 0) into shared memory, synchronously or with cp.async.
-__device__ void load_act(uint8_t* dst, const int8_t* src, int K, bool async) {
-  for (int o = threadIdx.x * 16; o < K; o += kConsumerThreads * 16) {
-    if (async) cp_async16(smem_addr(dst + o), src + o);
-    else *reinterpret_cast<uint4*>(dst + o) = __ldcg(reinterpret_cast<const uint4*>(src + o));
+// Copies nb activation vectors of K bytes (vector b at src + b*K) into shared memory at
+// stride act_k, synchronously or with cp.async.
+template <class C>
+__device__ void load_act(uint8_t* dst, const int8_t* src, int K, int nb, int act_k, bool async) {
+  const int per = K / 16;
+  for (int i = threadIdx.x; i < per * nb; i += C::CT) {
+    const int b = i / per, o = (i - b * per) * 16;
+    if (async) cp_async16(smem_addr(dst + b * act_k + o), src + (int64_t)b * K + o);
+    else *reinterpret_cast<uint4*>(dst + b * act_k + o) = __ldcg(reinterpret_cast<const uint4*>(src + (int64_t)b * K + o));
   }
   if (async) cp_async_commit();
 }
 
-__device__ __forceinline__ const int8_t* item_act(const PersistParams& P, const WorkItem& it, int& K) {
+__device__ __forceinline__ const int8_t* item_act(const PersistParams& P, const WorkItem& it, int& K, int& nb) {
+  nb = min(P.chunk_b, P.B - it.b0);
   if (it.kind == kItemTernary) {
     K = P.mats[it.mat].K;
-    return P.mats[it.mat].q;
+    return P.mats[it.mat].q + (int64_t)it.b0 * K;
   }
   K = P.head_K;
-  return P.head_q;
+  return P.head_q + (int64_t)it.b0 * K;
 }
 
-// A consumer warp's wait for one chunk: every lane waits (each observes the mbarrier phase,
-// which makes the bulk copy's bytes visible to it) and the outcome is made warp-uniform, so
-// no lane leaves while others go on to warp-wide shuffles.
-__device__ __forceinline__ bool wait_chunk(uint32_t bar, uint32_t phase, const PersistParams& P,
-                                           int lane, volatile int* s_abort) {
-  const bool ok = __all_sync(0xffffffffu, wait_phase(bar, phase, P.timeout_ns, P.ctrl, s_abort));
-  if (!ok && lane == 0 && !*s_abort) record_error(P.ctrl, kErrFullWait, s_abort);
-  return ok;
-}
-
-// 16 bytes of one lane in one 512-byte piece: 4 rows x 16 trits against 16 activations.
-__device__ __forceinline__ void tile_piece(const uint8_t* sb, const uint8_t* ab, int& a0, int& a1,
-                                           int& a2, int& a3) {
+// 16 bytes of one lane in one 512-byte piece (4 rows x 16 trits), decoded once and dotted
+// with NB activation vectors (stride act_k in shared memory).
+template <int NB>
+__device__ __forceinline__ void tile_piece(const uint8_t* sb, const uint8_t* ab, int act_k, int (&acc)[NB][4]) {
   const uint4 wv = lds128(sb);
-  const uint4 a = lds128(ab);
-  a0 = tiled_word_dot(wv.x, a.x, a.y, a.z, a.w, a0);
-  a1 = tiled_word_dot(wv.y, a.x, a.y, a.z, a.w, a1);
-  a2 = tiled_word_dot(wv.z, a.x, a.y, a.z, a.w, a2);
-  a3 = tiled_word_dot(wv.w, a.x, a.y, a.z, a.w, a3);
+  const Trits16 d0 = tiled_word_decode(wv.x), d1 = tiled_word_decode(wv.y);
+  const Trits16 d2 = tiled_word_decode(wv.z), d3 = tiled_word_decode(wv.w);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const uint4 a = lds128(ab + b * act_k);
+    acc[b][0] = trits16_dot(d0, a.x, a.y, a.z, a.w, acc[b][0]);
+    acc[b][1] = trits16_dot(d1, a.x, a.y, a.z, a.w, acc[b][1]);
+    acc[b][2] = trits16_dot(d2, a.x, a.y, a.z, a.w, acc[b][2]);
+    acc[b][3] = trits16_dot(d3, a.x, a.y, a.z, a.w, acc[b][3]);
+  }
 }
 
-// One tile (4 rows) of a tiled ternary matrix. The row scale is loaded before the first
-// chunk so its latency hides behind the chunk work; sx is the item's activation scale.
-__device__ bool consume_tile(const PersistParams& P, const MatDesc& m, float sx, int64_t tile,
-                             const uint8_t* act, uint8_t* ring, uint32_t full0, uint32_t empty0,
-                             ConsumerState& st, int cw, int lane, volatile int* s_abort) {
-  constexpr int kPieces = kSlotBytes / 512;
+// 16 bytes of one lane of an output-table row against NB activation vectors.
+template <int NB>
+__device__ __forceinline__ void row_piece(const uint8_t* sb, const uint8_t* ab, int act_k, int (&acc)[NB][2], int h) {
+  const uint4 t = lds128(sb);
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const uint4 a = lds128(ab + b * act_k);
+    int s = acc[b][h];
+    s = dp4a(t.x, a.x, s);
+    s = dp4a(t.y, a.y, s);
+    s = dp4a(t.z, a.z, s);
+    s = dp4a(t.w, a.w, s);
+    acc[b][h] = s;
+  }
+}
+
+// One tile (4 rows) of a tiled ternary matrix against NB activation vectors. The row scale
+// is loaded before the first chunk so its latency hides behind the chunk work.
+template <int NB>
+__device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDesc& m, const float (&sx)[NB], int b0,
+                             int64_t tile, const uint8_t* act, Ring& ring, int lane, volatile int* s_abort) {
   const int pieces = (int)(padded_k(m.K) / 512);
   const int64_t n = tile * 4 + (lane >> 3);
   const float sw = ((lane & 7) == 0 && n < m.N) ? __ldg(m.s_w + n) : 0.0f;
-  int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  for (int p0 = 0; p0 < pieces; p0 += kPieces) {
-    const uint32_t slot = st.cnt % kSlots, phase = (st.cnt / kSlots) & 1u;
-    const uint32_t idx = (uint32_t)cw * kSlots + slot;
-    if (!wait_chunk(full0 + 8 * idx, phase, P, lane, s_abort)) return false;
-    const uint8_t* sb = ring + idx * kSlotBytes + lane * 16;
-    const uint8_t* ab = act + (p0 * 32 + lane) * 16;
-    if (pieces - p0 >= kPieces) {
+  int acc[NB][4];
 #pragma unroll
-      for (int p = 0; p < kPieces; ++p) tile_piece(sb + p * 512, ab + p * 512, a0, a1, a2, a3);
+  for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0;
+  for (int p0 = 0; p0 < pieces; p0 += kPiecesPerSlot) {
+    const uint8_t* slot = wait_chunk(P, ring, lane, s_abort);
+    if (!slot) return;
+    const uint8_t* sb = slot + lane * 16;
+    const uint8_t* ab = act + (p0 * 32 + lane) * 16;
+    if (pieces - p0 >= kPiecesPerSlot) {  // full chunk: branch-free, so loads can run ahead
+#pragma unroll
+      for (int p = 0; p < kPiecesPerSlot; ++p) tile_piece<NB>(sb + p * 512, ab + p * 512, P.act_k, acc);
     } else {
-      for (int p = 0; p < pieces - p0; ++p) tile_piece(sb + p * 512, ab + p * 512, a0, a1, a2, a3);
+      for (int p = 0; p < pieces - p0; ++p) tile_piece<NB>(sb + p * 512, ab + p * 512, P.act_k, acc);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * idx);
-    ++st.cnt;
+    release_chunk(ring, lane);
   }
-  const int total = warp_sum4(a0, a1, a2, a3, lane);
-  if ((lane & 7) == 0 && n < m.N) m.y[n] = scale_out(total, sw, sx);
-  return true;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int total = warp_sum4(acc[b][0], acc[b][1], acc[b][2], acc[b][3], lane);
+    if ((lane & 7) == 0 && n < m.N) m.y[(int64_t)(b0 + b) * m.N + n] = scale_out(total, sw, sx[b]);
+  }
 }
 
-// One row of the int8 output table.
-__device__ __forceinline__ void row_piece(const uint8_t* sb, const uint8_t* ab, int& acc) {
-  const uint4 t = lds128(sb);
-  const uint4 a = lds128(ab);
-  acc = dp4a(t.x, a.x, acc);
-  acc = dp4a(t.y, a.y, acc);
-  acc = dp4a(t.z, a.z, acc);
-  acc = dp4a(t.w, a.w, acc);
-}
-
-__device__ bool consume_head_row(const PersistParams& P, float sx, int64_t v, const uint8_t* act,
-                                 uint8_t* ring, uint32_t full0, uint32_t empty0, ConsumerState& st,
-                                 int cw, int lane, volatile int* s_abort) {
+// One row of the int8 output table against NB activation vectors; lane 0 keeps each
+// vector's best (logit, row) for this warp in shared memory.
+template <int NB>
+__device__ __forceinline__ void consume_head_row(const PersistParams& P, const float (&sx)[NB], int b0, int64_t v,
+                                 const uint8_t* act, Ring& ring, HeadPartial* wbest, int lane,
+                                 volatile int* s_abort) {
   const float sv = lane == 0 ? __ldg(P.head_s + v) : 0.0f;
-  int acc = 0, acc2 = 0;
+  int acc[NB][2];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = 0;
   for (int off = 0; off < P.head_K; off += kSlotBytes) {
     const int cb = min(kSlotBytes, P.head_K - off);
-    const uint32_t slot = st.cnt % kSlots, phase = (st.cnt / kSlots) & 1u;
-    const uint32_t idx = (uint32_t)cw * kSlots + slot;
-    if (!wait_chunk(full0 + 8 * idx, phase, P, lane, s_abort)) return false;
-    const uint8_t* sb = ring + idx * kSlotBytes + lane * 16;
+    const uint8_t* slot = wait_chunk(P, ring, lane, s_abort);
+    if (!slot) return;
+    const uint8_t* sb = slot + lane * 16;
     const uint8_t* ab = act + off + lane * 16;
-    if (cb == kSlotBytes) {
+    if (cb == kSlotBytes) {  // full chunk: branch-free
 #pragma unroll
-      for (int o = 0; o < kSlotBytes; o += 1024) {
-        row_piece(sb + o, ab + o, acc);
-        row_piece(sb + o + 512, ab + o + 512, acc2);
-      }
+      for (int p = 0; p < kPiecesPerSlot; ++p) row_piece<NB>(sb + p * 512, ab + p * 512, P.act_k, acc, p & 1);
     } else {
-      for (int o = 0; o + lane * 16 < cb; o += 512) row_piece(sb + o, ab + o, acc);
+      for (int p = 0; p * 512 + lane * 16 < cb; ++p) row_piece<NB>(sb + p * 512, ab + p * 512, P.act_k, acc, 0);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * idx);
-    ++st.cnt;
+    release_chunk(ring, lane);
   }
-  const int total = warp_sum(acc + acc2);
-  if (lane == 0) {
-    const float lg = scale_out(total, sv, sx);
-    if (P.head_logits) P.head_logits[v] = lg;
-    if (lg > st.best_v) { st.best_v = lg; st.best_i = (int)v; }  // rows rise per warp
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int total = warp_sum(acc[b][0] + acc[b][1]);
+    if (lane == 0) {
+      const float lg = scale_out(total, sv, sx[b]);
+      if (P.head_logits) P.head_logits[(int64_t)(b0 + b) * P.head_V + v] = lg;
+      HeadPartial& hb = wbest[b0 + b];
+      if (better(lg, (int)v, hb.val, hb.idx)) hb = HeadPartial{lg, (int)v};
+    }
   }
-  return true;
 }
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+template <class C, int NB>
+__device__ __forceinline__ void consume_item(const PersistParams& P, const WorkItem& it, uint32_t seq, const uint8_t* act,
+                             Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort) {
+  float sx[NB];
+  const float* sxp = it.kind == kItemTernary ? P.mats[it.mat].s_x : P.head_sx;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) sx[b] = __ldcg(sxp + it.b0 + b);
+  const int64_t first = first_unit<C>(it, seq, cw);
+  // The abort flag is read by lane 0 and broadcast, so the whole warp takes one branch.
+  if (it.kind == kItemTernary) {
+    const MatDesc m = P.mats[it.mat];
+    for (int64_t u = first; u < it.end; u += C::CW)
+      if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+        consume_tile<NB>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
+  } else {
+    for (int64_t u = first; u < it.end; u += C::CW)
+      if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+        consume_head_row<NB>(P, sx, it.b0, u, act, ring, wbest, lane, s_abort);
+  }
 }
 
-__global__ void __launch_bounds__(kThreadsP, 1) persist_kernel(const PersistParams P) {
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_constant__ PersistParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  uint8_t* act = smem + kRingBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(act + 2 * P.act_stride);
-  HeadPartial* hbest = reinterpret_cast<HeadPartial*>(bars + 2 * kBars);
-  float* red = reinterpret_cast<float*>(hbest + kConsumerWarps);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(red + kConsumerWarps);
+  const SmemLayout L = smem_layout<C>(P.nslots, P.chunk_b, P.act_k);
+  uint8_t* ring = smem + L.ring;
+  uint8_t* act = smem + L.act;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  HeadPartial* hbest = reinterpret_cast<HeadPartial*>(smem + L.hbest);  // [warp][kStepMaxBatch]
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + kBars);
+  const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::BARS);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kBars; ++i) {
+    for (int i = 0; i < C::BARS; ++i) {
       mbar_init(full0 + 8 * i, 1);
       mbar_init(empty0 + 8 * i, 1);
     }
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  for (int i = threadIdx.x; i < C::CW * kStepMaxBatch; i += blockDim.x)
+    hbest[i] = HeadPartial{-INFINITY, INT_MAX};
   __syncthreads();
 
-  const int i0 = P.item_off[blockIdx.x], n_items = P.item_off[blockIdx.x + 1] - i0;
-  const WorkItem* items = P.items + i0;
-
-  if (warp == kConsumerWarps) {
-    if (lane < kConsumerWarps) producer(P, items, n_items, ring, full0, empty0, s_abort, lane);
+  const int n_items = item_count(P);
+  if (warp == C::CW) {
+    if (lane < C::CW) producer<C>(P, n_items, ring, full0, empty0, s_abort, lane);
     return;
   }
 
@@ -433,90 +549,105 @@ __global__ void __launch_bounds__(kThreadsP, 1) persist_kernel(const PersistPara
   // Every consumer warp walks the same sequence of named and grid barriers whatever
   // happens; after an abort (s_abort) they only skip the work, so no barrier is left short.
   const int cw = warp;
-  ConsumerState st{0u, 0u, -INFINITY, INT_MAX};
+  Ring rg{ring + cw * P.nslots * kSlotBytes, full0 + 8u * cw * kMaxSlots, empty0 + 8u * cw * kMaxSlots,
+          0u, 0u, P.nslots};
+  HeadPartial* wbest = hbest + cw * kStepMaxBatch;
   const uint32_t barrier_base = P.launch_idx * (uint32_t)P.n_barriers * gridDim.x;
-  uint32_t barriers = 0;
+  uint32_t barriers = 0, seq = 0;
 
   if (P.n_qjobs > 0) {  // quantize the step's fp32 inputs, then wait for every CTA
-    for (int j = blockIdx.x; j < P.n_qjobs; j += gridDim.x) quantize_consumers(P.qjobs[j], red);
+    for (int j = blockIdx.x; j < P.n_qjobs; j += gridDim.x) {
+      const QuantJob qj = P.qjobs[j];
+      for (int b = 0; b < qj.B; ++b)
+        quantize_consumers<C>(qj.x + (int64_t)b * qj.K, qj.K, qj.q + (int64_t)b * qj.K, qj.s + b, red);
+    }
     ++barriers;
-    grid_barrier(P, barrier_base + barriers * gridDim.x, s_abort);
+    grid_barrier<C>(P, barrier_base + barriers * gridDim.x, s_abort);
   }
 
+  const int act_buf = P.chunk_b * P.act_k;
   int buf = 0;
   bool prefetched = false;
   for (int i = 0; i < n_items; ++i) {
-    const WorkItem it = items[i];
+    const WorkItem it = get_item(P, i);
     if (it.flags & kFlagStage) {
       ++barriers;
-      grid_barrier(P, barrier_base + barriers * gridDim.x, s_abort);
+      grid_barrier<C>(P, barrier_base + barriers * gridDim.x, s_abort);
     }
-    int K;
-    const int8_t* q = item_act(P, it, K);
-    uint8_t* abuf = act + buf * P.act_stride;
+    int K, nb;
+    const int8_t* q = item_act(P, it, K, nb);
+    uint8_t* abuf = act + buf * act_buf;
     if (prefetched) cp_async_wait_all();
-    else load_act(abuf, q, K, false);
-    consumer_sync();  // act[buf] complete; every warp is past the previous item
+    else load_act<C>(abuf, q, K, nb, P.act_k, false);
+    consumer_sync<C>();  // act[buf] complete; every warp is past the previous item
     prefetched = false;
-    if (i + 1 < n_items && !(items[i + 1].flags & kFlagStage)) {
-      int K2;
-      const int8_t* q2 = item_act(P, items[i + 1], K2);
-      load_act(act + (buf ^ 1) * P.act_stride, q2, K2, true);
-      prefetched = true;
+    if (i + 1 < n_items) {
+      const WorkItem nx = get_item(P, i + 1);
+      if (!(nx.flags & kFlagStage)) {
+        int K2, nb2;
+        const int8_t* q2 = item_act(P, nx, K2, nb2);
+        load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
+        prefetched = true;
+      }
     }
-    // The abort flag is read by lane 0 and broadcast, so the whole warp takes one branch.
-    const int64_t first = it.begin + (int64_t)((cw - (int)(st.seq % kConsumerWarps) + kConsumerWarps) % kConsumerWarps);
-    if (it.kind == kItemTernary) {
-      const MatDesc m = P.mats[it.mat];
-      const float sx = __ldcg(m.s_x);
-      for (int64_t u = first; u < it.end; u += kConsumerWarps)
-        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
-          consume_tile(P, m, sx, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
+    if constexpr (C::NBMAX == 1) {
+      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort);
     } else {
-      const float sx = __ldcg(P.head_sx);
-      for (int64_t u = first; u < it.end; u += kConsumerWarps)
-        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
-          consume_head_row(P, sx, u, abuf, ring, full0, empty0, st, cw, lane, s_abort);
+      switch (nb) {
+        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
+        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
+        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
+        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
+      }
     }
-    st.seq += (uint32_t)(it.end - it.begin);
+    seq += (uint32_t)(it.end - it.begin);
     buf ^= 1;
   }
   if (prefetched) cp_async_wait_all();
 
-  if (P.has_head) {  // CTA best, then the last CTA reduces all CTAs
-    if (lane == 0) hbest[cw] = HeadPartial{st.best_v, st.best_i};
-    consumer_sync();
-    if (threadIdx.x == 0 && !*s_abort) {
-      HeadPartial b = hbest[0];
-      for (int w = 1; w < kConsumerWarps; ++w)
-        if (better(hbest[w].val, hbest[w].idx, b.val, b.idx)) b = hbest[w];
-      P.head_ws->part[blockIdx.x] = b;
+  if (P.has_head) {  // CTA best per vector, then the last CTA to finish reduces all CTAs
+    volatile int& s_last = *reinterpret_cast<volatile int*>(smem + L.abort_flag + 4);
+    consumer_sync<C>();
+    if (threadIdx.x < P.B && !*s_abort) {
+      HeadPartial b = hbest[threadIdx.x];
+      for (int w = 1; w < C::CW; ++w) {
+        const HeadPartial c = hbest[w * kStepMaxBatch + threadIdx.x];
+        if (better(c.val, c.idx, b.val, b.idx)) b = c;
+      }
+      P.head_ws->part[(int64_t)blockIdx.x * P.B + threadIdx.x] = b;
       __threadfence();
-      if (atomicAdd(&P.ctrl->head_done, 1u) == gridDim.x - 1) {
-        __threadfence();
+    }
+    consumer_sync<C>();
+    if (threadIdx.x == 0) s_last = !*s_abort && atomicAdd(&P.ctrl->head_done, 1u) == gridDim.x - 1;
+    consumer_sync<C>();
+    if (s_last) {
+      __threadfence();
+      if (threadIdx.x < P.B) {
         float bv = -INFINITY;
         int bi = INT_MAX;
         for (int c = 0; c < (int)gridDim.x; ++c) {
-          const float pv = __ldcg(&P.head_ws->part[c].val);
-          const int pi = __ldcg(&P.head_ws->part[c].idx);
+          const HeadPartial* pp = &P.head_ws->part[(int64_t)c * P.B + threadIdx.x];
+          const float pv = __ldcg(&pp->val);
+          const int pi = __ldcg(&pp->idx);
           if (better(pv, pi, bv, bi)) { bv = pv; bi = pi; }
         }
-        P.head_argmax[0] = bi == INT_MAX ? 0 : bi;
-        P.ctrl->head_done = 0u;
+        P.head_argmax[threadIdx.x] = bi == INT_MAX ? 0 : bi;
       }
+      if (threadIdx.x == 0) P.ctrl->head_done = 0u;
     }
   }
 }
 
-// ---- host: schedule --------------------------------------------------------------------
+// ---- host ------------------------------------------------------------------------------
 struct Unitset {
   int kind, mat;
   int64_t units;
   int64_t unit_bytes;
 };
 
-// Splits one stage's units into `grid` contiguous byte ranges and appends each CTA's items.
-void partition_stage(const std::vector<Unitset>& sets, int grid, bool barrier_before,
+// Splits one stage's units into `grid` contiguous byte ranges and appends each CTA's items
+// for the pass starting at vector b0.
+void partition_stage(const std::vector<Unitset>& sets, int grid, int b0, bool barrier_before,
                      std::vector<std::vector<WorkItem>>& per_cta) {
   int64_t total = 0;
   for (const Unitset& s : sets) total += s.units * s.unit_bytes;
@@ -526,42 +657,85 @@ void partition_stage(const std::vector<Unitset>& sets, int grid, bool barrier_be
     if (barrier_before && !flagged[c]) { x.flags |= kFlagStage; flagged[c] = true; }
     per_cta[c].push_back(x);
   };
-  int64_t start = 0;  // byte offset of the current unit within the stage
+  int64_t start = 0;  // byte offset of the current unit set within the stage
   for (const Unitset& s : sets) {
     int64_t u = 0;
     while (u < s.units) {
       // owner of unit u: the CTA whose byte range holds the unit's first byte
       const int c = (int)std::min<int64_t>(grid - 1, (start + u * s.unit_bytes) * grid / std::max<int64_t>(total, 1));
-      const int64_t end_byte = (int64_t)(c + 1) * total / grid;  // first byte of CTA c+1
+      const int64_t end_byte = (int64_t)(c + 1) * total / grid;
       int64_t v = u + 1;
       while (v < s.units && start + v * s.unit_bytes < end_byte) ++v;
-      push(c, WorkItem{s.kind, s.mat, 0, 0, u, v});
+      push(c, WorkItem{s.kind, s.mat, 0, b0, u, v});
       u = v;
     }
     start += s.units * s.unit_bytes;
   }
   if (barrier_before)  // every CTA takes part in the barrier, with or without work
     for (int c = 0; c < grid; ++c)
-      if (!flagged[c]) push(c, WorkItem{kItemTernary, 0, 0, 0, 0, 0});
+      if (!flagged[c]) push(c, WorkItem{sets.front().kind, sets.front().mat, 0, b0, 0, 0});
+}
+
+// Ring depth and vectors per pass that fit the shared-memory budget for activations of
+// act_k bytes: 3 slots when possible (deeper ring), else 2; then fewer vectors per pass.
+template <class C>
+bool pick_config_for(int B, int act_k, int* nslots, int* chunk_b, size_t* smem) {
+  int dev = 0, optin = kMaxSmem;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const int limit = std::min(kMaxSmem, optin);
+  for (int cb = std::min(B, C::NBMAX); cb >= 1; --cb)
+    for (int ns = kMaxSlots; ns >= 2; --ns) {
+      const SmemLayout L = smem_layout<C>(ns, cb, act_k);
+      if (L.total <= limit) {
+        *nslots = ns;
+        *chunk_b = cb;
+        *smem = (size_t)L.total;
+        return true;
+      }
+    }
+  return false;
+}
+
+bool pick_config(int B, int act_k, int* nslots, int* chunk_b, size_t* smem) {
+  return B == 1 ? pick_config_for<Cfg1>(B, act_k, nslots, chunk_b, smem)
+                : pick_config_for<CfgB>(B, act_k, nslots, chunk_b, smem);
+}
+
+std::mutex g_attr_mu;
+bool g_attr_set[64] = {};
+
+nt_status configure_kernel(int device) {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (device >= 0 && device < 64 && g_attr_set[device]) return NT_OK;
+  NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<Cfg1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+  NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<CfgB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+  if (device >= 0 && device < 64) g_attr_set[device] = true;
+  return NT_OK;
+}
+
+// The kernel instance and block size for a batch.
+const void* kernel_for(int B, int* threads) {
+  if (B == 1) {
+    *threads = Cfg1::THREADS;
+    return reinterpret_cast<const void*>(persist_kernel<Cfg1>);
+  }
+  *threads = CfgB::THREADS;
+  return reinterpret_cast<const void*>(persist_kernel<CfgB>);
 }
 
 }  // namespace
 
 nt_status persist_prepare(nt_decode_plan* p) {
-  if (p->B != 1)
-    return set_error(NT_ERR_INVALID_ARG, "the persistent launcher runs batch 1; use NT_LAUNCH_GRAPH for batch > 1");
-  int kmax = p->has_head ? p->head_K : 0;
+  int kmax = p->has_head ? p->head_K : 16;
   for (const MatDesc& m : p->mats) kmax = std::max<int>(kmax, (int)padded_k(m.K));
   p->act_stride = (int)padded_k(kmax);
-  p->smem_bytes = kRingBytes + 2 * (size_t)p->act_stride + 2 * kBars * 8 +
-                  kConsumerWarps * sizeof(HeadPartial) + kConsumerWarps * 4 + 16;
-  int optin = 0;
-  NT_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device));
-  if (p->smem_bytes > (size_t)optin)
-    return set_error(NT_ERR_INVALID_ARG, "persistent launcher: K too large for the shared-memory budget (K <= 16384)");
-  NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p->smem_bytes));
-  int per_sm = 0;
-  NT_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, persist_kernel, kThreadsP, p->smem_bytes));
+  if (!pick_config(p->B, p->act_stride, &p->nslots, &p->chunk_b, &p->smem_bytes))
+    return set_error(NT_ERR_INVALID_ARG, "persistent launcher: K too large for the shared-memory budget");
+  NT_TRY(configure_kernel(p->device));
+  int per_sm = 0, threads = 0;
+  const void* kern = kernel_for(p->B, &threads);
+  NT_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, p->smem_bytes));
   if (per_sm < 1) return set_error(NT_ERR_CUDA, "persistent kernel cannot be resident on an SM");
   const int grid = p->sm_count;
   p->grid = grid;
@@ -574,29 +748,32 @@ nt_status persist_prepare(nt_decode_plan* p) {
   const Unitset head{kItemHead, 0, p->head_V, p->head_K};
   int barriers = p->n_qjobs > 0 ? 1 : 0;
   if (p->mode == NT_STEP_INDEPENDENT) {
-    // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table, so every
-    // CTA has the same mix of decode-heavy and decode-free work.
-    std::vector<Unitset> all;
-    for (int i = 0; i < n_proj; ++i) all.push_back(ternary(i));
-    partition_stage(all, grid, false, per_cta);
-    if (p->has_head) partition_stage({head}, grid, false, per_cta);
+    // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table (per pass),
+    // so every CTA has the same mix of decode-heavy and decode-free work.
+    for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) {
+      std::vector<Unitset> all;
+      for (int i = 0; i < n_proj; ++i) all.push_back(ternary(i));
+      partition_stage(all, grid, b0, false, per_cta);
+      if (p->has_head) partition_stage({head}, grid, b0, false, per_cta);
+    }
   } else {
     bool first = true;
+    auto stage = [&](const std::vector<Unitset>& sets) {
+      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b)
+        partition_stage(sets, grid, b0, !first && b0 == 0, per_cta);
+      barriers += first ? 0 : 1;
+      first = false;
+    };
     for (int l = 0; l < p->n_layers; ++l) {
       const int b = l * kProjPerLayer;
       const int groups[4][2] = {{b, 3}, {b + 3, 1}, {b + 4, 2}, {b + 6, 1}};
       for (const auto& g : groups) {
         std::vector<Unitset> sets;
         for (int i = 0; i < g[1]; ++i) sets.push_back(ternary(g[0] + i));
-        partition_stage(sets, grid, !first, per_cta);
-        barriers += first ? 0 : 1;
-        first = false;
+        stage(sets);
       }
     }
-    if (p->has_head) {
-      partition_stage({head}, grid, true, per_cta);
-      ++barriers;
-    }
+    if (p->has_head) stage({head});
   }
   p->n_barriers = barriers;
 
@@ -635,19 +812,61 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.head_V = p->head_V;
   P.head_K = p->head_K;
   P.has_head = p->has_head ? 1 : 0;
-  P.act_stride = p->act_stride;
+  P.B = p->B;
+  P.chunk_b = p->chunk_b;
+  P.nslots = p->nslots;
+  P.act_k = p->act_stride;
   P.launch_idx = (uint32_t)p->launches;
   P.barrier_extra = p->test_fault == 1 ? 1u : 0u;
   P.timeout_ns = p->timeout_ns;
   void* args[] = {&P};
-  const cudaError_t e = cudaLaunchCooperativeKernel((const void*)persist_kernel, dim3(p->grid), dim3(kThreadsP), args,
-                                                    p->smem_bytes, st);
+  int threads = 0;
+  const void* kern = kernel_for(p->B, &threads);
+  const cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p->grid), dim3(threads), args, p->smem_bytes, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return set_error(NT_ERR_CUDA, std::string("persistent launch: ") + cudaGetErrorString(e));
   }
   ++p->launches;
   return NT_OK;
+}
+
+bool persist_head_fits(int K, int B) {
+  int ns, cb;
+  size_t smem;
+  return B >= 1 && B <= kStepMaxBatch && pick_config(B, (int)padded_k(K), &ns, &cb, &smem);
+}
+
+nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
+                              const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
+                              cudaStream_t st) {
+  int dev = 0;
+  NT_CUDA_TRY(cudaGetDevice(&dev));
+  PersistParams P{};
+  P.act_k = (int)padded_k(K);
+  size_t smem = 0;
+  if (!pick_config(B, P.act_k, &P.nslots, &P.chunk_b, &smem))
+    return set_error(NT_ERR_INVALID_ARG, "output projection: K too large for the streaming kernel");
+  NT_TRY(configure_kernel(dev));
+  // The workspace's 16-byte header serves as the control word (error, counter); it is zero
+  // before the first call and every successful call leaves it zero.
+  P.ctrl = reinterpret_cast<StepCtrl*>(ws);
+  P.head_ws = ws;
+  P.head_T = T;
+  P.head_s = s_T;
+  P.head_q = q;
+  P.head_sx = s_x;
+  P.head_logits = logits;
+  P.head_argmax = argmax;
+  P.head_V = V;
+  P.head_K = K;
+  P.has_head = 1;
+  P.B = B;
+  P.timeout_ns = 250000000ull;
+  const int grid = (int)std::min<int64_t>(device_sm_count(), V);
+  if (B == 1) persist_kernel<Cfg1><<<grid, Cfg1::THREADS, smem, st>>>(P);
+  else persist_kernel<CfgB><<<grid, CfgB::THREADS, smem, st>>>(P);
+  return check_launch("persist_kernel (output projection)");
 }
 
 }  // namespace nt

@@ -32,7 +32,7 @@ struct WorkItem {
   int kind;      // kItemTernary (begin/end count tiles of mats[mat]) or kItemHead (rows)
   int mat;
   int flags;
-  int pad_;
+  int b0;        // first activation vector of this pass
   int64_t begin, end;
 };
 
@@ -66,11 +66,18 @@ struct nt_decode_plan {
   size_t sched_item_bytes = 0;
   int grid = 0, n_barriers = 0;
   size_t smem_bytes = 0;
-  int act_stride = 0;               // bytes of one activation buffer in shared memory
+  int act_stride = 0;               // bytes of one activation vector in shared memory
+  int nslots = 0, chunk_b = 0;      // ring slots per consumer warp; vectors per pass
   uint64_t launches = 0;
 };
 
 namespace nt {
 nt_status persist_prepare(nt_decode_plan* p);
 nt_status persist_launch(nt_decode_plan* p, cudaStream_t st);
+// Standalone output projection on the streaming kernel (no plan): B <= 16 and K small
+// enough for its shared-memory activation buffers.
+bool persist_head_fits(int K, int B);
+nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
+                              const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
+                              cudaStream_t st);
 }  // namespace nt

@@ -64,6 +64,16 @@ def projection(workload: int, layer: int, p: int, N: int, K: int, B: int = 1,
     return Projection(name, N, K, w, s_w, x)
 
 
+def projection_x(workload: int, layer: int, p: int, K: int, B: int, seed: int = 0) -> np.ndarray:
+    """Only the fp32 inputs of one projection (the same stream as :func:`projection`)."""
+    return normal(B * K, seed, tag(workload, layer, p, ROLE_X)).reshape(B, K)
+
+
+def head_x(K: int = HEAD_K, B: int = 1, seed: int = 0, workload: int = WL_HEAD) -> np.ndarray:
+    """Only the hidden vectors of the output projection (the same stream as :func:`head`)."""
+    return normal(B * K, seed, tag(workload, 0, 0, ROLE_HIDDEN)).reshape(B, K)
+
+
 def single_gemv(seed: int = 0) -> Projection:
     """The single ternary GEMV: W 1536 x 512, x of length 512, batch 1, seed 0."""
     return projection(WL_SINGLE, 0, 0, SINGLE_N, SINGLE_K, 1, seed, "single")

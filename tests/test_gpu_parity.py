@@ -140,7 +140,7 @@ def _head_call(T, s_T, V, K, q, s, B, ws=None):
     return host(logits), host(am), ws
 
 
-@pytest.mark.parametrize("B", [1, 3])
+@pytest.mark.parametrize("B", [1, 3, 16, 17])
 def test_head_small(B):
     h = wl.head(V=5000, K=4096, B=B, seed=3)
     q, s = oracle.quantize(h.x)
@@ -213,15 +213,33 @@ def test_decode_step_small(launcher, mode):
     plan.close()
 
 
-@pytest.mark.parametrize("B", [2, 4])
-def test_decode_step_batched_graph(B):
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_PERSISTENT, nt.NT_LAUNCH_GRAPH])
+@pytest.mark.parametrize("mode", [nt.NT_STEP_INDEPENDENT, nt.NT_STEP_ORDERED])
+@pytest.mark.parametrize("B", [2, 5, 16])
+def test_decode_step_batched(launcher, mode, B):
+    # Batches above 4 vectors take several passes in the persistent kernel (4 + 1, 4 x 4).
     projs = wl.decoder_projections(1, SMALL, B=B, seed=5, workload=11)
     head = wl.head(V=2000, K=512, B=B, seed=5, workload=11)
     dp, hd = plan_inputs(projs, head, B=B)
-    plan = nt.DecodePlan(1, B, dp, hd, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_GRAPH)
+    plan = nt.DecodePlan(1, B, dp, hd, mode, launcher)
+    for _ in range(2):
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, head, dp, hd, B=B)
+    plan.close()
+
+
+def test_decode_step_batched_8b_down_projection_shape():
+    # K = 12288 activations for 4 vectors fill the shared-memory budget of one pass.
+    shapes = dict(SMALL, down=(512, 12288), gate=(12288, 512), up=(12288, 512))
+    projs = wl.decoder_projections(1, shapes, B=4, seed=8, workload=15)
+    dp, _ = plan_inputs(projs, None, B=4)
+    plan = nt.DecodePlan(1, 4, dp, None, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_PERSISTENT)
     plan.nt_decode_step()
     torch.cuda.synchronize()
-    _check_step(projs, head, dp, hd, B=B)
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, None, dp, None, B=4)
     plan.close()
 
 
