@@ -153,6 +153,8 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
   if (layout == NT_LAYOUT_PLAIN)
     return launch_gemv_plain(static_cast<const uint32_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt,
                              as_stream(stream));
+  if (tc_gemm_supported(B, K))  // prefill-shaped batch: tensor cores
+    return launch_gemm_tc(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, as_stream(stream));
   MatDesc m{};
   m.w = static_cast<const uint8_t*>(w);
   m.s_w = s_w;

@@ -54,4 +54,11 @@ nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
                       cudaStream_t st);
 
+// Tensor-core ternary GEMM (tcgen05, bf16 operands, exact fp32 accumulation) for
+// prefill-shaped batches of at least kTcMinBatch vectors.
+constexpr int kTcMinBatch = 64;
+bool tc_gemm_supported(int M, int K);
+nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
+                         int M, float* y, int32_t* acc, cudaStream_t st);
+
 }  // namespace nt

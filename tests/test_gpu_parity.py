@@ -274,3 +274,41 @@ def test_persistent_timeout_is_reported_and_recoverable():
     assert good.nt_decode_step_status() == nt.NT_OK
     _check_step(projs, None, dp, None)
     good.close()
+
+
+# ---- prefill-shaped batches on the tensor cores -----------------------------------------
+
+TC_SHAPES = [(128, 256, 512), (200, 260, 1024), (64, 20, 528), (256, 3072, 1024),
+             (2048, 1024, 3072), (130, 1024, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+def test_gemm_tensor_cores(M, N, K):
+    p = wl.projection(16, M % 7, N % 5, N, K, M, seed=9)
+    q, s = oracle.quantize(p.x)
+    acc, y, _ = oracle.gemm(p.w_plain, p.s_w, N, K, q, s)
+    gy = torch.full((M, N), float("nan"), device=DEV)
+    gacc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    nt.nt_ternary_gemm(tiled(p.w_plain, N, K), nt.NT_LAYOUT_TILED, dev(p.s_w), N, K, dev(q), dev(s),
+                       M, gy, gacc)
+    assert np.array_equal(host(gacc), acc)
+    assert_close(host(gy), y, f"tensor-core gemm {M}x{N}x{K}")
+
+
+def test_gemm_tensor_cores_cancellation():
+    # Rows of alternating +1/-1 against constant activations cancel to exactly 0; all-+1 rows
+    # against 127 reach 127 * K. A tensor-core accumulator that rounded would miss either.
+    M, N, K = 128, 256, 16384
+    w = np.empty((N, K // 16), dtype=np.uint32)
+    w[0::2] = 0xDDDDDDDD
+    w[1::2] = 0x55555555
+    q = np.full((M, K), 127, dtype=np.int8)
+    q[1::2] = -127
+    s_w = np.ones(N, dtype=np.float32)
+    s = np.ones(M, dtype=np.float32)
+    acc, _, _ = oracle.gemm(w, s_w, N, K, q, s)
+    assert (acc[:, 0::2] == 0).all() and (np.abs(acc[:, 1::2]) == 127 * K).all()
+    gy = torch.empty((M, N), device=DEV)
+    gacc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    nt.nt_ternary_gemm(tiled(w, N, K), nt.NT_LAYOUT_TILED, dev(s_w), N, K, dev(q), dev(s), M, gy, gacc)
+    assert np.array_equal(host(gacc), acc)
