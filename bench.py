@@ -482,6 +482,93 @@ def run_sweep(args):
         plan.close()
 
 
+# ---------------------------------------------------------------------------------------
+# Prefill (not the headline line): the 28-layer small model at M = 2048 and 8192 tokens on
+# the tensor-core GEMM
+# ---------------------------------------------------------------------------------------
+
+def run_prefill(args):
+    import torch
+
+    import oracle
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    shapes, L = wl.SMALL_28, wl.SMALL_28_LAYERS
+    mats = []
+    for layer in range(L):
+        for pi, name in enumerate(wl.PROJ_NAMES):
+            N, K = shapes[name]
+            w = wl.ternary_plain(N, K, 0, wl.tag(wl.WL_PREFILL, layer, pi, wl.ROLE_TRITS))
+            s_w = wl.scales(N, np.sqrt(K), 0, wl.tag(wl.WL_PREFILL, layer, pi, wl.ROLE_ROW_SCALE))
+            wt = torch.empty(nt.nt_repack_size(N, K), dtype=torch.uint8, device=dev)
+            nt.nt_repack_ternary(torch.from_numpy(w.view(np.int32)).to(dev), N, K, wt)
+            mats.append(dict(name=f"L{layer}.{name}", N=N, K=K, w=wt, s_w=torch.from_numpy(s_w).to(dev),
+                             host_w=w if layer == 0 else None, host_sw=s_w if layer == 0 else None))
+    macs = sum(m["N"] * m["K"] for m in mats)
+    peak = 1872.8
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        pass
+    stream = torch.cuda.current_stream()
+    for M in wl.PREFILL_TOKENS:
+        # One fp32 input per distinct K (shared by the layers: values do not change the work),
+        # quantized per token inside the timed pass, then every projection's GEMM.
+        xs = {K: torch.from_numpy(wl.normal(M * K, 0, wl.tag(wl.WL_PREFILL, 99, K, wl.ROLE_X))
+                                  .reshape(M, K)).to(dev) for K in sorted({m["K"] for m in mats})}
+        qs = {K: torch.empty((M, K), dtype=torch.int8, device=dev) for K in xs}
+        ss = {K: torch.empty(M, dtype=torch.float32, device=dev) for K in xs}
+        ys = [torch.empty((M, m["N"]), dtype=torch.float32, device=dev) for m in mats]
+        ws = torch.empty(max(nt.nt_ternary_gemm_workspace_size(m["N"], m["K"], M, nt.NT_LAYOUT_TILED)
+                             for m in mats), dtype=torch.uint8, device=dev)
+
+        def one_pass():
+            for K in xs:
+                nt.nt_quantize_act(xs[K], qs[K], ss[K], stream)
+            for m, y in zip(mats, ys):
+                nt.nt_ternary_gemm(m["w"], nt.NT_LAYOUT_TILED, m["s_w"], m["N"], m["K"], qs[m["K"]],
+                                   ss[m["K"]], M, y, None, ws, stream)
+
+        for _ in range(max(1, args.warmup)):
+            one_pass()
+        torch.cuda.synchronize()
+        # parity: the first layer's projections on 64 sampled tokens
+        rows = np.linspace(0, M - 1, 64).astype(np.int64)
+        parity = "pass"
+        for K in xs:
+            xq, xs_ = oracle.quantize(xs[K].cpu().numpy()[rows])
+            if not np.array_equal(qs[K].cpu().numpy()[rows], xq):
+                parity = "int8 codes differ"
+        for m, y in zip(mats[:7], ys[:7]):
+            xq, xs_ = oracle.quantize(xs[m["K"]].cpu().numpy()[rows])
+            _, yo, _ = oracle.gemm(m["host_w"], m["host_sw"], m["N"], m["K"], xq, xs_)
+            got = y.cpu().numpy()[rows].astype(np.float64)
+            if np.any(np.abs(got - yo) > 1e-6 * np.abs(yo.astype(np.float64))):
+                parity = f"{m['name']} differs"
+        n_pass = max(2, min(args.steps, 20))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(n_pass):
+            one_pass()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / n_pass
+        tflops = 2.0 * M * macs / (ms * 1e-3) / 1e12
+        out_bytes = 4 * M * sum(m["N"] for m in mats)
+        print(json.dumps({"metric": "prefill ternary GEMM (28-layer small model)", "tokens": M,
+                          "passes": n_pass, "ms_per_pass": round(ms, 3),
+                          "tflops": round(tflops, 1), "peak_tflops_bf16": peak,
+                          "frac_of_bf16_peak": round(tflops / peak, 4),
+                          "output_GBps": round(out_bytes / (ms * 1e-3) / 1e9, 1),
+                          "parity": parity}), flush=True)
+        del xs, qs, ss, ys, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,6 +580,8 @@ def main():
                          "for small profiling captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="batched sweep B = 1, 2, 4, 8, 16 (one JSON line per batch)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -504,6 +593,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.prefill:
+        run_prefill(args)
         return
     if world > 1:
         import torch

@@ -142,13 +142,20 @@ nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, in
                           void* stream);
 
 /* Ternary projection of B activation vectors that share the weights (the batched verify
- * pass in "The 0.6B model does not get to decide" scores several positions in one pass).
+ * pass in "The 0.6B model does not get to decide" scores several positions in one pass;
+ * prefill pushes whole prompts through the same weights).
  *   q [B][K] int8, s_x [B], y [B][N] fp32 (output), acc_opt [B][N] int32 or NULL.
  * Results equal B independent nt_ternary_gemv calls, bit for bit. Any B >= 1 is accepted.
+ * With NT_LAYOUT_TILED, B >= 64 and K <= 131072 the call runs on the tensor cores and needs
+ * a workspace of nt_ternary_gemm_workspace_size bytes (16-byte aligned device memory; its
+ * contents are scratch: bf16 copies of this call's activations and weights, overwritten by
+ * the next call that uses it; calls sharing it must not overlap). Otherwise the size is 0
+ * and ws may be NULL. A missing or short workspace returns NT_ERR_WORKSPACE.
  */
+nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes);
 nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, int B, float* y,
-                          int32_t* acc_opt, void* stream);
+                          int32_t* acc_opt, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * int8 output projection with fused greedy arg-max ("A 104 microsecond floor ...": the

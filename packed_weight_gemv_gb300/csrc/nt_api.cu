@@ -143,18 +143,33 @@ nt_status nt_repack_ternary(const uint32_t* w_plain, int N, int K, void* w_tiled
   return launch_repack(w_plain, N, K, static_cast<uint8_t*>(w_tiled), n_invalid_opt, as_stream(stream));
 }
 
+nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes) {
+  clear_error();
+  if (!bytes) return set_error(NT_ERR_INVALID_ARG, "NULL size pointer");
+  if (N < 1 || K < 16 || K % 16 != 0 || B < 1)
+    return set_error(NT_ERR_INVALID_ARG, "need N >= 1, B >= 1 and K a positive multiple of 16");
+  if (layout != NT_LAYOUT_PLAIN && layout != NT_LAYOUT_TILED)
+    return set_error(NT_ERR_INVALID_ARG, "layout must be NT_LAYOUT_PLAIN or NT_LAYOUT_TILED");
+  *bytes = (layout == NT_LAYOUT_TILED && tc_gemm_supported(B, K)) ? tc_gemm_workspace_bytes(B, N, K) : 0;
+  return NT_OK;
+}
+
 nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, int B, float* y, int32_t* acc_opt,
-                          void* stream) {
+                          void* ws, size_t ws_bytes, void* stream) {
   clear_error();
   NT_TRY(validate_ternary(w, layout, s_w, N, K, q, s_x, B, y));
   if (acc_opt && !aligned(acc_opt, 4)) return set_error(NT_ERR_ALIGNMENT, "acc must be 4-byte aligned");
+  const bool tc = layout == NT_LAYOUT_TILED && tc_gemm_supported(B, K);
+  if (tc && (!ws || !aligned(ws, 16) || ws_bytes < tc_gemm_workspace_bytes(B, N, K)))
+    return set_error(NT_ERR_WORKSPACE, "tensor-core path: workspace NULL, misaligned or smaller than "
+                                       "nt_ternary_gemm_workspace_size");
   NT_TRY(check_device());
   if (layout == NT_LAYOUT_PLAIN)
     return launch_gemv_plain(static_cast<const uint32_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt,
                              as_stream(stream));
-  if (tc_gemm_supported(B, K))  // prefill-shaped batch: tensor cores
-    return launch_gemm_tc(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, as_stream(stream));
+  if (tc)  // prefill-shaped batch: tensor cores
+    return launch_gemm_tc(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws, as_stream(stream));
   MatDesc m{};
   m.w = static_cast<const uint8_t*>(w);
   m.s_w = s_w;
@@ -171,7 +186,7 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
 nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, float* y, int32_t* acc_opt,
                           void* stream) {
-  return nt_ternary_gemm(w, layout, s_w, N, K, q, s_x, 1, y, acc_opt, stream);
+  return nt_ternary_gemm(w, layout, s_w, N, K, q, s_x, 1, y, acc_opt, nullptr, 0, stream);
 }
 
 nt_status nt_int8_logits_workspace_size(int V, int K, int B, size_t* bytes) {

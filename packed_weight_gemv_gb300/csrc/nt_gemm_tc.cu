@@ -2,42 +2,56 @@
 // the 5th-generation tensor cores.
 //
 // Y[m][n] = fl(fl(acc[m][n] * s_w[n]) * s_x[m]),  acc = sum_k q[m][k] * t[n][k].
-// Prefill pushes M >= 2048 tokens through the same weights, so the work is a dense contraction
-// (the MLxcel page measures prefill as compute-bound); the batch-1 decode path stays on the
-// streaming kernels.
+// Prefill pushes thousands of tokens through the same weights, so the work is a dense
+// contraction (the MLxcel page measures prefill as compute-bound); batch-1 decode stays on
+// the streaming kernels.
 //
 // Exactness: ternary weights and int8 activations are exact in bf16, each product is an
 // integer of magnitude <= 127, and every partial sum stays below 127 * K < 2^24 for
 // K <= 131072, so the fp32 accumulator in tensor memory holds the exact integer sum; the
 // epilogue applies the same two rounded products as every other path.
 //
-// CTA tile: 128 tokens (MMA M) x 256 weight rows (MMA N); K in steps of 64 through a
-// 4-stage shared-memory pipeline; both operands K-major with the 128-byte swizzle.
-//   warps 0-3 (converters): int8 activations -> bf16 and 2-bit tiled trits -> bf16, written
-//     in the swizzled operand layout; then the epilogue (tensor memory -> scaled fp32 out);
-//   warp 4: allocates the 256 tensor-memory columns; lane 0 issues tcgen05.mma (4 per
-//     K-step, K = 16 each) and commits each stage's completion to its "empty" mbarrier.
-// Every wait is bounded; after a timeout the CTA skips its remaining work (outputs are then
-// invalid) but still frees its tensor memory and waits for its own MMAs.
+// A call runs three kernels:
+//   1. int8 activations -> bf16 [M][K] and 2. tiled trits -> bf16 [N][K], both into the
+//      caller's workspace (operands for this call only; nothing is kept across calls);
+//   3. a persistent GEMM, one CTA per SM, looping over tiles of 128 weight rows (MMA M) x 256
+//      tokens (MMA N):
+//        warp 8 lane 0: 2-D TMA loads (128-byte swizzle) of both operands of each 64-wide K
+//          step into a 4-stage ring (full/empty mbarriers);
+//        warp 9: allocates 512 tensor-memory columns (two 256-column accumulators); lane 0
+//          issues tcgen05.mma (M = 128, N = 256, K = 16; 4 per K step), commits each stage's
+//          release and each finished accumulator;
+//        warps 0-7: epilogue -- tcgen05.ld of a finished accumulator (lane = weight row,
+//          column = token), scales, fp32 stores that are 128-byte coalesced per warp --
+//          overlapping the next tile's MMAs in the other accumulator.
+// Every wait is bounded (2 s); a CTA that gives up still drains its own copies and MMAs and
+// frees its tensor memory.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
 
 #include "nt_kernels.cuh"
 
 namespace nt {
 namespace {
 
-constexpr int kBM = 128;             // tokens per CTA (MMA M)
-constexpr int kBN = 256;             // weight rows per CTA (MMA N)
-constexpr int kBK = 64;              // K per pipeline stage (one 128-byte bf16 row segment)
+constexpr int kBM = 128;             // tokens per tile (MMA M)
+constexpr int kBN = 256;             // weight rows per tile (MMA N)
+constexpr int kBK = 64;              // K per stage: one 128-byte row of bf16
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kConvThreads = 128;
-constexpr int kThreadsTc = kConvThreads + 32;
-constexpr int kTmemCols = 256;
-constexpr uint64_t kTcTimeoutNs = 2000000000ull;  // 2 s per wait
-constexpr int kSmemTc = kStages * kStageBytes + 1024 /* alignment */ + 256 /* barriers */;
+constexpr int kEpiThreads = 256;         // warps 0-7: two per tensor-memory lane quarter
+constexpr int kThreadsTc = kEpiThreads + 64;
+constexpr int kTmemCols = 2 * kBN;       // two accumulators
+constexpr uint64_t kTcTimeoutNs = 2000000000ull;
+constexpr int kSmemTc = kStages * kStageBytes + 1024 /* alignment */ + 2 * kBN * 4 /* token scales */ +
+                        256 /* barriers */;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -47,6 +61,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -58,24 +75,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false after the timeout.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait; false after the timeout or once another role of the CTA has given up.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0u && globaltimer_ns() > deadline) return false;
+    if ((it & 255u) == 0u && (*fail || globaltimer_ns() > deadline)) {
+      *fail = 1;
+      return false;
+    }
   }
 }
 
-// Shared-memory matrix descriptor of a K-major bf16 operand with the 128-byte swizzle: rows
-// of 128 bytes (64 elements), 8-row groups 1024 bytes apart; sm_100 descriptor version 1.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 operand with the 128-byte swizzle (the
+// layout the TMA writes): rows of 128 bytes, 8-row groups 1024 bytes apart; version 1.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);
-  // leading byte offset: 0 (not used by a K-major operand with the 128-byte swizzle)
   d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;  // stride byte offset: 8-row group pitch
-  d |= (uint64_t)1 << 46;                      // descriptor version (sm_100)
-  d |= (uint64_t)2 << 61;                      // layout: 128-byte swizzle
+  d |= (uint64_t)1 << 46;                          // descriptor version (sm_100)
+  d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle
   return d;
 }
 
@@ -93,11 +119,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
 // 4 int8 trits (0x00 / 0x01 / 0xFF bytes) -> 4 bf16 (0, +1.0 = 0x3F80, -1.0 = 0xBF80).
@@ -118,80 +139,81 @@ __device__ __forceinline__ uint2 int8x4_bf16(uint32_t x) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
 }
 
-struct TcParams {
-  const uint8_t* w;   // tiled weights
-  const float* s_w;   // [N]
-  const int8_t* q;    // [M][K]
-  const float* s_x;   // [M]
-  float* y;           // [M][N]
-  int32_t* acc;       // [M][N] or null
-  int M, N, K;
-};
-
-// Converts K-step `ks` of the CTA's operands into stage buffers sa (A) and sb (B).
-__device__ __forceinline__ void convert_stage(const TcParams& p, int m0, int n0, int ks, uint8_t* sa,
-                                              uint8_t* sb, int t) {
-  const int k0 = ks * kBK;
-  // A: token row t (one per thread), 64 int8 -> 64 bf16 (8 swizzled chunks).
-  {
-    const int m = m0 + t;
-    const int8_t* src = p.q + (int64_t)m * p.K + k0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {  // 16 int8 per group -> chunks 2g, 2g+1
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (m < p.M && k0 + 16 * g < p.K) v = __ldg(reinterpret_cast<const uint4*>(src + 16 * g));
-      const uint2 c0 = int8x4_bf16(v.x), c1 = int8x4_bf16(v.y), c2 = int8x4_bf16(v.z), c3 = int8x4_bf16(v.w);
-      *reinterpret_cast<uint4*>(sa + swz(t, 2 * g)) = make_uint4(c0.x, c0.y, c1.x, c1.y);
-      *reinterpret_cast<uint4*>(sa + swz(t, 2 * g + 1)) = make_uint4(c2.x, c2.y, c3.x, c3.y);
-    }
-  }
-  // B: 64 tiles x 4 groups of 16 bytes (4 rows x 16 trits each); 2 groups per thread.
-  {
-    const int64_t Kp = padded_k(p.K), tiles_total = padded_rows(p.N) / 4;
-    const int tl = t >> 1;                    // tile within the CTA's 256 rows
-    const int64_t tile = (int64_t)(n0 >> 2) + tl;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int jj = (t & 1) * 2 + h;         // group within the K-step (0..3)
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (tile < tiles_total) v = __ldg(reinterpret_cast<const uint4*>(p.w + tile * Kp + (int64_t)(k0 / 16 + jj) * 16));
-      const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const Trits16 d = tiled_word_decode(words[r]);
-        const uint2 a0 = trits4_bf16(d.t0), a1 = trits4_bf16(d.t1);
-        const uint2 a2 = trits4_bf16(d.t2), a3 = trits4_bf16(d.t3);
-        const int row = tl * 4 + r;
-        *reinterpret_cast<uint4*>(sb + swz(row, 2 * jj)) = make_uint4(a0.x, a0.y, a1.x, a1.y);
-        *reinterpret_cast<uint4*>(sb + swz(row, 2 * jj + 1)) = make_uint4(a2.x, a2.y, a3.x, a3.y);
-      }
-    }
+// ---- operand conversion --------------------------------------------------------------
+__global__ void __launch_bounds__(256) act_bf16_kernel(const uint4* __restrict__ q, int64_t groups,
+                                                       uint4* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < groups; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldg(q + i);
+    const uint2 c0 = int8x4_bf16(v.x), c1 = int8x4_bf16(v.y), c2 = int8x4_bf16(v.z), c3 = int8x4_bf16(v.w);
+    out[2 * i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+    out[2 * i + 1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
   }
 }
 
-__global__ void __launch_bounds__(kThreadsTc, 1) gemm_tc_kernel(const TcParams p) {
+// Tiled trits -> bf16 [N][K]: one thread per (row, 16-trit word), consecutive threads along K
+// so that each warp writes 32 consecutive 32-byte pieces of a row.
+__global__ void __launch_bounds__(256) trits_bf16_kernel(const uint8_t* __restrict__ w, int N, int K,
+                                                         uint8_t* __restrict__ out) {
+  const int kg = K / 16;
+  const int64_t Kp = padded_k(K), total = (int64_t)N * kg;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / kg, j = i % kg;
+    const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(w + (n >> 2) * Kp + j * 16 + (n & 3) * 4));
+    const Trits16 d = tiled_word_decode(word);
+    const uint2 a0 = trits4_bf16(d.t0), a1 = trits4_bf16(d.t1), a2 = trits4_bf16(d.t2), a3 = trits4_bf16(d.t3);
+    uint4* dst = reinterpret_cast<uint4*>(out + (n * K + j * 16) * 2);
+    dst[0] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+    dst[1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+  }
+}
+
+// ---- GEMM ------------------------------------------------------------------------------
+// The weights are the MMA's M side (128 rows per tile) and the tokens its N side (256 per
+// tile), so tensor-memory lane = weight row and column = token: each epilogue store of one
+// column by a warp is 32 consecutive floats of one output row.
+struct TcParams {
+  const float* s_w;  // [N]
+  const float* s_x;  // [M]
+  float* y;          // [M][N]
+  int32_t* acc;      // [M][N] or null
+  int M, N, K;
+  int tiles_n, tiles_m;  // 128-row weight tiles, 256-token tiles
+};
+
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  // Operand stages must sit on 1024-byte boundaries (swizzle atom).
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
-  volatile int* s_fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages), accbar = smem_u32(bars + 2 * kStages);
+  float* sxs = reinterpret_cast<float*>(smem + kStages * kStageBytes);  // [2][kBN] token scales
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sxs + 2 * kBN);
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * kStages;
+  const uint32_t tfull0 = empty0 + 8 * kStages, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
-  const int ksteps = (int)(padded_k(p.K) / kBK);
+  const int n_tiles = p.tiles_n * p.tiles_m;
+  const int ksteps = (p.K + kBK - 1) / kBK;
+  constexpr int kProducerWarp = kEpiThreads / 32, kMmaWarp = kProducerWarp + 1;
 
   if (t == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, kConvThreads);
+      mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(accbar, 1);
-    *s_fail = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, kEpiThreads);
+    }
+    mbar_init(drain, 1);
+    *fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -202,78 +224,174 @@ __global__ void __launch_bounds__(kThreadsTc, 1) gemm_tc_kernel(const TcParams p
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
-    if (lane == 0) {  // MMA issuer
-      for (int ks = 0; ks < ksteps; ++ks) {
-        const int s = ks % kStages;
-        if (!mbar_wait(full0 + 8 * s, (uint32_t)(ks / kStages) & 1u)) { *s_fail = 1; break; }
+  if (warp == kProducerWarp && lane == 0) {
+    // ---- TMA producer ----
+    uint32_t it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles && !*fail; tile += gridDim.x) {
+      const int tn = tile % p.tiles_n, tm = tile / p.tiles_n;
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const uint32_t s = it % kStages;
+        if (it >= kStages && !mbar_wait(empty0 + 8 * s, ((it / kStages) - 1) & 1u, fail)) break;
+        const uint32_t a = smem_u32(smem + s * kStageBytes);
+        mbar_expect_tx(full0 + 8 * s, kStageBytes);
+        tma_load_2d(a, &tmW, ks * kBK, tn * kBM, full0 + 8 * s);
+        tma_load_2d(a + kABytes, &tmX, ks * kBK, tm * kBN, full0 + 8 * s);
+      }
+    }
+    // Drain: the last copy issued into each stage must land before the CTA may exit.
+    for (uint32_t s = 0; s < kStages && s < it; ++s) {
+      const uint32_t last = (it - 1 - s) / kStages * kStages + s;
+      const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
+      while (!mbar_try_wait(full0 + 8 * s, (last / kStages) & 1u))
+        if (globaltimer_ns() > deadline) break;
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ---- MMA issuer ----
+    uint32_t it = 0, j = 0;
+    for (int tile = blockIdx.x; tile < n_tiles && !*fail; tile += gridDim.x, ++j) {
+      const uint32_t buf = j & 1u;
+      if (j >= 2 && !mbar_wait(tempty0 + 8 * buf, ((j >> 1) - 1) & 1u, fail)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t d = tmem + buf * kBN;
+      bool ok = true;
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const uint32_t s = it % kStages;
+        if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1u, fail)) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t a = smem_u32(smem + s * kStageBytes), b = a + kABytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_bf16(tmem, sdesc_sw128(a + kk * 32), sdesc_sw128(b + kk * 32), (ks | kk) != 0);
-        mma_commit(empty0 + 8 * s);  // stage s free once these MMAs have read it
+          mma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(b + kk * 32), (ks | kk) != 0);
+        mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
       }
-      mma_commit(accbar);  // accumulator complete (or, after a failure, MMAs drained)
+      if (!ok) break;
+      mma_commit(tfull0 + 8 * buf);  // accumulator buf complete
     }
-  } else {
-    // Converters: fill stage s once the MMAs of K-step ks - kStages have released it.
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kStages;
-      if (ks >= kStages && !mbar_wait(empty0 + 8 * s, (uint32_t)(ks / kStages - 1) & 1u)) { *s_fail = 1; }
-      if (*s_fail) break;
-      uint8_t* sa = smem + s * kStageBytes;
-      convert_stage(p, m0, n0, ks, sa, sa + kABytes, t);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core
-      mbar_arrive(full0 + 8 * s);
-    }
-    // Epilogue: thread t owns token row m0 + t (tensor-memory lane t).
-    const bool ok = mbar_wait(accbar, 0);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int m = m0 + t;
-    const float sx = (m < p.M) ? p.s_x[m] : 0.0f;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c0 = 0; c0 < kBN; c0 += 16) {
-      uint32_t r[16];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(lane_base + (uint32_t)c0)
-          : "memory");
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (!ok || *s_fail || m >= p.M) continue;
+    mma_commit(drain);  // every MMA of this CTA done (waited below before the memory is freed)
+    const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
+    while (!mbar_try_wait(drain, 0))
+      if (globaltimer_ns() > deadline) break;
+  } else if (warp < kProducerWarp) {
+    // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. +31 (weight rows) and
+    // columns (tokens) [128 (w / 4), +128) of the finished accumulator ----
+    const int quarter = warp & 3, half = warp >> 2;
+    uint32_t j = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
+      const uint32_t buf = j & 1u;
+      const int tn = tile % p.tiles_n, tm = tile / p.tiles_n;
+      const int n = tn * kBM + quarter * 32 + lane, m0 = tm * kBN;
+      sxs[buf * kBN + t] = (m0 + t < p.M) ? __ldg(p.s_x + m0 + t) : 0.0f;
+      const float sw = (n < p.N) ? __ldg(p.s_w + n) : 0.0f;
+      epi_sync();  // token scales of this tile visible to every epilogue thread
+      // After a failed wait the thread keeps walking the tiles (the named barrier above needs
+      // every epilogue thread) and only skips the stores.
+      const bool ok = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1u, fail);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const uint32_t base = tmem + buf * kBN + half * (kBN / 2) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBN / 2; c0 += 16) {
+        uint32_t r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7), "=r"(r8), "=r"(r9),
+              "=r"(r10), "=r"(r11), "=r"(r12), "=r"(r13), "=r"(r14), "=r"(r15)
+            : "r"(base + (uint32_t)c0)
+            : "memory");
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const uint32_t r[16] = {r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15};
+        const int mc = m0 + half * (kBN / 2) + c0;
+        if (ok && n < p.N) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int n = n0 + c0 + j;
-        if (n < p.N) {
-          const float a = __int_as_float((int)r[j]);  // an exact integer
-          p.y[(int64_t)m * p.N + n] = __fmul_rn(__fmul_rn(a, __ldg(p.s_w + n)), sx);
-          if (p.acc) p.acc[(int64_t)m * p.N + n] = __float2int_rn(a);
+          for (int q = 0; q < 16; ++q) {
+            const int m = mc + q;
+            if (m < p.M) {
+              const float a = __int_as_float((int)r[q]);  // an exact integer
+              p.y[(int64_t)m * p.N + n] = __fmul_rn(__fmul_rn(a, sw), sxs[buf * kBN + half * (kBN / 2) + c0 + q]);
+              if (p.acc) p.acc[(int64_t)m * p.N + n] = __float2int_rn(a);
+            }
+          }
         }
       }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(tempty0 + 8 * buf);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 4)
+  if (warp == kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
+
+// ---- host ----------------------------------------------------------------------------
+std::mutex g_tc_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_tc_attr[64] = {};
+
+nt_status tc_setup(int dev) {
+  std::lock_guard<std::mutex> lock(g_tc_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    NT_CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || !fn) return set_error(NT_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (dev >= 0 && dev < 64 && !g_tc_attr[dev]) {
+    NT_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc));
+    g_tc_attr[dev] = true;
+  }
+  return NT_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][K] matrix, box 64 (K) x box_rows, 128B swizzle.
+nt_status encode_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(NT_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return NT_OK;
+}
+
+size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace
 
 bool tc_gemm_supported(int M, int K) { return M >= kTcMinBatch && K <= 131072; }
 
+size_t tc_gemm_workspace_bytes(int M, int N, int K) {
+  return align256((size_t)M * K * 2) + align256((size_t)N * K * 2);
+}
+
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
-                         int M, float* y, int32_t* acc, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    NT_CUDA_TRY(cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc));
-    attr_set = true;
+                         int M, float* y, int32_t* acc, void* ws, cudaStream_t st) {
+  int dev = 0;
+  NT_CUDA_TRY(cudaGetDevice(&dev));
+  NT_TRY(tc_setup(dev));
+  uint8_t* a_bf16 = static_cast<uint8_t*>(ws);
+  uint8_t* b_bf16 = a_bf16 + align256((size_t)M * K * 2);
+  const int sms = device_sm_count();
+  {
+    const int64_t groups = (int64_t)M * K / 16;
+    const int g = (int)std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 8);
+    act_bf16_kernel<<<g, 256, 0, st>>>(reinterpret_cast<const uint4*>(q), groups, reinterpret_cast<uint4*>(a_bf16));
+    NT_TRY(check_launch("act_bf16_kernel"));
   }
-  TcParams p{w, s_w, q, s_x, y, acc, M, N, K};
-  const dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN);
-  gemm_tc_kernel<<<grid, kThreadsTc, kSmemTc, st>>>(p);
+  {
+    const int64_t total = (int64_t)N * (K / 16);
+    const int g = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
+    trits_bf16_kernel<<<g, 256, 0, st>>>(w, N, K, b_bf16);
+    NT_TRY(check_launch("trits_bf16_kernel"));
+  }
+  CUtensorMap mw, mx;
+  NT_TRY(encode_map(&mw, b_bf16, N, K, kBM));  // weights: MMA M side, 128-row boxes
+  NT_TRY(encode_map(&mx, a_bf16, M, K, kBN));  // tokens: MMA N side, 256-row boxes
+  TcParams p{s_w, s_x, y, acc, M, N, K, (N + kBM - 1) / kBM, (M + kBN - 1) / kBN};
+  const int tiles = p.tiles_m * p.tiles_n;
+  gemm_tc_kernel<<<std::min(tiles, sms), kThreadsTc, kSmemTc, st>>>(mw, mx, p);
   return check_launch("gemm_tc_kernel");
 }
 

@@ -58,7 +58,8 @@ nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int
 // prefill-shaped batches of at least kTcMinBatch vectors.
 constexpr int kTcMinBatch = 64;
 bool tc_gemm_supported(int M, int K);
+size_t tc_gemm_workspace_bytes(int M, int N, int K);
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
-                         int M, float* y, int32_t* acc, cudaStream_t st);
+                         int M, float* y, int32_t* acc, void* ws, cudaStream_t st);
 
 }  // namespace nt

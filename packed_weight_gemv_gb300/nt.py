@@ -37,7 +37,7 @@ NT_LAUNCH_STREAM = 2
 EXPORTS = (
     "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
-    "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
+    "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
     "nt_int8_logits_argmax_noalloc",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
     "nt_decode_plan_destroy",
@@ -92,7 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_repack_size": ([i, i, ctypes.POINTER(sz)], i),
             "nt_repack_ternary": ([vp, i, i, vp, vp, vp], i),
             "nt_ternary_gemv": ([vp, i, vp, i, i, vp, vp, vp, vp, vp], i),
-            "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp], i),
+            "nt_ternary_gemm_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], i),
+            "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
             "nt_int8_logits_workspace_size": ([i, i, i, ctypes.POINTER(sz)], i),
             "nt_int8_logits_argmax": ([vp, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
             "nt_int8_logits_argmax_noalloc": ([vp, vp, i, i, vp, vp, i, vp, vp, vp], i),
@@ -162,11 +163,21 @@ def nt_ternary_gemv(w: torch.Tensor, layout: int, s_w: torch.Tensor, N: int, K: 
                                           _ptr(y), _ptr(acc), _stream(stream)), "nt_ternary_gemv")
 
 
+def nt_ternary_gemm_workspace_size(N: int, K: int, B: int, layout: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().nt_ternary_gemm_workspace_size(N, K, B, layout, ctypes.byref(n)),
+           "nt_ternary_gemm_workspace_size")
+    return n.value
+
+
 def nt_ternary_gemm(w: torch.Tensor, layout: int, s_w: torch.Tensor, N: int, K: int,
                     q: torch.Tensor, s_x: torch.Tensor, B: int, y: torch.Tensor,
-                    acc: Optional[torch.Tensor] = None, stream=None):
+                    acc: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+                    stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load_library().nt_ternary_gemm(_ptr(w), layout, _ptr(s_w), N, K, _ptr(q), _ptr(s_x), B,
-                                          _ptr(y), _ptr(acc), _stream(stream)), "nt_ternary_gemm")
+                                          _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream)),
+           "nt_ternary_gemm")
 
 
 def nt_int8_logits_workspace_size(V: int, K: int, B: int) -> int:

@@ -52,7 +52,7 @@ def test_size_queries(lib):
 def _gemv(lib, w, layout, N, K, q, y, B=1):
     vp = ctypes.c_void_p
     return lib.nt_ternary_gemm(vp(w), layout, vp(0x1000), N, K, vp(q), vp(0x2000), B, vp(y),
-                               None, None)
+                               None, None, 0, None)
 
 
 def test_argument_errors_without_gpu(lib):
@@ -63,6 +63,10 @@ def test_argument_errors_without_gpu(lib):
     assert _gemv(lib, 0x10008, 1, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_ALIGNMENT
     assert _gemv(lib, 0x10000, 1, 16, 16, 0x20004, 0x30000) == nt.NT_ERR_ALIGNMENT
     assert _gemv(lib, 0, 1, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
+    # the tensor-core path (tiled, B >= 64) needs a workspace: refused before any device call
+    assert _gemv(lib, 0x10000, 1, 256, 512, 0x20000, 0x30000, B=64) == nt.NT_ERR_WORKSPACE
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == 64 * 512 * 2 + 256 * 512 * 2
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == 0
     assert b"multiple of 16" in lib.nt_last_error_string() or True
     vp = ctypes.c_void_p
     assert lib.nt_quantize_act(None, 1, 16, vp(0x100), vp(0x200), None) == nt.NT_ERR_INVALID_ARG

@@ -289,8 +289,11 @@ def test_gemm_tensor_cores(M, N, K):
     acc, y, _ = oracle.gemm(p.w_plain, p.s_w, N, K, q, s)
     gy = torch.full((M, N), float("nan"), device=DEV)
     gacc = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    ws = torch.empty(nt.nt_ternary_gemm_workspace_size(N, K, M, nt.NT_LAYOUT_TILED), dtype=torch.uint8,
+                     device=DEV)
+    assert ws.numel() > 0
     nt.nt_ternary_gemm(tiled(p.w_plain, N, K), nt.NT_LAYOUT_TILED, dev(p.s_w), N, K, dev(q), dev(s),
-                       M, gy, gacc)
+                       M, gy, gacc, ws)
     assert np.array_equal(host(gacc), acc)
     assert_close(host(gy), y, f"tensor-core gemm {M}x{N}x{K}")
 
@@ -310,5 +313,7 @@ def test_gemm_tensor_cores_cancellation():
     assert (acc[:, 0::2] == 0).all() and (np.abs(acc[:, 1::2]) == 127 * K).all()
     gy = torch.empty((M, N), device=DEV)
     gacc = torch.empty((M, N), dtype=torch.int32, device=DEV)
-    nt.nt_ternary_gemm(tiled(w, N, K), nt.NT_LAYOUT_TILED, dev(s_w), N, K, dev(q), dev(s), M, gy, gacc)
+    ws = torch.empty(nt.nt_ternary_gemm_workspace_size(N, K, M, nt.NT_LAYOUT_TILED), dtype=torch.uint8,
+                     device=DEV)
+    nt.nt_ternary_gemm(tiled(w, N, K), nt.NT_LAYOUT_TILED, dev(s_w), N, K, dev(q), dev(s), M, gy, gacc, ws)
     assert np.array_equal(host(gacc), acc)
