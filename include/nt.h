@@ -264,6 +264,19 @@ nt_status nt_decode_step_status(nt_decode_plan* plan, nt_status* device_status);
 /* Clears the plan's device-side error word and barrier counters (synchronous). */
 nt_status nt_decode_plan_reset(nt_decode_plan* plan);
 
+/* Step timeline of the persistent launcher, the instrumentation "A 104 microsecond floor
+ * ..." describes for one decoder step (Fig. 1: DRAM time against launch/dependency latency).
+ * nt_decode_plan_trace_layout reports the grid size G and the number of grid barriers S per
+ * step (host ints). A trace buffer is G * (S + 1) * 4 device uint64 values; record (c, b) =
+ * trace[(c * (S + 1) + b) * 4 + i] holds %globaltimer nanoseconds of CTA c:
+ *   b = 0:      i = 0 kernel start, i = 1 consumers done with the whole step;
+ *   b = 1..S:   i = 0 consumers done with the work before barrier b, i = 1 barrier b passed,
+ *               i = 2 the next stage's activations in shared memory.
+ * nt_decode_plan_set_trace installs (or, with NULL, removes) the buffer; every later step
+ * of the plan overwrites it. Other launchers and stream/graph plans record nothing. */
+nt_status nt_decode_plan_trace_layout(const nt_decode_plan* plan, int* grid, int* barriers);
+nt_status nt_decode_plan_set_trace(nt_decode_plan* plan, unsigned long long* trace);
+
 /* Releases the plan and everything it allocated. NULL is ignored. */
 void nt_decode_plan_destroy(nt_decode_plan* plan);
 

@@ -83,7 +83,14 @@ struct PersistParams {
   uint32_t launch_idx;
   uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
   uint64_t timeout_ns;
+  unsigned long long* trace;  // optional timeline: [grid][n_barriers + 1][4]
 };
+
+// One timeline stamp (thread 0 of the consumers only).
+__device__ __forceinline__ void stamp(const PersistParams& P, int b, int i) {
+  if (P.trace && threadIdx.x == 0)
+    P.trace[((int64_t)blockIdx.x * (P.n_barriers + 1) + b) * 4 + i] = globaltimer_ns();
+}
 
 struct SmemLayout {
   int ring, act, bars, hbest, red, abort_flag, total;
@@ -352,9 +359,10 @@ __device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_ou
 
 // Grid-wide barrier among the consumers of all CTAs; `target` counts arrivals modulo 2^32.
 template <class C>
-__device__ void grid_barrier(const PersistParams& P, uint32_t target, volatile int* s_abort) {
+__device__ void grid_barrier(const PersistParams& P, uint32_t target, int b, volatile int* s_abort) {
   target += P.barrier_extra;
   consumer_sync<C>();
+  stamp(P, b, 0);
   if (threadIdx.x == 0 && !*s_abort) {
     __threadfence();
     red_release_add(&P.ctrl->arrive, 1u);
@@ -367,6 +375,7 @@ __device__ void grid_barrier(const PersistParams& P, uint32_t target, volatile i
       }
     }
   }
+  stamp(P, b, 1);
   consumer_sync<C>();
 }
 
@@ -540,6 +549,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   __syncthreads();
 
   const int n_items = item_count(P);
+  stamp(P, 0, 0);
   if (warp == C::CW) {
     if (lane < C::CW) producer<C>(P, n_items, ring, full0, empty0, s_abort, lane);
     return;
@@ -562,7 +572,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
         quantize_consumers<C>(qj.x + (int64_t)b * qj.K, qj.K, qj.q + (int64_t)b * qj.K, qj.s + b, red);
     }
     ++barriers;
-    grid_barrier<C>(P, barrier_base + barriers * gridDim.x, s_abort);
+    grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
+    stamp(P, (int)barriers, 2);
   }
 
   const int act_buf = P.chunk_b * P.act_k;
@@ -570,9 +581,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   bool prefetched = false;
   for (int i = 0; i < n_items; ++i) {
     const WorkItem it = get_item(P, i);
-    if (it.flags & kFlagStage) {
+    const bool staged = (it.flags & kFlagStage) != 0;
+    if (staged) {
       ++barriers;
-      grid_barrier<C>(P, barrier_base + barriers * gridDim.x, s_abort);
+      grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
     }
     int K, nb;
     const int8_t* q = item_act(P, it, K, nb);
@@ -580,6 +592,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     if (prefetched) cp_async_wait_all();
     else load_act<C>(abuf, q, K, nb, P.act_k, false);
     consumer_sync<C>();  // act[buf] complete; every warp is past the previous item
+    if (staged) stamp(P, (int)barriers, 2);
     prefetched = false;
     if (i + 1 < n_items) {
       const WorkItem nx = get_item(P, i + 1);
@@ -604,6 +617,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     buf ^= 1;
   }
   if (prefetched) cp_async_wait_all();
+  consumer_sync<C>();
+  stamp(P, 0, 1);
 
   if (P.has_head) {  // CTA best per vector, then the last CTA to finish reduces all CTAs
     volatile int& s_last = *reinterpret_cast<volatile int*>(smem + L.abort_flag + 4);
@@ -819,6 +834,7 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.launch_idx = (uint32_t)p->launches;
   P.barrier_extra = p->test_fault == 1 ? 1u : 0u;
   P.timeout_ns = p->timeout_ns;
+  P.trace = p->trace;
   void* args[] = {&P};
   int threads = 0;
   const void* kern = kernel_for(p->B, &threads);

@@ -241,6 +241,22 @@ nt_status nt_decode_plan_reset(nt_decode_plan* p) {
   return NT_OK;
 }
 
+nt_status nt_decode_plan_trace_layout(const nt_decode_plan* p, int* grid, int* barriers) {
+  clear_error();
+  if (!p || !grid || !barriers) return set_error(NT_ERR_INVALID_ARG, "NULL argument");
+  *grid = p->launcher == NT_LAUNCH_PERSISTENT ? p->grid : 0;
+  *barriers = p->launcher == NT_LAUNCH_PERSISTENT ? p->n_barriers : 0;
+  return NT_OK;
+}
+
+nt_status nt_decode_plan_set_trace(nt_decode_plan* p, unsigned long long* trace) {
+  clear_error();
+  if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
+  if (trace && !aligned(trace, 8)) return set_error(NT_ERR_ALIGNMENT, "trace must be 8-byte aligned");
+  p->trace = trace;
+  return NT_OK;
+}
+
 void nt_decode_plan_destroy(nt_decode_plan* p) {
   if (!p) return;
   cudaDeviceSynchronize();

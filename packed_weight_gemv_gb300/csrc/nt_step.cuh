@@ -69,6 +69,7 @@ struct nt_decode_plan {
   int act_stride = 0;               // bytes of one activation vector in shared memory
   int nslots = 0, chunk_b = 0;      // ring slots per consumer warp; vectors per pass
   uint64_t launches = 0;
+  unsigned long long* trace = nullptr;  // optional step timeline (nt_decode_plan_set_trace)
 };
 
 namespace nt {

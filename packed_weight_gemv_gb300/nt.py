@@ -40,7 +40,7 @@ EXPORTS = (
     "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
     "nt_int8_logits_argmax_noalloc",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
-    "nt_decode_plan_destroy",
+    "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_destroy",
 )
 
 
@@ -101,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_decode_step": ([vp, vp], i),
             "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
             "nt_decode_plan_reset": ([vp], i),
+            "nt_decode_plan_trace_layout": ([vp, ctypes.POINTER(i), ctypes.POINTER(i)], i),
+            "nt_decode_plan_set_trace": ([vp, vp], i),
             "nt_decode_plan_destroy": ([vp], None),
         }
         for name, (args, res) in sig.items():
@@ -252,6 +254,18 @@ class DecodePlan:
 
     def nt_decode_plan_reset(self):
         _check(load_library().nt_decode_plan_reset(self._h), "nt_decode_plan_reset")
+
+    def nt_decode_plan_trace_layout(self):
+        """(grid, barriers per step) of the persistent launcher's timeline."""
+        g, b = ctypes.c_int(0), ctypes.c_int(0)
+        _check(load_library().nt_decode_plan_trace_layout(self._h, ctypes.byref(g), ctypes.byref(b)),
+               "nt_decode_plan_trace_layout")
+        return g.value, b.value
+
+    def nt_decode_plan_set_trace(self, trace: Optional[torch.Tensor]):
+        """Installs a device int64 tensor of grid * (barriers + 1) * 4 values (or None)."""
+        self._trace = trace
+        _check(load_library().nt_decode_plan_set_trace(self._h, _ptr(trace)), "nt_decode_plan_set_trace")
 
     def close(self):
         if getattr(self, "_h", None) and self._h.value:
