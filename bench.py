@@ -526,12 +526,12 @@ def run_prefill(args):
         ws = torch.empty(max(nt.nt_ternary_gemm_workspace_size(m["N"], m["K"], M, nt.NT_LAYOUT_TILED)
                              for m in mats), dtype=torch.uint8, device=dev)
 
-        def one_pass():
+        def one_pass():  # on the current stream (the capture stream while a graph records)
             for K in xs:
-                nt.nt_quantize_act(xs[K], qs[K], ss[K], stream)
+                nt.nt_quantize_act(xs[K], qs[K], ss[K])
             for m, y in zip(mats, ys):
                 nt.nt_ternary_gemm(m["w"], nt.NT_LAYOUT_TILED, m["s_w"], m["N"], m["K"], qs[m["K"]],
-                                   ss[m["K"]], M, y, None, ws, stream)
+                                   ss[m["K"]], M, y, None, ws)
 
         for _ in range(max(1, args.warmup)):
             one_pass()
@@ -556,15 +556,29 @@ def run_prefill(args):
             one_pass()
         ev1.record(stream)
         torch.cuda.synchronize()
+        ms_eager = ev0.elapsed_time(ev1) / n_pass
+        # The same calls captured once in a CUDA graph and replayed (no host work per call).
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_pass()
+        graph.replay()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(n_pass):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1) / n_pass
         tflops = 2.0 * M * macs / (ms * 1e-3) / 1e12
         out_bytes = 4 * M * sum(m["N"] for m in mats)
         print(json.dumps({"metric": "prefill ternary GEMM (28-layer small model)", "tokens": M,
                           "passes": n_pass, "ms_per_pass": round(ms, 3),
+                          "ms_per_pass_eager": round(ms_eager, 3),
                           "tflops": round(tflops, 1), "peak_tflops_bf16": peak,
                           "frac_of_bf16_peak": round(tflops / peak, 4),
                           "output_GBps": round(out_bytes / (ms * 1e-3) / 1e9, 1),
                           "parity": parity}), flush=True)
+        del graph
         del xs, qs, ss, ys, ws
         torch.cuda.empty_cache()
 
