@@ -13,7 +13,9 @@ Every function takes and returns numpy arrays and runs the plain loops of ``orac
 * :func:`logits_argmax` -- int8 output projection with the lowest-index arg-max;
 * :func:`unpack_plain`, :func:`count_invalid` -- the plain exchange format;
 * :func:`repack_tiled`, :func:`unpack_tiled` -- the library's tiled layout, from its
-  written definition.
+  written definition;
+* :func:`embed_rows` -- the input-table rows of the current tokens, dequantized;
+* :func:`verify_accept` -- the longest agreeing prefix of a batched verify pass.
 
 Pins (``tests/test_oracle_*.py``) tie each of these to brute force, closed forms, invariants
 and hand-worked fixtures under ``tests/golden/``.
@@ -85,6 +87,10 @@ class Oracle:
         lib.orc_repack_tiled.restype = None
         lib.orc_unpack_tiled.argtypes = [vp, i32, i32, vp]
         lib.orc_unpack_tiled.restype = i32
+        lib.orc_embed_rows.argtypes = [vp, vp, i32, i32, vp, i32, vp]
+        lib.orc_embed_rows.restype = i32
+        lib.orc_verify_accept.argtypes = [vp, vp, i32, vp]
+        lib.orc_verify_accept.restype = i32
         self.lib = lib
 
     def threads(self) -> int:
@@ -176,6 +182,28 @@ class Oracle:
         return t
 
 
+    def embed_rows(self, T, s_T, V: int, K: int, tokens):
+        """Selected input-table rows dequantized: (x fp32 [B, K], number of bad tokens)."""
+        T = _c(T, np.int8)
+        sT = _c(s_T, np.float32)
+        tok = _c(tokens, np.int32).reshape(-1)
+        x = np.empty((tok.size, K), dtype=np.float32)
+        bad = self.lib.orc_embed_rows(T.ctypes.data, sT.ctypes.data, V, K, tok.ctypes.data, tok.size,
+                                      x.ctypes.data)
+        return x, int(bad)
+
+    def verify_accept(self, draft, argmax):
+        """Longest agreeing prefix of a verify pass: (emitted tokens int32 [n])."""
+        am = _c(argmax, np.int32).reshape(-1)
+        B = am.size
+        d = _c(draft, np.int32).reshape(-1)
+        assert d.size == B - 1
+        emit = np.empty(B, dtype=np.int32)
+        n = self.lib.orc_verify_accept(d.ctypes.data if d.size else None, am.ctypes.data, B,
+                                       emit.ctypes.data)
+        return emit[:n]
+
+
 def default() -> Oracle:
     global _lib
     with _lock:
@@ -222,3 +250,11 @@ def repack_tiled(w_plain, N, K):
 
 def unpack_tiled(tiled, N, K):
     return default().unpack_tiled(tiled, N, K)
+
+
+def embed_rows(T, s_T, V, K, tokens):
+    return default().embed_rows(T, s_T, V, K, tokens)
+
+
+def verify_accept(draft, argmax):
+    return default().verify_accept(draft, argmax)

@@ -242,3 +242,38 @@ int orc_unpack_tiled(const uint8_t* tiled, int N, int K, int8_t* t) {
     }
   return status;
 }
+
+/* ---- input-table row gather ("The file is not the traffic": of the input table only the
+ * rows of the current tokens are read) ----------------------------------------------------
+ * x[b][k] = fp32((float)T[tok[b]][k] * s[tok[b]]) -- the int8 value is exact in fp32, one
+ * rounded product. A token outside [0, V) gives a row of zeros and is counted. */
+int orc_embed_rows(const int8_t* T, const float* s, int V, int K, const int32_t* tok, int B, float* x) {
+  int bad = 0;
+  for (int b = 0; b < B; ++b) {
+    const int t = tok[b];
+    for (int k = 0; k < K; ++k) {
+      float v = 0.0f;
+      if (t >= 0 && t < V) v = (float)T[(int64_t)t * K + k] * s[t];
+      x[(int64_t)b * K + k] = v;
+    }
+    if (t < 0 || t >= V) ++bad;
+  }
+  return bad;
+}
+
+/* ---- verify-pass acceptance ("The 0.6B model does not get to decide": the large model
+ * scores every drafted position in one pass, the longest prefix where the draft agrees with
+ * it is kept, and at the first disagreement the large model's own token is emitted) -------
+ * Positions 0..B-1 of the verify pass hold the last emitted token followed by the B-1
+ * drafted tokens draft[0..B-2]; argmax[i] is the large model's greedy token after position i.
+ * Draft token i is accepted when it equals argmax[i] and every earlier draft was accepted.
+ * With j accepted drafts the emitted tokens are draft[0..j-1] then argmax[j]; returns j + 1. */
+int orc_verify_accept(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit) {
+  int j = 0;
+  while (j < B - 1 && draft[j] == argmax[j]) {
+    emit[j] = draft[j];
+    ++j;
+  }
+  emit[j] = argmax[j];
+  return j + 1;
+}

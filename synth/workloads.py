@@ -20,7 +20,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import int8_uniform, normal, scales, ternary_plain
+from . import draws, int8_uniform, normal, scales, ternary_plain
 
 PROJ_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
 
@@ -36,8 +36,9 @@ SINGLE_N, SINGLE_K = 1536, 512
 SWEEP_BATCHES = (1, 2, 4, 8, 16)
 PREFILL_TOKENS = (2048, 8192)
 
-WL_SINGLE, WL_DECODE, WL_HEAD, WL_SWEEP, WL_PREFILL = 1, 2, 3, 4, 5
+WL_SINGLE, WL_DECODE, WL_HEAD, WL_SWEEP, WL_PREFILL, WL_EMBED = 1, 2, 3, 4, 5, 6
 ROLE_TRITS, ROLE_ROW_SCALE, ROLE_X, ROLE_TABLE, ROLE_TABLE_SCALE, ROLE_HIDDEN = 1, 2, 3, 4, 5, 6
+ROLE_TOKENS, ROLE_DRAFT = 7, 8
 
 
 def tag(workload: int, layer: int, proj: int, role: int) -> int:
@@ -127,3 +128,33 @@ def head_bytes(V: int = HEAD_V, K: int = HEAD_K, B: int = 1, with_logits: bool =
     """Algorithmic bytes of the output projection: int8 table, fp32 row scales, int8 hidden,
     activation scale, fp32 logits (optional) and the int32 arg-max."""
     return V * K + 4 * V + B * K + 4 * B + (4 * B * V if with_logits else 0) + 4 * B
+
+
+@dataclass
+class Embedding:
+    """The int8 input table and the tokens whose rows one step gathers."""
+    V: int
+    K: int
+    T: np.ndarray       # int8 [V, K], uniform integers in [-127, 127]
+    s_T: np.ndarray     # fp32 [V], U[0.5,1.5)/127
+    tokens: np.ndarray  # int32 [B], uniform in [0, V)
+
+
+def embedding(V: int = HEAD_V, K: int = HEAD_K, B: int = 1, seed: int = 0,
+              workload: int = WL_EMBED) -> Embedding:
+    T = int8_uniform(V * K, seed, tag(workload, 0, 0, ROLE_TABLE)).reshape(V, K)
+    s_T = scales(V, 127.0, seed, tag(workload, 0, 0, ROLE_TABLE_SCALE))
+    tokens = (draws(seed, tag(workload, 0, 0, ROLE_TOKENS), 0, B) % np.uint64(V)).astype(np.int32)
+    return Embedding(V, K, T, s_T, tokens)
+
+
+def draft_tokens(greedy: np.ndarray, n_agree: int, V: int, seed: int = 0,
+                 workload: int = WL_EMBED) -> np.ndarray:
+    """B - 1 drafted tokens for a verify pass whose greedy tokens are ``greedy`` [B]: the
+    first ``n_agree`` copy the greedy tokens, the next one differs, the rest are uniform."""
+    B = greedy.size
+    d = (draws(seed, tag(workload, 0, 0, ROLE_DRAFT), 0, max(B - 1, 0)) % np.uint64(V)).astype(np.int32)
+    d[:n_agree] = greedy[:n_agree]
+    if n_agree < B - 1:
+        d[n_agree] = (greedy[n_agree] + 1) % V
+    return d

@@ -82,3 +82,22 @@ def tiled_layout():
                     "tiled": {int(o): int(w, 16) for o, w in (p.split(":") for p in tiled.split())},
                     "bytes": int(total)})
     return out
+
+
+def embed_verify_hand():
+    """([(tokens, x rows, bad)], [(draft, argmax, emitted)])"""
+    embeds, verifies = [], []
+    for line in _lines("embed_verify_hand.txt"):
+        kind, rest = line.split(" ", 1)
+        left, right = rest.split("->")
+        if kind == "embed":
+            toks = [int(v) for v in left.split()[1:]]
+            parts = right.split("|")
+            rows = [[float(v) for v in p.split()] for p in parts[:-1]]
+            bad = int(parts[-1].split()[1])
+            embeds.append((toks, rows, bad))
+        else:
+            d, a = left.split("|")
+            verifies.append(([int(v) for v in d.split()], [int(v) for v in a.split()],
+                             [int(v) for v in right.split()]))
+    return embeds, verifies

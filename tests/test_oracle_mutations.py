@@ -31,6 +31,9 @@ MUTATIONS = {
     "tile_rows_transposed": ("out + t * Kp + j * 16 + 4 * r", "out + t * Kp + j * 16 + 4 * (3 - r)"),
     "table_row_stride_wrong": ("const int8_t* row = T + (int64_t)v * K;",
                                "const int8_t* row = T + (int64_t)v * (K - 1);"),
+    "embed_scale_of_row_zero": ("v = (float)T[(int64_t)t * K + k] * s[t];",
+                                "v = (float)T[(int64_t)t * K + k] * s[0];"),
+    "verify_compares_next_position": ("draft[j] == argmax[j])", "draft[j] == argmax[j + 1])"),
 }
 
 
@@ -93,8 +96,25 @@ def _check_tiled(o):
     return True
 
 
+def _check_embed(o):
+    T = np.array([[1, -2, 3, -4], [127, -127, 0, 64], [0, 0, 0, 1]], dtype=np.int8)
+    s = np.array([0.5, 0.25, 8.0], dtype=np.float32)
+    embeds, _ = _golden.embed_verify_hand()
+    for toks, rows, bad in embeds:
+        x, nbad = o.embed_rows(T, s, 3, 4, np.array(toks, np.int32))
+        if x.tolist() != rows or nbad != bad:
+            return False
+    return True
+
+
+def _check_verify(o):
+    _, verifies = _golden.embed_verify_hand()
+    return all(o.verify_accept(np.array(d, np.int32), np.array(a, np.int32)).tolist() == e
+               for d, a, e in verifies)
+
+
 CHECKS = [_check_plain, _check_gemv, _check_gemm_matmul, _check_quantize, _check_logits,
-          _check_tiled]
+          _check_tiled, _check_embed, _check_verify]
 
 
 def _failures(o):

@@ -329,3 +329,48 @@ def test_tiled_all_nine_pairs():
                     word |= np.uint32(code[j] << (2 * j))
                 out = oracle.repack_tiled(np.array([[word]], dtype=np.uint32), 1, 16)
                 assert np.array_equal(oracle.unpack_tiled(out, 1, 16)[0], dense)
+
+
+# ---- input-table gather and verify-pass acceptance --------------------------------------
+
+EMBED_T = np.array([[1, -2, 3, -4], [127, -127, 0, 64], [0, 0, 0, 1]], dtype=np.int8)
+EMBED_S = np.array([0.5, 0.25, 8.0], dtype=np.float32)
+
+
+def test_embed_rows_hand_worked():
+    embeds, _ = _golden.embed_verify_hand()
+    for toks, rows, bad in embeds:
+        x, nbad = oracle.embed_rows(EMBED_T, EMBED_S, 3, 4, np.array(toks, np.int32))
+        assert x.tolist() == rows and nbad == bad
+
+
+def test_embed_rows_selects_rows():
+    V, K = 1000, 256
+    T = synth.int8_uniform(V * K, 12, 1).reshape(V, K)
+    s = synth.scales(V, 4096.0, 12, 2)
+    toks = np.array([999, 0, 17, 17, 500], dtype=np.int32)
+    x, bad = oracle.embed_rows(T, s, V, K, toks)
+    assert bad == 0
+    for b, t in enumerate(toks):
+        # row t only: every element is T[t][k] times the row's scale, within one rounding
+        exact = T[t].astype(np.float64) * float(s[t])
+        assert np.all(np.abs(x[b] - exact) <= 2 ** -24 * np.abs(exact))
+
+
+def test_verify_accept_hand_worked():
+    _, verifies = _golden.embed_verify_hand()
+    for draft, am, emit in verifies:
+        assert oracle.verify_accept(np.array(draft, np.int32), np.array(am, np.int32)).tolist() == emit
+
+
+def test_verify_accept_exhaustive_small():
+    # Brute force over every draft/argmax pair on a 3-token vocabulary with B = 4: the emitted
+    # tokens are a prefix of the drafts that agrees with the large model, then its own token.
+    import itertools
+    for d in itertools.product(range(3), repeat=3):
+        for a in itertools.product(range(3), repeat=4):
+            emit = oracle.verify_accept(np.array(d, np.int32), np.array(a, np.int32)).tolist()
+            j = len(emit) - 1
+            assert list(d[:j]) == list(a[:j]) == emit[:j]
+            assert emit[j] == a[j]
+            assert j == 3 or d[j] != a[j]
