@@ -194,6 +194,33 @@ nt_status nt_int8_logits_argmax_noalloc(const int8_t* T, const float* s_T, int V
                                         float* logits_opt, int32_t* argmax, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Input-table row gather ("The file is not the traffic": of the input table only the rows of
+ * the current tokens are read). x[b][k] = fl((float)T[tokens[b]][k] * s_T[tokens[b]]): the
+ * int8 value converted exactly, one rounded product -- the fp32 hidden vector the first layer
+ * quantizes (the pages do not say how the row becomes the hidden vector; this is the plain
+ * reading of an int8 table with row scales).
+ *   T [V][K] int8 (16-byte aligned, K % 16 == 0)   s_T [V] fp32   tokens [B] int32
+ *   x [B][K] fp32 (output, 16-byte aligned)
+ *   n_bad_opt: device uint32 counter or NULL; the call ADDS the number of tokens outside
+ *   [0, V), whose rows are written as zeros.
+ */
+nt_status nt_embed_rows(const int8_t* T, const float* s_T, int V, int K, const int32_t* tokens,
+                        int B, float* x, uint32_t* n_bad_opt, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Verify-pass acceptance ("The 0.6B model does not get to decide": the large model scores
+ * every drafted position in one batched pass; the longest prefix on which the draft agrees
+ * with it is kept, and at the first disagreement the large model's own token is emitted).
+ * Positions 0..B-1 of the verify pass hold the last emitted token and the drafts
+ * draft[0..B-2]; argmax[i] is the pass's greedy token after position i (for example the
+ * argmax output of nt_int8_logits_argmax with B vectors). With j leading drafts accepted
+ * (draft[i] == argmax[i] for all i < j), emit[0..j] = draft[0..j-1], argmax[j] and
+ * *n_emit = j + 1. All pointers device; draft may be NULL when B == 1. One tiny kernel.
+ */
+nt_status nt_verify_accept(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit,
+                           int32_t* n_emit, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Decode step: every projection of every layer, then optionally the output projection, in
  * one submission ("A 104 microsecond floor ...": on the instrumented A100 step, roughly
  * 590 of 694 microseconds were spent across about 120 kernel boundaries rather than in
@@ -243,6 +270,19 @@ typedef struct nt_decode_desc {
                             persistent kernel wait for one arrival more than the grid makes,
                             so that wait runs out after timeout_ms and the step reports
                             NT_ERR_TIMEOUT: the hook the tests of the timeout path use. */
+  /* Input-table gather at the start of the step (nt_embed_rows); embed_T == NULL leaves it
+     out. Projection inputs (x) may point into embed_x: the gather finishes before any
+     input is quantized. Tokens outside [0, embed_V) give zero rows. */
+  const int8_t* embed_T;   /* [embed_V][embed_K] int8 */
+  const float* embed_s;    /* [embed_V] */
+  int embed_V, embed_K;
+  const int32_t* tokens;   /* [batch] */
+  float* embed_x;          /* [batch][embed_K] fp32 output */
+  /* Verify-pass acceptance after the output projection (nt_verify_accept on head_argmax);
+     needs the head; verify_emit == NULL leaves it out. */
+  const int32_t* verify_draft;  /* [batch - 1] drafted tokens (NULL when batch == 1) */
+  int32_t* verify_emit;         /* [batch] emitted tokens */
+  int32_t* verify_n;            /* [1] number of emitted tokens */
 } nt_decode_desc;
 
 typedef struct nt_decode_plan nt_decode_plan;

@@ -123,6 +123,20 @@ __device__ __forceinline__ float scale_out(int acc, float s_row, float s_vec) {
   return __fmul_rn(__fmul_rn(__int2float_rn(acc), s_row), s_vec);
 }
 
+// Verify-pass acceptance by one thread: positions 0..B-1 hold the last emitted token and the
+// B-1 drafted tokens; with j drafts equal to the model's arg-max at the position before them
+// (and every earlier draft accepted), emit draft[0..j-1] then argmax[j]; returns j + 1.
+__device__ __forceinline__ int verify_accept_device(const int32_t* draft, const int32_t* argmax, int B,
+                                                    int32_t* emit) {
+  int j = 0;
+  while (j < B - 1 && draft[j] == argmax[j]) {
+    emit[j] = draft[j];
+    ++j;
+  }
+  emit[j] = argmax[j];
+  return j + 1;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -54,6 +54,11 @@ nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
                       cudaStream_t st);
 
+nt_status launch_embed(const int8_t* T, const float* s, int V, int K, const int32_t* tokens, int B, float* x,
+                       uint32_t* n_bad, cudaStream_t st);
+nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit, int32_t* n_emit,
+                        cudaStream_t st);
+
 // Tensor-core ternary GEMM (tcgen05, bf16 operands, exact fp32 accumulation) for
 // prefill-shaped batches of at least kTcMinBatch vectors.
 constexpr int kTcMinBatch = 64;

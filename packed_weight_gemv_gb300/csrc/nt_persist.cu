@@ -84,6 +84,16 @@ struct PersistParams {
   uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
   uint64_t timeout_ns;
   unsigned long long* trace;  // optional timeline: [grid][n_barriers + 1][4]
+  // input-table gather before quantization (embed_T == NULL: none)
+  const int8_t* embed_T;
+  const float* embed_s;
+  int embed_V, embed_K;
+  const int32_t* tokens;
+  float* embed_x;
+  // verify-pass acceptance after the arg-max (verify_emit == NULL: none)
+  const int32_t* verify_draft;
+  int32_t* verify_emit;
+  int32_t* verify_n;
 };
 
 // One timeline stamp (thread 0 of the consumers only).
@@ -357,6 +367,27 @@ __device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_ou
   consumer_sync<C>();  // red[] reuse
 }
 
+// Input-table row of token b, dequantized into embed_x[b] by the consumer threads:
+// x[k] = fl((float)T[tok][k] * s[tok]); a token outside [0, V) gives a zero row.
+template <class C>
+__device__ void embed_row_consumers(const PersistParams& P, int b) {
+  const int t = P.tokens[b];
+  const bool ok = t >= 0 && t < P.embed_V;
+  const float sc = ok ? P.embed_s[t] : 0.0f;
+  float4* out = reinterpret_cast<float4*>(P.embed_x + (int64_t)b * P.embed_K);
+  for (int g = threadIdx.x; g < P.embed_K / 16; g += C::CT) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (ok) v = __ldg(reinterpret_cast<const uint4*>(P.embed_T + (int64_t)t * P.embed_K) + g);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int8_t* c = reinterpret_cast<const int8_t*>(&w[i]);
+      out[4 * g + i] = make_float4(__fmul_rn((float)c[0], sc), __fmul_rn((float)c[1], sc),
+                                   __fmul_rn((float)c[2], sc), __fmul_rn((float)c[3], sc));
+    }
+  }
+}
+
 // Grid-wide barrier among the consumers of all CTAs; `target` counts arrivals modulo 2^32.
 template <class C>
 __device__ void grid_barrier(const PersistParams& P, uint32_t target, int b, volatile int* s_abort) {
@@ -565,6 +596,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   const uint32_t barrier_base = P.launch_idx * (uint32_t)P.n_barriers * gridDim.x;
   uint32_t barriers = 0, seq = 0;
 
+  if (P.embed_T) {  // input-table rows of the step's tokens; quantization may read them
+    for (int b = blockIdx.x; b < P.B; b += gridDim.x) embed_row_consumers<C>(P, b);
+    if (P.n_qjobs > 0) {
+      ++barriers;
+      grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
+      stamp(P, (int)barriers, 2);
+    }
+  }
+
   if (P.n_qjobs > 0) {  // quantize the step's fp32 inputs, then wait for every CTA
     for (int j = blockIdx.x; j < P.n_qjobs; j += gridDim.x) {
       const QuantJob qj = P.qjobs[j];
@@ -649,6 +689,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
         P.head_argmax[threadIdx.x] = bi == INT_MAX ? 0 : bi;
       }
       if (threadIdx.x == 0) P.ctrl->head_done = 0u;
+      if (P.verify_emit) {  // accept the longest agreeing draft prefix on the device
+        consumer_sync<C>();
+        if (threadIdx.x == 0) *P.verify_n = verify_accept_device(P.verify_draft, P.head_argmax, P.B, P.verify_emit);
+      }
     }
   }
 }
@@ -761,7 +805,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
     return Unitset{kItemTernary, mi, padded_rows(p->mats[mi].N) / 4, padded_k(p->mats[mi].K)};
   };
   const Unitset head{kItemHead, 0, p->head_V, p->head_K};
-  int barriers = p->n_qjobs > 0 ? 1 : 0;
+  int barriers = (p->n_qjobs > 0 ? 1 : 0) + (p->embed_T && p->n_qjobs > 0 ? 1 : 0);
   if (p->mode == NT_STEP_INDEPENDENT) {
     // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table (per pass),
     // so every CTA has the same mix of decode-heavy and decode-free work.
@@ -835,6 +879,15 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.barrier_extra = p->test_fault == 1 ? 1u : 0u;
   P.timeout_ns = p->timeout_ns;
   P.trace = p->trace;
+  P.embed_T = p->embed_T;
+  P.embed_s = p->embed_s;
+  P.embed_V = p->embed_V;
+  P.embed_K = p->embed_K;
+  P.tokens = p->tokens;
+  P.embed_x = p->embed_x;
+  P.verify_draft = p->verify_draft;
+  P.verify_emit = p->verify_emit;
+  P.verify_n = p->verify_n;
   void* args[] = {&P};
   int threads = 0;
   const void* kern = kernel_for(p->B, &threads);

@@ -46,11 +46,25 @@ nt_status validate_desc(const nt_decode_desc* d) {
     if (!aligned(d->head_T, 16) || !aligned(d->head_q, 16) || (d->head_x && !aligned(d->head_x, 4)))
       return set_error(NT_ERR_ALIGNMENT, "head: misaligned pointer");
   }
+  if (d->embed_T) {
+    if (d->embed_V < 1 || d->embed_K < 16 || d->embed_K % 16 != 0)
+      return set_error(NT_ERR_INVALID_ARG, "embed: need V >= 1 and K a positive multiple of 16");
+    if (!d->embed_s || !d->tokens || !d->embed_x) return set_error(NT_ERR_INVALID_ARG, "embed: NULL pointer");
+    if (!aligned(d->embed_T, 16) || !aligned(d->embed_x, 16) || !aligned(d->tokens, 4) || !aligned(d->embed_s, 4))
+      return set_error(NT_ERR_ALIGNMENT, "embed: misaligned pointer");
+  }
+  if (d->verify_emit) {
+    if (!d->head_T) return set_error(NT_ERR_INVALID_ARG, "verify: needs the output projection (head_T)");
+    if (!d->verify_n || (d->batch > 1 && !d->verify_draft))
+      return set_error(NT_ERR_INVALID_ARG, "verify: NULL pointer");
+  }
   return NT_OK;
 }
 
 // Issues the per-stage launches of one step on `st` (stream and graph launchers).
 nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
+  if (p->embed_T)
+    NT_TRY(launch_embed(p->embed_T, p->embed_s, p->embed_V, p->embed_K, p->tokens, p->B, p->embed_x, nullptr, st));
   if (p->n_qjobs) NT_TRY(launch_quantize_jobs(p->d_qjobs, p->n_qjobs, p->B, st));
   for (const PlanStage& s : p->stages)
     NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
@@ -58,6 +72,7 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
   if (p->has_head)
     NT_TRY(launch_head(p->head_T, p->head_s, p->head_V, p->head_K, p->head_q, p->head_sx, p->B,
                        p->head_logits, p->head_argmax, p->d_head_ws, st));
+  if (p->verify_emit) NT_TRY(launch_verify(p->verify_draft, p->head_argmax, p->B, p->verify_emit, p->verify_n, st));
   return NT_OK;
 }
 
@@ -151,6 +166,15 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     if (d->head_x) jobs.push_back(QuantJob{d->head_x, d->head_q, d->head_sx, d->head_K, d->batch});
   }
   p->n_qjobs = (int)jobs.size();
+  p->embed_T = d->embed_T;
+  p->embed_s = d->embed_s;
+  p->embed_V = d->embed_V;
+  p->embed_K = d->embed_K;
+  p->tokens = d->tokens;
+  p->embed_x = d->embed_x;
+  p->verify_draft = d->verify_draft;
+  p->verify_emit = d->verify_emit;
+  p->verify_n = d->verify_n;
 
   auto fail = [&](nt_status s) { free_plan(p); return s; };
   auto cuda_fail = [&](cudaError_t e, const char* what) {

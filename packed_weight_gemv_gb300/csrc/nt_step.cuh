@@ -58,6 +58,16 @@ struct nt_decode_plan {
   float* head_logits = nullptr;
   int32_t* head_argmax = nullptr;
   nt::HeadWs* d_head_ws = nullptr;
+  // input-table gather at the start of the step
+  const int8_t* embed_T = nullptr;
+  const float* embed_s = nullptr;
+  int embed_V = 0, embed_K = 0;
+  const int32_t* tokens = nullptr;
+  float* embed_x = nullptr;
+  // verify-pass acceptance after the output projection
+  const int32_t* verify_draft = nullptr;
+  int32_t* verify_emit = nullptr;
+  int32_t* verify_n = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   nt::StepCtrl* d_ctrl = nullptr;

@@ -38,7 +38,7 @@ EXPORTS = (
     "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
     "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
-    "nt_int8_logits_argmax_noalloc",
+    "nt_int8_logits_argmax_noalloc", "nt_embed_rows", "nt_verify_accept",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
     "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_destroy",
 )
@@ -65,7 +65,12 @@ class nt_decode_desc(ctypes.Structure):
                 ("head_sx", ctypes.c_void_p), ("head_logits", ctypes.c_void_p),
                 ("head_argmax", ctypes.c_void_p), ("mode", ctypes.c_int),
                 ("launcher", ctypes.c_int), ("timeout_ms", ctypes.c_double),
-                ("test_fault", ctypes.c_int)]
+                ("test_fault", ctypes.c_int),
+                ("embed_T", ctypes.c_void_p), ("embed_s", ctypes.c_void_p),
+                ("embed_V", ctypes.c_int), ("embed_K", ctypes.c_int),
+                ("tokens", ctypes.c_void_p), ("embed_x", ctypes.c_void_p),
+                ("verify_draft", ctypes.c_void_p), ("verify_emit", ctypes.c_void_p),
+                ("verify_n", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -97,6 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_int8_logits_workspace_size": ([i, i, i, ctypes.POINTER(sz)], i),
             "nt_int8_logits_argmax": ([vp, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
             "nt_int8_logits_argmax_noalloc": ([vp, vp, i, i, vp, vp, i, vp, vp, vp], i),
+            "nt_embed_rows": ([vp, vp, i, i, vp, i, vp, vp, vp], i),
+            "nt_verify_accept": ([vp, vp, i, vp, vp, vp], i),
             "nt_decode_plan_create": ([ctypes.POINTER(nt_decode_desc), ctypes.POINTER(vp)], i),
             "nt_decode_step": ([vp, vp], i),
             "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
@@ -208,20 +215,35 @@ def nt_int8_logits_argmax_noalloc(T: torch.Tensor, s_T: torch.Tensor, V: int, K:
         _stream(stream)), "nt_int8_logits_argmax_noalloc")
 
 
+def nt_embed_rows(T: torch.Tensor, s_T: torch.Tensor, V: int, K: int, tokens: torch.Tensor,
+                  B: int, x: torch.Tensor, n_bad: Optional[torch.Tensor] = None, stream=None):
+    _check(load_library().nt_embed_rows(_ptr(T), _ptr(s_T), V, K, _ptr(tokens), B, _ptr(x),
+                                        _ptr(n_bad), _stream(stream)), "nt_embed_rows")
+
+
+def nt_verify_accept(draft: Optional[torch.Tensor], argmax: torch.Tensor, B: int,
+                     emit: torch.Tensor, n_emit: torch.Tensor, stream=None):
+    _check(load_library().nt_verify_accept(_ptr(draft), _ptr(argmax), B, _ptr(emit), _ptr(n_emit),
+                                           _stream(stream)), "nt_verify_accept")
+
+
 class DecodePlan:
     """Owns an nt_decode_plan and keeps every tensor it names alive.
 
     ``projs`` is a sequence of dicts with keys N, K, w, s_w, q, s_x, y and optionally x
     (torch tensors on the current device), n_layers * 7 of them in q, k, v, o, gate, up, down
     order per layer. ``head`` is None or a dict with T, s, V, K, q, sx, argmax and optionally
-    x and logits.
+    x and logits. ``embed`` is None or a dict with T, s, V, K, tokens, x (the input-table
+    gather that runs first; projection inputs may be views of its x). ``verify`` is None or a
+    dict with emit, n and (for batch > 1) draft, applied to the head's arg-max.
     """
 
     def __init__(self, n_layers: int, batch: int, projs: Sequence[dict], head: Optional[dict],
                  mode: int = NT_STEP_INDEPENDENT, launcher: int = NT_LAUNCH_PERSISTENT,
-                 timeout_ms: float = 0.0, test_fault: int = 0):
+                 timeout_ms: float = 0.0, test_fault: int = 0, embed: Optional[dict] = None,
+                 verify: Optional[dict] = None):
         lib = load_library()
-        self._keep = [projs, head]
+        self._keep = [projs, head, embed, verify]
         arr = (nt_proj * len(projs))()
         for i, p in enumerate(projs):
             arr[i] = nt_proj(p["N"], p["K"], p["w"].data_ptr(), p["s_w"].data_ptr(),
@@ -237,6 +259,13 @@ class DecodePlan:
             d.head_logits = head["logits"].data_ptr() if head.get("logits") is not None else None
             d.head_argmax = head["argmax"].data_ptr()
         d.mode, d.launcher, d.timeout_ms, d.test_fault = mode, launcher, timeout_ms, test_fault
+        if embed is not None:
+            d.embed_T, d.embed_s = embed["T"].data_ptr(), embed["s"].data_ptr()
+            d.embed_V, d.embed_K = embed["V"], embed["K"]
+            d.tokens, d.embed_x = embed["tokens"].data_ptr(), embed["x"].data_ptr()
+        if verify is not None:
+            d.verify_draft = verify["draft"].data_ptr() if verify.get("draft") is not None else None
+            d.verify_emit, d.verify_n = verify["emit"].data_ptr(), verify["n"].data_ptr()
         self._arr = arr
         handle = ctypes.c_void_p(None)
         _check(lib.nt_decode_plan_create(ctypes.byref(d), ctypes.byref(handle)),
