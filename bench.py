@@ -483,6 +483,92 @@ def run_sweep(args):
 
 
 # ---------------------------------------------------------------------------------------
+# Speculative verify pass (not the headline line): B positions (the last emitted token and
+# B - 1 drafts) gathered from the input table into layer 0's q, k and v, every projection,
+# the output projection and the acceptance of the longest agreeing draft prefix, in one step
+# ---------------------------------------------------------------------------------------
+
+def run_verify(args):
+    import torch
+
+    import oracle
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    L = args.layers
+    projs, head, dp, hd, _ = build_inputs(torch, nt, dev, L)
+    emb = wl.embedding(B=8)
+    eT, es = torch.from_numpy(emb.T).to(dev), torch.from_numpy(emb.s_T).to(dev)
+    stream = torch.cuda.current_stream()
+    for B in (2, 4, 8):
+        tokens = emb.tokens[:B].copy()
+        ex = torch.empty((B, emb.K), dtype=torch.float32, device=dev)
+        dpB, hosts = [], []
+        for i, (p, d) in enumerate(zip(projs, dp)):
+            layer, name = p.name.split(".")
+            x = wl.projection_x(wl.WL_DECODE, int(layer[1:]), wl.PROJ_NAMES.index(name), p.K, B)
+            hosts.append(x)
+            dpB.append(dict(N=p.N, K=p.K, w=d["w"], s_w=d["s_w"],
+                            x=ex if i < 3 else torch.from_numpy(x).to(dev),
+                            q=torch.empty((B, p.K), dtype=torch.int8, device=dev),
+                            s_x=torch.empty(B, dtype=torch.float32, device=dev),
+                            y=torch.empty((B, p.N), dtype=torch.float32, device=dev)))
+        hx = wl.head_x(B=B)
+        hdB = dict(T=hd["T"], s=hd["s"], V=head.V, K=head.K, x=torch.from_numpy(hx).to(dev),
+                   q=torch.empty((B, head.K), dtype=torch.int8, device=dev),
+                   sx=torch.empty(B, dtype=torch.float32, device=dev),
+                   logits=torch.empty((B, head.V), dtype=torch.float32, device=dev),
+                   argmax=torch.empty(B, dtype=torch.int32, device=dev))
+        # drafts that agree with the greedy tokens at every position (a fully accepted pass)
+        q, s = oracle.quantize(hx)
+        _, greedy, _ = oracle.logits_argmax(head.T, head.s_T, head.V, head.K, q, s)
+        greedy = np.asarray(greedy, dtype=np.int32)
+        draft = wl.draft_tokens(greedy, B - 1, head.V)
+        emit = torch.empty(B, dtype=torch.int32, device=dev)
+        n_emit = torch.empty(1, dtype=torch.int32, device=dev)
+        embed = dict(T=eT, s=es, V=emb.V, K=emb.K, tokens=torch.from_numpy(tokens).to(dev), x=ex)
+        verify = dict(draft=torch.from_numpy(draft).to(dev), emit=emit, n=n_emit)
+        plan = nt.DecodePlan(L, B, dpB, hdB, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT,
+                             embed=embed, verify=verify)
+        base = nt.DecodePlan(L, B, dpB, hdB, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+        for _ in range(args.warmup):
+            base.nt_decode_step(stream)
+            plan.nt_decode_step(stream)
+        torch.cuda.synchronize()
+        parity = "pass"
+        xe, _ = oracle.embed_rows(emb.T, emb.s_T, emb.V, emb.K, tokens)
+        if not np.array_equal(ex.cpu().numpy().view(np.uint32), xe.view(np.uint32)):
+            parity = "gathered rows differ"
+        for i in range(len(wl.PROJ_NAMES)):  # every projection of layer 0
+            p = projs[i]
+            full = wl.projection(wl.WL_DECODE, 0, i, p.N, p.K)
+            qi, si = oracle.quantize(xe if i < 3 else hosts[i])
+            _, y, _ = oracle.gemm(full.w_plain, full.s_w, p.N, p.K, qi, si)
+            got = dpB[i]["y"].cpu().numpy().astype(np.float64)
+            if np.any(np.abs(got - y) > 1e-6 * np.abs(y.astype(np.float64))):
+                parity = f"{p.name} differs"
+        if not np.array_equal(hdB["argmax"].cpu().numpy(), greedy):
+            parity = "arg-max differs"
+        want = oracle.verify_accept(draft, greedy)
+        if int(n_emit.item()) != want.size or not np.array_equal(emit.cpu().numpy()[:want.size], want):
+            parity = "emitted tokens differ"
+        steps = max(3, min(args.steps, 300))
+        us_base = time_steps(torch, base, steps, stream) / steps
+        us = time_steps(torch, plan, steps, stream) / steps
+        if plan.nt_decode_step_status() != nt.NT_OK or base.nt_decode_step_status() != nt.NT_OK:
+            parity = "timeout reported"
+        print(json.dumps({"metric": "speculative verify pass", "positions": B, "steps": steps,
+                          "us_per_pass": round(us, 2), "us_per_pass_without_gather_accept": round(us_base, 2),
+                          "us_per_token_if_all_accepted": round(us / B, 2),
+                          "tokens_emitted": int(n_emit.item()),
+                          "gather_bytes": B * (emb.K + 4 + 4 * emb.K), "parity": parity}), flush=True)
+        plan.close()
+        base.close()
+
+
+# ---------------------------------------------------------------------------------------
 # Prefill (not the headline line): the 28-layer small model at M = 2048 and 8192 tokens on
 # the tensor-core GEMM
 # ---------------------------------------------------------------------------------------
@@ -594,6 +680,8 @@ def main():
                          "for small profiling captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="batched sweep B = 1, 2, 4, 8, 16 (one JSON line per batch)")
+    ap.add_argument("--verify", action="store_true",
+                    help="speculative verify passes of 2, 4 and 8 positions (gather + step + acceptance)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
@@ -607,6 +695,9 @@ def main():
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.verify:
+        run_verify(args)
         return
     if args.prefill:
         run_prefill(args)
