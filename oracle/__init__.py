@@ -15,7 +15,9 @@ Every function takes and returns numpy arrays and runs the plain loops of ``orac
 * :func:`repack_tiled`, :func:`unpack_tiled` -- the library's tiled layout, from its
   written definition;
 * :func:`embed_rows` -- the input-table rows of the current tokens, dequantized;
-* :func:`verify_accept` -- the longest agreeing prefix of a batched verify pass.
+* :func:`verify_accept` -- the longest agreeing prefix of a batched verify pass;
+* :func:`decode_chained` (``chain.py``) -- a step whose stages quantize the previous stage's
+  output (single-position attention, residual stream, gated product).
 
 Pins (``tests/test_oracle_*.py``) tie each of these to brute force, closed forms, invariants
 and hand-worked fixtures under ``tests/golden/``.
@@ -258,3 +260,8 @@ def embed_rows(T, s_T, V, K, tokens):
 
 def verify_accept(draft, argmax):
     return default().verify_accept(draft, argmax)
+
+
+def decode_chained(layers, x0, head=None, head_dim: int = 128):
+    from .chain import decode_chained as _chained
+    return _chained(default(), layers, x0, head, head_dim)

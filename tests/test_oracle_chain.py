@@ -1,0 +1,177 @@
+"""Pins of the oracle's chained decode step (CPU only).
+
+The chain is wired from pinned parts (quantizer, ternary GEMM, output projection); what needs
+pinning is the wiring: which tensor feeds which stage, the two residual additions, the gated
+product and the single-position attention. Two closed forms do it:
+
+* all-zero weights: every projection gives +0, so the residual stream carries the first
+  layer's hidden vectors through unchanged and the output projection scores them;
+* signed selection weights (row n holds one +-1 at column pi(n), row scale 1): a projection
+  returns its own quantized input, permuted and signed, within the quantizer's error bound,
+  so each stage's output is checked against the tensor that must have fed it, and the
+  elementwise steps are checked exactly against sums and products formed in float64 (exact
+  for two fp32 operands) and rounded once.
+
+Planted wiring mistakes in a copy of ``oracle/chain.py`` must each fail one of the checks.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from oracle import chain as chain_mod
+
+CHAIN_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "chain.py")
+
+
+def pack_plain(t: np.ndarray) -> np.ndarray:
+    """int8 trits [N, K] -> plain words [N, K/16] (01 = +1, 11 = -1, field k%16 of word k/16)."""
+    N, K = t.shape
+    w = np.zeros((N, K // 16), dtype=np.uint32)
+    for n in range(N):
+        for k in range(K):
+            code = {0: 0, 1: 1, -1: 3}[int(t[n, k])]
+            w[n, k // 16] |= np.uint32(code << (2 * (k % 16)))
+    return w
+
+
+def selection(N, K, rng):
+    """A signed selection matrix: (trits, pi, sign)."""
+    pi = rng.integers(0, K, size=N)
+    if N <= K:
+        pi = rng.permutation(K)[:N]
+    sign = rng.choice([-1, 1], size=N)
+    t = np.zeros((N, K), dtype=np.int8)
+    t[np.arange(N), pi] = sign
+    return t, pi, sign
+
+
+# tiny model: 4 query heads and 2 key-value heads of 16 dimensions (G = 2), feed-forward 96
+HD, D, KV, F = 16, 64, 32, 96
+SHAPES = [(D, D), (KV, D), (KV, D), (D, D), (F, D), (F, D), (D, F)]  # (N, K) q k v o gate up down
+
+
+def build_model(n_layers, seed, zero=False):
+    rng = np.random.default_rng(seed)
+    layers, sel = [], []
+    for _ in range(n_layers):
+        mats, s = [], []
+        for N, K in SHAPES:
+            if zero:
+                t, pi, sg = np.zeros((N, K), np.int8), None, None
+                s_w = synth.scales(N, np.sqrt(K), seed, N * 31 + K)
+            else:
+                t, pi, sg = selection(N, K, rng)
+                s_w = np.ones(N, dtype=np.float32)
+            mats.append((pack_plain(t), s_w, N, K))
+            s.append((pi, sg))
+        layers.append(mats)
+        sel.append(s)
+    return layers, sel
+
+
+def within_quant_bound(y, x_in, s, pi, sign):
+    """y[b, n] ~ sign[n] * x_in[b, pi[n]] within s_b/2 (1 + 2^-16) plus one fp32 rounding."""
+    want = sign[None, :].astype(np.float64) * x_in[:, pi].astype(np.float64)
+    bound = (s.astype(np.float64)[:, None] / 2) * (1 + 2 ** -16) + np.abs(want) * 2 ** -23
+    return bool(np.all(np.abs(y.astype(np.float64) - want) <= bound))
+
+
+def fp32_add(a, b):
+    return (a.astype(np.float64) + b.astype(np.float64)).astype(np.float32)
+
+
+def fp32_mul(a, b):
+    return (a.astype(np.float64) * b.astype(np.float64)).astype(np.float32)
+
+
+def expand_by_loops(y_v, n_out, hd):
+    B, n_kv = y_v.shape
+    G = n_out // n_kv
+    u = np.empty((B, n_out), dtype=np.float32)
+    for b in range(B):
+        for i in range(n_out // hd):
+            for j in range(hd):
+                u[b, i * hd + j] = y_v[b, (i // G) * hd + j]
+    return u
+
+
+def check_selection_chain(decode_chained, n_layers=2, B=3, seed=5):
+    layers, sel = build_model(n_layers, seed)
+    x0 = synth.normal(B * D, seed, 77).reshape(B, D)
+    out = decode_chained(oracle.default(), layers, x0, None, HD)
+    ok = np.array_equal(out["h"][0].view(np.uint32), x0.view(np.uint32))
+    for l in range(n_layers):
+        y = out["y"][7 * l:7 * l + 7]
+        s = out["s"][7 * l:7 * l + 7]
+        (pq, sq), (pk, sk), (pv, sv), (po, so), (pg, sg), (pu, su), (pd, sd) = sel[l]
+        h, u, a, g, h1 = out["h"][l], out["u"][l], out["a"][l], out["g"][l], out["h"][l + 1]
+        ok &= within_quant_bound(y[0], h, s[0], pq, sq)
+        ok &= within_quant_bound(y[1], h, s[1], pk, sk)
+        ok &= within_quant_bound(y[2], h, s[2], pv, sv)
+        ok &= np.array_equal(u, expand_by_loops(y[2], D, HD))
+        ok &= within_quant_bound(y[3], u, s[3], po, so)
+        ok &= np.array_equal(a, fp32_add(h, y[3]))
+        ok &= within_quant_bound(y[4], a, s[4], pg, sg)
+        ok &= within_quant_bound(y[5], a, s[5], pu, su)
+        ok &= np.array_equal(g, fp32_mul(y[4], y[5]))
+        ok &= within_quant_bound(y[6], g, s[6], pd, sd)
+        ok &= np.array_equal(h1, fp32_add(a, y[6]))
+    return bool(ok)
+
+
+def check_zero_chain(decode_chained, n_layers=3, B=2, seed=6):
+    layers, _ = build_model(n_layers, seed, zero=True)
+    x0 = synth.normal(B * D, seed, 78).reshape(B, D)
+    V = 300
+    T = synth.int8_uniform(V * D, seed, 79).reshape(V, D)
+    s_T = synth.scales(V, 4096.0, seed, 80)
+    out = decode_chained(oracle.default(), layers, x0, (T, s_T, V, D), HD)
+    ok = all(np.all(y.view(np.uint32) == 0) for y in out["y"])  # +0 everywhere
+    ok &= np.array_equal(out["h"][-1].view(np.uint32), x0.view(np.uint32))
+    ok &= all(np.all(s == 0) for s in out["s"][3::7])  # o sees u = 0
+    q, s = oracle.quantize(x0)
+    logits, am, _ = oracle.logits_argmax(T, s_T, V, D, q, s)
+    ok &= np.array_equal(out["argmax"], am) and np.array_equal(out["logits"], logits)
+    return bool(ok)
+
+
+def test_chain_zero_weights_carry_hidden_through():
+    assert check_zero_chain(chain_mod.decode_chained)
+
+
+def test_chain_selection_weights_stage_by_stage():
+    assert check_selection_chain(chain_mod.decode_chained)
+
+
+def test_single_position_attention_groups():
+    # query heads 0,1 read key-value head 0; heads 2,3 read head 1
+    y_v = np.arange(2 * 2 * 3, dtype=np.float32).reshape(2, 6)
+    u = chain_mod.gqa_single_position(y_v, 12, head_dim=3)
+    assert u[0].tolist() == [0, 1, 2, 0, 1, 2, 3, 4, 5, 3, 4, 5]
+    assert u[1].tolist() == [6, 7, 8, 6, 7, 8, 9, 10, 11, 9, 10, 11]
+
+
+MUTATIONS = {
+    "attention_residual_dropped": ("a = np.add(h, y_o, dtype=np.float32)", "a = np.add(h, 0 * y_o, dtype=np.float32)"),
+    "gate_squared": ("g = np.multiply(y_gate, y_up,", "g = np.multiply(y_gate, y_gate,"),
+    "ffn_residual_from_h": ("h = np.add(a, y_down,", "h = np.add(h, y_down,"),
+    "gate_fed_from_h": ("y_gate = project(mats[4], qc, sc)", "y_gate = project(mats[4], qa, sa)"),
+    "heads_interleaved": ("np.broadcast_to(heads, (B, n_kv // head_dim, G, head_dim))\n                                .reshape(B, n_out)",
+                          "np.tile(y_v, (1, G))"),
+    "o_fed_from_q": ("u = gqa_single_position(y_v, mats[3][3], head_dim)",
+                     "u = out['y'][-3][:, :mats[3][3]]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_chain_mutant_is_caught(name):
+    old, new = MUTATIONS[name]
+    src = open(CHAIN_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    ns = {"__name__": "chain_mutant"}
+    exec(compile(src.replace(old, new), "chain_mutant.py", "exec"), ns)
+    caught = not check_selection_chain(ns["decode_chained"]) or not check_zero_chain(ns["decode_chained"])
+    assert caught, f"mutation {name} was not caught"
