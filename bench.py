@@ -305,7 +305,9 @@ def run_ours(args, rank, world):
     for name, mode, launcher in [("ordered_persistent", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_PERSISTENT),
                                  ("independent_graph", nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_GRAPH),
                                  ("ordered_graph", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_GRAPH),
-                                 ("ordered_stream", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_STREAM)]:
+                                 ("ordered_stream", nt.NT_STEP_ORDERED, nt.NT_LAUNCH_STREAM),
+                                 ("chained_persistent", nt.NT_STEP_CHAINED, nt.NT_LAUNCH_PERSISTENT),
+                                 ("chained_graph", nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH)]:
         pl = nt.DecodePlan(L, 1, dp, hd, mode, launcher)
         for _ in range(3):
             pl.nt_decode_step(stream)
@@ -313,6 +315,8 @@ def run_ours(args, rank, world):
         if pl.nt_decode_step_status() != nt.NT_OK:
             raise RuntimeError(f"{name}: step reported a timeout")
         pl.close()
+    plan.nt_decode_step(stream)  # chained plans rewrote the codes: requantize the supplied inputs
+    torch.cuda.synchronize()
     parity_after = parity_gate(oracle, projs, head, dp, hd, layers=(L // 2,)) if rank == 0 else "pass"
 
     peak, peak_kind = measured_peak()

@@ -228,8 +228,28 @@ nt_status nt_verify_accept(const int32_t* draft, const int32_t* argmax, int B, i
  */
 enum nt_step_mode {
   NT_STEP_INDEPENDENT = 0, /* every projection has its own supplied input; no ordering */
-  NT_STEP_ORDERED = 1      /* per layer {q,k,v} -> {o} -> {gate,up} -> {down}, layer by
+  NT_STEP_ORDERED = 1,     /* per layer {q,k,v} -> {o} -> {gate,up} -> {down}, layer by
                               layer, each stage complete before the next one starts */
+  NT_STEP_CHAINED = 2      /* the ORDERED stages, each quantizing what the previous stages
+                              produced ("A 104 microsecond floor ...": each layer applies its
+                              matrices to the current activations and the engine reads no
+                              tensor twice per token). With hidden h (fp32 [B][d], d = the q
+                              projection's K) and every + and * one fp32 rounding:
+                                {q,k,v} <- Q(h);
+                                {o}     <- Q(u), u = attention over one cached position: query
+                                           head i (head_dim columns) takes the value head
+                                           i / G, G = o.K / v.N (grouped-query attention);
+                                {gate,up} <- Q(a), a = h + y_o;
+                                {down}  <- Q(y_gate * y_up);
+                                next h = a + y_down; the output projection scores Q(h_last).
+                              h of the first layer is proj[0].x (or the gathered rows when it
+                              points at embed_x); every other x and head_x is ignored. Every
+                              projection's q / s_x (and head_q / head_sx) receive the codes and
+                              scale of its input. Needs matching shapes (d = k.K = v.K = o.N =
+                              gate.K = up.K = down.N = head_K, o.K = q.N, gate.N = up.N =
+                              down.K, v.N = k.N a multiple of head_dim dividing o.K). The plan
+                              owns the residual stream (B x d fp32). Normalisations, rotary
+                              embedding and the gate's activation function are not applied. */
 };
 enum nt_launcher {
   NT_LAUNCH_PERSISTENT = 0, /* one cooperative kernel streams the whole step */
@@ -283,6 +303,8 @@ typedef struct nt_decode_desc {
   const int32_t* verify_draft;  /* [batch - 1] drafted tokens (NULL when batch == 1) */
   int32_t* verify_emit;         /* [batch] emitted tokens */
   int32_t* verify_n;            /* [1] number of emitted tokens */
+  int head_dim;                 /* NT_STEP_CHAINED: dimensions per attention head, a multiple of
+                                   4 (0 selects 128, "At 26K tokens ...": 128 per head) */
 } nt_decode_desc;
 
 typedef struct nt_decode_plan nt_decode_plan;

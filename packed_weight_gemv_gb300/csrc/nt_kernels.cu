@@ -77,6 +77,37 @@ __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob*
   quantize_vector(j.x + (int64_t)b * j.K, j.K, j.q + (int64_t)b * j.K, j.s + b);
 }
 
+// Chained stage input of vector blockIdx.x (stream / graph launchers): the fp32 values go to
+// job.vbuf with the absmax (for kChainSum vbuf is the residual stream, updated in place: each
+// thread rewrites only the elements it read), then the codes to every recorded q.
+__global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
+  __shared__ float red[kWarps];
+  const ChainJob j = *jobs;
+  const int b = blockIdx.x, K = j.src.K;
+  float* vb = j.vbuf + (int64_t)b * K;
+  float m = 0.0f;
+  for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+    const float4 v = chain_load4(j.src, b, k);
+    *reinterpret_cast<float4*>(vb + k) = v;
+    m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = red[0];
+#pragma unroll
+  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
+  const bool nz = m != 0.0f;
+  const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
+  if (threadIdx.x == 0)
+    for (int r = 0; r < j.n_rec; ++r) j.s[r][b] = s;
+  for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+    const uint32_t c = quant4(*reinterpret_cast<const float4*>(vb + k), s, nz);
+    for (int r = 0; r < j.n_rec; ++r) *reinterpret_cast<uint32_t*>(j.q[r] + (int64_t)b * K + k) = c;
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // Repack plain -> tiled. Word (row n, group g) of the tiled layout holds the same 16 trits
 // as plain word g of row n, re-coded as 8 pair codes; one thread per tiled word.
@@ -347,6 +378,11 @@ nt_status launch_quantize(const float* x, int B, int K, int8_t* q, float* s, cud
 nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st) {
   quantize_jobs_kernel<<<dim3(n_jobs, max_B), kThreads, 0, st>>>(d_jobs, max_B);
   return check_launch("quantize_jobs_kernel");
+}
+
+nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st) {
+  chain_quant_kernel<<<B, kThreads, 0, st>>>(d_job);
+  return check_launch("chain_quant_kernel");
 }
 
 nt_status launch_repack(const uint32_t* w, int N, int K, uint8_t* out, uint32_t* n_invalid,

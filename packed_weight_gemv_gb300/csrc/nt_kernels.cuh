@@ -13,6 +13,19 @@ struct QuantJob {
   int K, B;
 };
 
+// Where a chained stage's input comes from (vector b, element k of K):
+//   kChainDirect   in0[b][k]
+//   kChainHeads    in0[b][((k / hd) / grp) * hd + k % hd]: attention over one cached position,
+//                  query head i takes value head i / grp (in0 has K / grp columns)
+//   kChainProduct  fl(in0[b][k] * in1[b][k])
+//   kChainSum      fl(in0[b][k] + in1[b][k])
+enum : int { kChainNone = 0, kChainDirect = 1, kChainHeads = 2, kChainProduct = 3, kChainSum = 4 };
+struct ChainSrc {
+  const float* in0;
+  const float* in1;
+  int kind, K, grp, hd;
+};
+
 // One ternary projection in the tiled layout, B activation vectors.
 struct MatDesc {
   const uint8_t* w;  // tiles (nt_repack_ternary output)
@@ -22,7 +35,24 @@ struct MatDesc {
   float* y;          // [B][N]
   int32_t* acc;      // [B][N] or null
   int N, K, B;
+  int rec_first;     // chained steps: first of the rec_count matrices whose q / s_x record
+  int rec_count;     //   this matrix's input (the stage's matrices)
   int pad_;
+  ChainSrc src;      // chained steps (persistent launcher): the stage input; kind 0 = none
+  const float* res_in;  // chained steps: res_out[b][n] = fl(res_in[b][n] + y[b][n]), or null
+  float* res_out;
+};
+
+// One stage input of a chained step on the stream / graph launchers: the source, a buffer
+// for the fp32 values (the residual stream itself for kChainSum), and the matrices whose
+// q / s_x receive the codes.
+struct ChainJob {
+  ChainSrc src;
+  float* vbuf;       // [B][K]
+  int n_rec;
+  int pad_;
+  int8_t* q[3];
+  float* s[3];
 };
 
 // Scratch of the output-projection kernel's cross-CTA arg-max (caller-owned workspace).
@@ -54,6 +84,9 @@ nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
                       cudaStream_t st);
 
+// Quantizes one chained stage input per vector (one CTA per vector).
+nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st);
+
 nt_status launch_embed(const int8_t* T, const float* s, int V, int K, const int32_t* tokens, int B, float* x,
                        uint32_t* n_bad, cudaStream_t st);
 nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit, int32_t* n_emit,
@@ -66,5 +99,38 @@ bool tc_gemm_supported(int M, int K);
 size_t tc_gemm_workspace_bytes(int M, int N, int K);
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
                          int M, float* y, int32_t* acc, void* ws, cudaStream_t st);
+
+#ifdef __CUDACC__
+// Four consecutive elements k..k+3 (k % 4 == 0) of vector b of a chained stage input. The
+// sources were written earlier in the same step by other CTAs, so they are read through L2.
+__device__ __forceinline__ float4 chain_load4(const ChainSrc& c, int b, int k) {
+  if (c.kind == kChainHeads) {
+    const int kv = c.K / c.grp;
+    const int i = ((k / c.hd) / c.grp) * c.hd + k % c.hd;
+    return __ldcg(reinterpret_cast<const float4*>(c.in0 + (int64_t)b * kv + i));
+  }
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(c.in0 + (int64_t)b * c.K + k));
+  if (c.kind == kChainDirect) return a;
+  const float4 d = __ldcg(reinterpret_cast<const float4*>(c.in1 + (int64_t)b * c.K + k));
+  if (c.kind == kChainProduct)
+    return make_float4(__fmul_rn(a.x, d.x), __fmul_rn(a.y, d.y), __fmul_rn(a.z, d.z), __fmul_rn(a.w, d.w));
+  return make_float4(__fadd_rn(a.x, d.x), __fadd_rn(a.y, d.y), __fadd_rn(a.z, d.z), __fadd_rn(a.w, d.w));
+}
+
+// The int8 code of x for scale s of a vector whose absmax m is nonzero (nz), as in the
+// quantizer (m = 0 gives code 0 everywhere).
+__device__ __forceinline__ uint32_t quant_byte(float x, float s, bool nz) {
+  int v = 0;
+  if (nz) {
+    v = __float2int_rn(__fdiv_rn(x, s));
+    v = v > 127 ? 127 : (v < -127 ? -127 : v);
+  }
+  return (uint32_t)(v & 0xFF);
+}
+__device__ __forceinline__ uint32_t quant4(float4 v, float s, bool nz) {
+  return quant_byte(v.x, s, nz) | (quant_byte(v.y, s, nz) << 8) | (quant_byte(v.z, s, nz) << 16) |
+         (quant_byte(v.w, s, nz) << 24);
+}
+#endif
 
 }  // namespace nt

@@ -46,8 +46,9 @@ constexpr int kMaxSmem = 232448;                     // 227 KB per CTA on sm_103
 // runs 16 consumer warps (17 warps, registers capped at 96 by the 5 warps one SM
 // sub-partition holds); batched plans need more registers for 4 vectors' accumulators and run
 // 15 (16 warps, up to 128 registers).
-template <int CW_, int NBMAX_>
+template <int CW_, int NBMAX_, bool CHAINED_ = false>
 struct KCfg {
+  static constexpr bool CHAINED = CHAINED_;  // NT_STEP_CHAINED plans (a separate instance)
   static constexpr int CW = CW_;
   static constexpr int CT = CW * 32;       // consumer threads
   static constexpr int THREADS = CT + 32;  // + the producer warp
@@ -56,6 +57,8 @@ struct KCfg {
 };
 using Cfg1 = KCfg<16, 1>;
 using CfgB = KCfg<15, kChunkBatch>;
+using Cfg1C = KCfg<16, 1, true>;
+using CfgBC = KCfg<15, kChunkBatch, true>;
 
 enum : unsigned int { kErrFullWait = 1, kErrEmptyWait = 2, kErrGridBarrier = 3, kErrDrain = 4 };
 
@@ -94,6 +97,8 @@ struct PersistParams {
   const int32_t* verify_draft;
   int32_t* verify_emit;
   int32_t* verify_n;
+  // chained steps: every stage quantizes its input from the previous stages' outputs
+  ChainSrc head_src;  // the output projection's input (the residual stream)
 };
 
 // One timeline stamp (thread 0 of the consumers only).
@@ -103,7 +108,7 @@ __device__ __forceinline__ void stamp(const PersistParams& P, int b, int i) {
 }
 
 struct SmemLayout {
-  int ring, act, bars, hbest, red, abort_flag, total;
+  int ring, act, bars, hbest, red, abort_flag, chain_s, total;
 };
 
 template <class C>
@@ -115,7 +120,8 @@ __host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int a
   L.hbest = L.bars + 2 * C::BARS * 8;
   L.red = L.hbest + C::CW * kStepMaxBatch * (int)sizeof(HeadPartial);
   L.abort_flag = L.red + C::CW * 4;
-  L.total = L.abort_flag + 16;
+  L.chain_s = L.abort_flag + 16;
+  L.total = L.chain_s + kStepMaxBatch * 4;
   return L;
 }
 
@@ -388,6 +394,49 @@ __device__ void embed_row_consumers(const PersistParams& P, int b) {
   }
 }
 
+// Chained steps: quantizes the stage input of vectors b0 .. b0+nb-1 straight into this CTA's
+// activation buffer; every CTA computes the same codes from the same fp32 values, read
+// through L2. The scales go to s_chain. With `record` (CTA 0) the codes and scales are also
+// written to the q / s_x of the stage's matrices (rec[0..n_rec)) or of the output projection.
+template <class C>
+__device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, uint8_t* abuf, float* s_chain,
+                               float* red, bool record, const MatDesc* rec, int n_rec, int8_t* hq, float* hs) {
+  const int t = threadIdx.x;
+  for (int b = 0; b < nb; ++b) {
+    float m = 0.0f;
+    for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
+      const float4 v = chain_load4(cs, b0 + b, k);
+      m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((t & 31) == 0) red[t >> 5] = m;
+    consumer_sync<C>();
+    m = red[0];
+#pragma unroll
+    for (int i = 1; i < C::CW; ++i) m = fmaxf(m, red[i]);
+    const bool nz = m != 0.0f;
+    const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
+    for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
+      const uint32_t c = quant4(chain_load4(cs, b0 + b, k), s, nz);
+      *reinterpret_cast<uint32_t*>(abuf + b * act_k + k) = c;
+      if (record) {
+        const int64_t o = (int64_t)(b0 + b) * cs.K + k;
+        if (hq) *reinterpret_cast<uint32_t*>(hq + o) = c;
+        for (int r = 0; r < n_rec; ++r) *reinterpret_cast<uint32_t*>(const_cast<int8_t*>(rec[r].q) + o) = c;
+      }
+    }
+    if (t == 0) {
+      s_chain[b] = s;
+      if (record) {
+        if (hs) hs[b0 + b] = s;
+        for (int r = 0; r < n_rec; ++r) const_cast<float*>(rec[r].s_x)[b0 + b] = s;
+      }
+    }
+    consumer_sync<C>();  // red[] is reused by the next vector
+  }
+}
+
 // Grid-wide barrier among the consumers of all CTAs; `target` counts arrivals modulo 2^32.
 template <class C>
 __device__ void grid_barrier(const PersistParams& P, uint32_t target, int b, volatile int* s_abort) {
@@ -468,7 +517,7 @@ __device__ __forceinline__ void row_piece(const uint8_t* sb, const uint8_t* ab, 
 
 // One tile (4 rows) of a tiled ternary matrix against NB activation vectors. The row scale
 // is loaded before the first chunk so its latency hides behind the chunk work.
-template <int NB>
+template <int NB, bool CH>
 __device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDesc& m, const float (&sx)[NB], int b0,
                              int64_t tile, const uint8_t* act, Ring& ring, int lane, volatile int* s_abort) {
   const int pieces = (int)(padded_k(m.K) / 512);
@@ -493,7 +542,14 @@ __device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDe
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const int total = warp_sum4(acc[b][0], acc[b][1], acc[b][2], acc[b][3], lane);
-    if ((lane & 7) == 0 && n < m.N) m.y[(int64_t)(b0 + b) * m.N + n] = scale_out(total, sw, sx[b]);
+    if ((lane & 7) == 0 && n < m.N) {
+      const int64_t o = (int64_t)(b0 + b) * m.N + n;
+      const float yv = scale_out(total, sw, sx[b]);
+      m.y[o] = yv;
+      if constexpr (CH) {  // chained: the residual stream
+        if (m.res_out) m.res_out[o] = __fadd_rn(__ldcg(m.res_in + o), yv);
+      }
+    }
   }
 }
 
@@ -535,18 +591,22 @@ __device__ __forceinline__ void consume_head_row(const PersistParams& P, const f
 
 template <class C, int NB>
 __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkItem& it, uint32_t seq, const uint8_t* act,
-                             Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort) {
+                             Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort,
+                             const float* s_chain) {
   float sx[NB];
   const float* sxp = it.kind == kItemTernary ? P.mats[it.mat].s_x : P.head_sx;
 #pragma unroll
-  for (int b = 0; b < NB; ++b) sx[b] = __ldcg(sxp + it.b0 + b);
+  for (int b = 0; b < NB; ++b) {
+    if constexpr (C::CHAINED) sx[b] = s_chain[b];
+    else sx[b] = __ldcg(sxp + it.b0 + b);
+  }
   const int64_t first = first_unit<C>(it, seq, cw);
   // The abort flag is read by lane 0 and broadcast, so the whole warp takes one branch.
   if (it.kind == kItemTernary) {
     const MatDesc m = P.mats[it.mat];
     for (int64_t u = first; u < it.end; u += C::CW)
       if (!__shfl_sync(0xffffffffu, *s_abort, 0))
-        consume_tile<NB>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
+        consume_tile<NB, C::CHAINED>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
   } else {
     for (int64_t u = first; u < it.end; u += C::CW)
       if (!__shfl_sync(0xffffffffu, *s_abort, 0))
@@ -564,6 +624,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   HeadPartial* hbest = reinterpret_cast<HeadPartial*>(smem + L.hbest);  // [warp][kStepMaxBatch]
   float* red = reinterpret_cast<float*>(smem + L.red);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
+  float* s_chain = reinterpret_cast<float*>(smem + L.chain_s);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::BARS);
@@ -598,7 +659,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
 
   if (P.embed_T) {  // input-table rows of the step's tokens; quantization may read them
     for (int b = blockIdx.x; b < P.B; b += gridDim.x) embed_row_consumers<C>(P, b);
-    if (P.n_qjobs > 0) {
+    if (P.n_qjobs > 0 || C::CHAINED) {
       ++barriers;
       grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
       stamp(P, (int)barriers, 2);
@@ -619,6 +680,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   const int act_buf = P.chunk_b * P.act_k;
   int buf = 0;
   bool prefetched = false;
+  const float* chain_in0 = nullptr;  // chained: the stage input now in act[buf]
+  int chain_b0 = -1;
   for (int i = 0; i < n_items; ++i) {
     const WorkItem it = get_item(P, i);
     const bool staged = (it.flags & kFlagStage) != 0;
@@ -628,33 +691,58 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     }
     int K, nb;
     const int8_t* q = item_act(P, it, K, nb);
-    uint8_t* abuf = act + buf * act_buf;
-    if (prefetched) cp_async_wait_all();
-    else load_act<C>(abuf, q, K, nb, P.act_k, false);
-    consumer_sync<C>();  // act[buf] complete; every warp is past the previous item
-    if (staged) stamp(P, (int)barriers, 2);
-    prefetched = false;
-    if (i + 1 < n_items) {
-      const WorkItem nx = get_item(P, i + 1);
-      if (!(nx.flags & kFlagStage)) {
-        int K2, nb2;
-        const int8_t* q2 = item_act(P, nx, K2, nb2);
-        load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
-        prefetched = true;
+    const uint8_t* abuf;
+    const float* sc = nullptr;  // chained: the scales of the vectors in act[buf]
+    if constexpr (C::CHAINED) {  // the stage's matrices share one input: quantize it once per stage and pass
+      const ChainSrc cs = it.kind == kItemTernary ? P.mats[it.mat].src : P.head_src;
+      if ((staged || cs.in0 != chain_in0 || it.b0 != chain_b0) && (it.begin < it.end || blockIdx.x == 0)) {
+        buf ^= 1;
+        const bool rec = blockIdx.x == 0;
+        if (it.kind == kItemTernary) {
+          const int rf = P.mats[it.mat].rec_first, rn = P.mats[it.mat].rec_count;
+          chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, P.mats + rf, rn,
+                            nullptr, nullptr);
+        } else {
+          chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, nullptr, 0,
+                            const_cast<int8_t*>(P.head_q), const_cast<float*>(P.head_sx));
+        }
+        chain_in0 = cs.in0;
+        chain_b0 = it.b0;
       }
+      consumer_sync<C>();
+      if (staged) stamp(P, (int)barriers, 2);
+      abuf = act + buf * act_buf;
+      sc = s_chain;
+    } else {
+      uint8_t* ab = act + buf * act_buf;
+      if (prefetched) cp_async_wait_all();
+      else load_act<C>(ab, q, K, nb, P.act_k, false);
+      consumer_sync<C>();  // act[buf] complete; every warp is past the previous item
+      if (staged) stamp(P, (int)barriers, 2);
+      prefetched = false;
+      if (i + 1 < n_items) {
+        const WorkItem nx = get_item(P, i + 1);
+        if (!(nx.flags & kFlagStage)) {
+          int K2, nb2;
+          const int8_t* q2 = item_act(P, nx, K2, nb2);
+          load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
+          prefetched = true;
+        }
+      }
+      abuf = ab;
     }
     if constexpr (C::NBMAX == 1) {
-      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort);
+      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc);
     } else {
       switch (nb) {
-        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
-        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
-        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
-        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort); break;
+        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
+        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
+        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
+        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
       }
     }
     seq += (uint32_t)(it.end - it.begin);
-    buf ^= 1;
+    if constexpr (!C::CHAINED) buf ^= 1;
   }
   if (prefetched) cp_async_wait_all();
   consumer_sync<C>();
@@ -769,18 +857,20 @@ nt_status configure_kernel(int device) {
   if (device >= 0 && device < 64 && g_attr_set[device]) return NT_OK;
   NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<Cfg1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
   NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<CfgB>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+  NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<Cfg1C>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+  NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<CfgBC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
   if (device >= 0 && device < 64) g_attr_set[device] = true;
   return NT_OK;
 }
 
-// The kernel instance and block size for a batch.
-const void* kernel_for(int B, int* threads) {
-  if (B == 1) {
-    *threads = Cfg1::THREADS;
-    return reinterpret_cast<const void*>(persist_kernel<Cfg1>);
-  }
-  *threads = CfgB::THREADS;
-  return reinterpret_cast<const void*>(persist_kernel<CfgB>);
+// The kernel instance and block size for a batch and step mode.
+const void* kernel_for(int B, bool chained, int* threads) {
+  *threads = B == 1 ? Cfg1::THREADS : CfgB::THREADS;
+  if (chained)
+    return B == 1 ? reinterpret_cast<const void*>(persist_kernel<Cfg1C>)
+                  : reinterpret_cast<const void*>(persist_kernel<CfgBC>);
+  return B == 1 ? reinterpret_cast<const void*>(persist_kernel<Cfg1>)
+                : reinterpret_cast<const void*>(persist_kernel<CfgB>);
 }
 
 }  // namespace
@@ -793,7 +883,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
     return set_error(NT_ERR_INVALID_ARG, "persistent launcher: K too large for the shared-memory budget");
   NT_TRY(configure_kernel(p->device));
   int per_sm = 0, threads = 0;
-  const void* kern = kernel_for(p->B, &threads);
+  const void* kern = kernel_for(p->B, p->mode == NT_STEP_CHAINED, &threads);
   NT_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, p->smem_bytes));
   if (per_sm < 1) return set_error(NT_ERR_CUDA, "persistent kernel cannot be resident on an SM");
   const int grid = p->sm_count;
@@ -805,7 +895,8 @@ nt_status persist_prepare(nt_decode_plan* p) {
     return Unitset{kItemTernary, mi, padded_rows(p->mats[mi].N) / 4, padded_k(p->mats[mi].K)};
   };
   const Unitset head{kItemHead, 0, p->head_V, p->head_K};
-  int barriers = (p->n_qjobs > 0 ? 1 : 0) + (p->embed_T && p->n_qjobs > 0 ? 1 : 0);
+  const bool chained = p->mode == NT_STEP_CHAINED;
+  int barriers = (p->n_qjobs > 0 ? 1 : 0) + (p->embed_T && (p->n_qjobs > 0 || chained) ? 1 : 0);
   if (p->mode == NT_STEP_INDEPENDENT) {
     // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table (per pass),
     // so every CTA has the same mix of decode-heavy and decode-free work.
@@ -888,9 +979,10 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.verify_draft = p->verify_draft;
   P.verify_emit = p->verify_emit;
   P.verify_n = p->verify_n;
+  P.head_src = p->head_src;
   void* args[] = {&P};
   int threads = 0;
-  const void* kern = kernel_for(p->B, &threads);
+  const void* kern = kernel_for(p->B, p->mode == NT_STEP_CHAINED, &threads);
   const cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p->grid), dim3(threads), args, p->smem_bytes, st);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -7,6 +7,7 @@
 //   NT_LAUNCH_STREAM     one launch per stage issued on the caller's stream every step;
 //   NT_LAUNCH_GRAPH      the same launches captured once into a CUDA graph, replayed per step;
 //   NT_LAUNCH_PERSISTENT one cooperative kernel streams the whole step (nt_persist.cu).
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -20,12 +21,36 @@ namespace {
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Shapes of a chained step: every stage input has the length its matrices reduce over.
+nt_status validate_chain(const nt_decode_desc* d) {
+  const int hd = d->head_dim > 0 ? d->head_dim : 128;
+  if (hd % 4 != 0) return set_error(NT_ERR_INVALID_ARG, "chained: head_dim must be a multiple of 4");
+  if (!d->proj[0].x) return set_error(NT_ERR_INVALID_ARG, "chained: proj[0].x (the first hidden state) is NULL");
+  const int dm = d->proj[0].K;
+  for (int l = 0; l < d->n_layers; ++l) {
+    const nt_proj* p = d->proj + l * kProjPerLayer;
+    const nt_proj &q = p[0], &k = p[1], &v = p[2], &o = p[3], &g = p[4], &u = p[5], &dn = p[6];
+    const std::string at = "chained: layer " + std::to_string(l) + ": ";
+    if (q.K != dm || k.K != dm || v.K != dm || o.N != dm || g.K != dm || u.K != dm || dn.N != dm)
+      return set_error(NT_ERR_INVALID_ARG, at + "q/k/v/gate/up K and o/down N must all equal proj[0].K");
+    if (o.K != q.N || k.N != v.N || g.N != u.N || dn.K != g.N)
+      return set_error(NT_ERR_INVALID_ARG, at + "need o.K == q.N, k.N == v.N, gate.N == up.N == down.K");
+    if (v.N % hd != 0 || o.K % v.N != 0)
+      return set_error(NT_ERR_INVALID_ARG, at + "v.N must be a multiple of head_dim and divide o.K");
+    for (int i = 0; i < kProjPerLayer; ++i)
+      if (!aligned(p[i].y, 16)) return set_error(NT_ERR_ALIGNMENT, at + "outputs must be 16-byte aligned");
+  }
+  if (!aligned(d->proj[0].x, 16)) return set_error(NT_ERR_ALIGNMENT, "chained: proj[0].x must be 16-byte aligned");
+  if (d->head_T && d->head_K != dm) return set_error(NT_ERR_INVALID_ARG, "chained: head_K must equal proj[0].K");
+  return NT_OK;
+}
+
 nt_status validate_desc(const nt_decode_desc* d) {
   if (!d) return set_error(NT_ERR_INVALID_ARG, "NULL descriptor");
   if (d->n_layers < 1 || !d->proj) return set_error(NT_ERR_INVALID_ARG, "need n_layers >= 1 and a projection array");
   if (d->batch < 1 || d->batch > kStepMaxBatch) return set_error(NT_ERR_INVALID_ARG, "batch must be in [1, 16]");
-  if (d->mode != NT_STEP_INDEPENDENT && d->mode != NT_STEP_ORDERED)
-    return set_error(NT_ERR_INVALID_ARG, "mode must be NT_STEP_INDEPENDENT or NT_STEP_ORDERED");
+  if (d->mode != NT_STEP_INDEPENDENT && d->mode != NT_STEP_ORDERED && d->mode != NT_STEP_CHAINED)
+    return set_error(NT_ERR_INVALID_ARG, "mode must be NT_STEP_INDEPENDENT, NT_STEP_ORDERED or NT_STEP_CHAINED");
   if (d->launcher != NT_LAUNCH_PERSISTENT && d->launcher != NT_LAUNCH_GRAPH && d->launcher != NT_LAUNCH_STREAM)
     return set_error(NT_ERR_INVALID_ARG, "unknown launcher");
   for (int i = 0; i < d->n_layers * kProjPerLayer; ++i) {
@@ -58,6 +83,7 @@ nt_status validate_desc(const nt_decode_desc* d) {
     if (!d->verify_n || (d->batch > 1 && !d->verify_draft))
       return set_error(NT_ERR_INVALID_ARG, "verify: NULL pointer");
   }
+  if (d->mode == NT_STEP_CHAINED) return validate_chain(d);
   return NT_OK;
 }
 
@@ -66,9 +92,14 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
   if (p->embed_T)
     NT_TRY(launch_embed(p->embed_T, p->embed_s, p->embed_V, p->embed_K, p->tokens, p->B, p->embed_x, nullptr, st));
   if (p->n_qjobs) NT_TRY(launch_quantize_jobs(p->d_qjobs, p->n_qjobs, p->B, st));
-  for (const PlanStage& s : p->stages)
+  const bool chained = p->mode == NT_STEP_CHAINED;
+  for (size_t i = 0; i < p->stages.size(); ++i) {
+    const PlanStage& s = p->stages[i];
+    if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st));
     NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
                                    s.total_tiles, p->B, st));
+  }
+  if (p->has_head && chained) NT_TRY(launch_chain_quant(p->d_cjobs + p->stages.size(), p->B, st));
   if (p->has_head)
     NT_TRY(launch_head(p->head_T, p->head_s, p->head_V, p->head_K, p->head_q, p->head_sx, p->B,
                        p->head_logits, p->head_argmax, p->d_head_ws, st));
@@ -86,6 +117,9 @@ void free_plan(nt_decode_plan* p) {
   cudaFree(p->d_head_ws);
   cudaFree(p->d_ctrl);
   cudaFree(p->d_sched);
+  cudaFree(p->d_resid);
+  cudaFree(p->d_chain_tmp);
+  cudaFree(p->d_cjobs);
   delete p;
 }
 
@@ -126,7 +160,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     m.N = pr.N;
     m.K = pr.K;
     m.B = d->batch;
-    if (pr.x) jobs.push_back(QuantJob{pr.x, pr.q, pr.s_x, pr.K, d->batch});
+    if (pr.x && d->mode != NT_STEP_CHAINED) jobs.push_back(QuantJob{pr.x, pr.q, pr.s_x, pr.K, d->batch});
   }
   p->mats = mats;
   std::vector<int64_t> prefix;
@@ -163,7 +197,8 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     p->head_sx = d->head_sx;
     p->head_logits = d->head_logits;
     p->head_argmax = d->head_argmax;
-    if (d->head_x) jobs.push_back(QuantJob{d->head_x, d->head_q, d->head_sx, d->head_K, d->batch});
+    if (d->head_x && d->mode != NT_STEP_CHAINED)
+      jobs.push_back(QuantJob{d->head_x, d->head_q, d->head_sx, d->head_K, d->batch});
   }
   p->n_qjobs = (int)jobs.size();
   p->embed_T = d->embed_T;
@@ -183,6 +218,75 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     return NT_ERR_CUDA;
   };
   cudaError_t e;
+  std::vector<ChainJob> cjobs;
+  if (d->mode == NT_STEP_CHAINED) {
+    // The residual stream and the stage inputs (see nt_step_mode): the persistent kernel
+    // reads each stage's input from the matrices' ChainSrc and adds o / down outputs into the
+    // residual stream in their epilogue; the stream / graph launchers run one ChainJob per
+    // stage, which also writes the residual stream.
+    const int dm = d->proj[0].K, B = d->batch;
+    p->head_dim = d->head_dim > 0 ? d->head_dim : 128;
+    int kmax = dm;
+    for (const MatDesc& m : mats) kmax = std::max(kmax, m.K);
+    if ((e = cudaMalloc(&p->d_resid, sizeof(float) * (size_t)B * dm)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMalloc(&p->d_chain_tmp, sizeof(float) * (size_t)B * kmax)) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc");
+    float* R = p->d_resid;
+    const float* x0 = d->proj[0].x;
+    const int hd = p->head_dim;
+    auto job = [&](ChainSrc src, float* vbuf, int first, int n) {
+      ChainJob j{};
+      j.src = src;
+      j.vbuf = vbuf;
+      j.n_rec = n;
+      for (int r = 0; r < n; ++r) {
+        j.q[r] = const_cast<int8_t*>(mats[first + r].q);
+        j.s[r] = const_cast<float*>(mats[first + r].s_x);
+      }
+      cjobs.push_back(j);
+    };
+    for (int l = 0; l < d->n_layers; ++l) {
+      const int b = l * kProjPerLayer;
+      MatDesc* m = mats.data() + b;
+      const float* h = l == 0 ? x0 : R;
+      const int G = m[3].K / m[2].N;
+      for (int i = 0; i < 3; ++i) m[i].src = ChainSrc{h, nullptr, kChainDirect, dm, 1, hd};
+      m[3].src = ChainSrc{m[2].y, nullptr, kChainHeads, m[3].K, G, hd};
+      m[3].res_in = h;
+      m[3].res_out = R;
+      for (int i = 4; i < 6; ++i) m[i].src = ChainSrc{R, nullptr, kChainDirect, dm, 1, hd};
+      m[6].src = ChainSrc{m[4].y, m[5].y, kChainProduct, m[6].K, 1, hd};
+      m[6].res_in = R;
+      m[6].res_out = R;
+      const int recf[4] = {b, b + 3, b + 4, b + 6}, recn[4] = {3, 1, 2, 1};
+      for (int g = 0; g < 4; ++g)
+        for (int i = 0; i < recn[g]; ++i) {
+          mats[recf[g] + i].rec_first = recf[g];
+          mats[recf[g] + i].rec_count = recn[g];
+        }
+      // stream / graph launchers: the residual additions happen in the stage-input jobs
+      if (l == 0) job(ChainSrc{x0, nullptr, kChainDirect, dm, 1, hd}, p->d_chain_tmp, b, 3);
+      else job(ChainSrc{R, mats[b - 1].y, kChainSum, dm, 1, hd}, R, b, 3);
+      job(m[3].src, p->d_chain_tmp, b + 3, 1);
+      job(ChainSrc{h, m[3].y, kChainSum, dm, 1, hd}, R, b + 4, 2);
+      job(m[6].src, p->d_chain_tmp, b + 6, 1);
+    }
+    p->head_src = ChainSrc{R, nullptr, kChainDirect, dm, 1, hd};
+    if (p->has_head) {
+      ChainJob j{};
+      j.src = ChainSrc{R, mats[n_proj - 1].y, kChainSum, dm, 1, hd};
+      j.vbuf = R;
+      j.n_rec = 1;
+      j.q[0] = const_cast<int8_t*>(p->head_q);
+      j.s[0] = const_cast<float*>(p->head_sx);
+      cjobs.push_back(j);
+    }
+    p->mats = mats;
+    p->n_cjobs = (int)cjobs.size();
+    if ((e = cudaMalloc(&p->d_cjobs, sizeof(ChainJob) * cjobs.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemcpy(p->d_cjobs, cjobs.data(), sizeof(ChainJob) * cjobs.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy");
+  }
   if ((e = cudaMalloc(&p->d_mats, sizeof(MatDesc) * mats.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
   if ((e = cudaMemcpy(p->d_mats, mats.data(), sizeof(MatDesc) * mats.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy");

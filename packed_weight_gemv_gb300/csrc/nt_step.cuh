@@ -80,6 +80,13 @@ struct nt_decode_plan {
   int nslots = 0, chunk_b = 0;      // ring slots per consumer warp; vectors per pass
   uint64_t launches = 0;
   unsigned long long* trace = nullptr;  // optional step timeline (nt_decode_plan_set_trace)
+  // chained steps (NT_STEP_CHAINED)
+  int head_dim = 128;
+  nt::ChainSrc head_src{};          // the output projection's input (persistent launcher)
+  float* d_resid = nullptr;         // [B][d] residual stream, owned by the plan
+  float* d_chain_tmp = nullptr;     // [B][max K] stage inputs of the stream / graph launchers
+  nt::ChainJob* d_cjobs = nullptr;  // one per stage, then one for the output projection
+  int n_cjobs = 0;
 };
 
 namespace nt {

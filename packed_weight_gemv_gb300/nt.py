@@ -29,6 +29,7 @@ NT_LAYOUT_PLAIN = 0
 NT_LAYOUT_TILED = 1
 NT_STEP_INDEPENDENT = 0
 NT_STEP_ORDERED = 1
+NT_STEP_CHAINED = 2
 NT_LAUNCH_PERSISTENT = 0
 NT_LAUNCH_GRAPH = 1
 NT_LAUNCH_STREAM = 2
@@ -70,7 +71,7 @@ class nt_decode_desc(ctypes.Structure):
                 ("embed_V", ctypes.c_int), ("embed_K", ctypes.c_int),
                 ("tokens", ctypes.c_void_p), ("embed_x", ctypes.c_void_p),
                 ("verify_draft", ctypes.c_void_p), ("verify_emit", ctypes.c_void_p),
-                ("verify_n", ctypes.c_void_p)]
+                ("verify_n", ctypes.c_void_p), ("head_dim", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -241,7 +242,7 @@ class DecodePlan:
     def __init__(self, n_layers: int, batch: int, projs: Sequence[dict], head: Optional[dict],
                  mode: int = NT_STEP_INDEPENDENT, launcher: int = NT_LAUNCH_PERSISTENT,
                  timeout_ms: float = 0.0, test_fault: int = 0, embed: Optional[dict] = None,
-                 verify: Optional[dict] = None):
+                 verify: Optional[dict] = None, head_dim: int = 0):
         lib = load_library()
         self._keep = [projs, head, embed, verify]
         arr = (nt_proj * len(projs))()
@@ -259,6 +260,7 @@ class DecodePlan:
             d.head_logits = head["logits"].data_ptr() if head.get("logits") is not None else None
             d.head_argmax = head["argmax"].data_ptr()
         d.mode, d.launcher, d.timeout_ms, d.test_fault = mode, launcher, timeout_ms, test_fault
+        d.head_dim = head_dim
         if embed is not None:
             d.embed_T, d.embed_s = embed["T"].data_ptr(), embed["s"].data_ptr()
             d.embed_V, d.embed_K = embed["V"], embed["K"]
