@@ -573,6 +573,71 @@ def run_verify(args):
 
 
 # ---------------------------------------------------------------------------------------
+# Attention over the key-value cache (not the headline line): the 36 layers' grouped-query
+# attention of one new position at several context lengths
+# ---------------------------------------------------------------------------------------
+
+def run_attention(args):
+    import torch
+
+    from oracle import layer_ops as lo
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    L, Hq, Hkv, D = args.layers, 32, 8, 128
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.current_stream()
+    for T in (4096, 16384, 32768):
+        # one cache per layer, bf16 N(0,1) keys and values (the layers' contents differ only by
+        # seed; the attention's cost does not depend on the values)
+        kb = wl.bf16_normal(Hkv * T * D, 0, wl.tag(wl.WL_ATTN, T, 1, 0))
+        vb = wl.bf16_normal(Hkv * T * D, 0, wl.tag(wl.WL_ATTN, T, 2, 0))
+        kc = [torch.from_numpy(kb.view(np.int16)).to(dev) for _ in range(L)]
+        vc = [torch.from_numpy(vb.view(np.int16)).to(dev) for _ in range(L)]
+        q = wl.normal(L * Hq * D, 0, wl.tag(wl.WL_ATTN, T, 3, 0)).reshape(L, 1, Hq, D)
+        qd = torch.from_numpy(q).to(dev)
+        out = torch.empty((L, 1, Hq, D), device=dev)
+        ws = torch.zeros(nt.nt_attention_workspace_size(1, Hq, Hkv, T), dtype=torch.uint8, device=dev)
+
+        def one_token():
+            for l in range(L):
+                nt.nt_attention_decode(qd[l], kc[l], vc[l], 1, Hq, Hkv, D, T, T, out[l], ws)
+
+        for _ in range(max(3, args.warmup)):
+            one_token()
+        torch.cuda.synchronize()
+        want = lo.attention_decode(q[0], lo.from_bf16_bits(kb.reshape(Hkv, T, D)),
+                                   lo.from_bf16_bits(vb.reshape(Hkv, T, D)), T)
+        vmax = float(np.abs(lo.from_bf16_bits(vb)).max())
+        err = float(np.abs(out[0].cpu().numpy().astype(np.float64) - want).max())
+        parity = "pass" if err <= 3e-5 * vmax else f"max error {err:.3g}"
+        steps = max(3, min(args.steps, 200))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_token()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / steps
+        nbytes = L * 2 * Hkv * T * D * 2
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"metric": "attention over the key-value cache (36 layers, 1 position)",
+                          "context": T, "steps": steps, "us_per_token": round(us, 2),
+                          "cache_bytes_per_token": nbytes, "achieved_GBps": round(gbs, 1),
+                          "peak_GBps": peak, "frac": round(gbs / peak, 4), "peak_source": peak_kind,
+                          "launches_per_token": L, "parity": parity}), flush=True)
+        del graph, kc, vc, qd, out, ws
+        torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------------------
 # Prefill (not the headline line): the 28-layer small model at M = 2048 and 8192 tokens on
 # the tensor-core GEMM
 # ---------------------------------------------------------------------------------------
@@ -686,6 +751,8 @@ def main():
                     help="batched sweep B = 1, 2, 4, 8, 16 (one JSON line per batch)")
     ap.add_argument("--verify", action="store_true",
                     help="speculative verify passes of 2, 4 and 8 positions (gather + step + acceptance)")
+    ap.add_argument("--attention", action="store_true",
+                    help="attention over the key-value cache at 4K/16K/32K context (36 layers)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
@@ -702,6 +769,9 @@ def main():
         return
     if args.verify:
         run_verify(args)
+        return
+    if args.attention:
+        run_attention(args)
         return
     if args.prefill:
         run_prefill(args)

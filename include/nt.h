@@ -221,6 +221,44 @@ nt_status nt_verify_accept(const int32_t* draft, const int32_t* argmax, int B, i
                            int32_t* n_emit, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Attention side of a layer ("At 26K tokens, the cache becomes larger than the model": 36
+ * layers x 8 key-value heads x 128 dimensions at 16 bits = 147,456 bytes per cached position;
+ * grouped-query attention, so the 32 query heads read the 8 key-value heads). The pages give
+ * no formulas for the layer's other operations; the plain readings are stated per call.
+ * Head dimension D must be 128 (NT_ERR_UNSUPPORTED otherwise).
+ *
+ * nt_attention_decode: B new positions attend over a cache of T rows whose last B rows are
+ * those positions (they were appended first, e.g. by nt_rope_append): position b sees rows
+ * 0 .. T - B + b. out[b][h] = sum_t softmax_t(q[b][h] . k[g][t] / sqrt(D)) v[g][t] with
+ * g = h / (Hq / Hkv). fp32 arithmetic; the result is within a few 1e-6 of the exact value
+ * relative to max |v| (one launch: 128-position chunks, merged by the last chunk to finish).
+ *   q [B][Hq][D] fp32; k_cache, v_cache [Hkv][t_stride][D] bf16 bit patterns (16-byte
+ *   aligned); out [B][Hq][D] fp32; Hq / Hkv in {1, 2, 4, 8}; 1 <= B <= 64; B <= T <= t_stride.
+ *   ws: device workspace of nt_attention_workspace_size(B, Hq, Hkv, T) bytes (16-byte
+ *   aligned), all zero before its first use (every call leaves its counters zero again);
+ *   calls sharing a workspace must not overlap.
+ */
+nt_status nt_attention_workspace_size(int B, int Hq, int Hkv, int T, size_t* bytes);
+nt_status nt_attention_decode(const float* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              int B, int Hq, int Hkv, int D, int T, int t_stride, float* out,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Rotary embedding of B new positions pos0 .. pos0 + B - 1 and their append to the cache.
+ * Rotate-half pairing (dimension i with i + D/2) by the angle pos * base^(-2i/D), the angles
+ * formed in double precision, the rotations in fp32. q_out[b][h] = rotated q[b][h] (fp32);
+ * k_cache[g][pos0 + b] = bf16(rotated k_new[b][g]); v_cache[g][pos0 + b] = bf16(v_new[b][g])
+ * (round to nearest even). q [B][Hq][D], k_new / v_new [B][Hkv][D] fp32; base > 1 (10000 is
+ * the textbook value); pos0 + B <= t_stride. q_out may alias q. */
+nt_status nt_rope_append(const float* q, const float* k_new, const float* v_new, int B, int Hq,
+                         int Hkv, int D, int pos0, float base, float* q_out, uint16_t* k_cache,
+                         uint16_t* v_cache, int t_stride, void* stream);
+
+/* RMS normalisation of B vectors of length D: y = fl(fl(x * r) * gamma) with
+ * r = fl32(1 / sqrt(mean(x^2) + eps)) formed in double. x, y [B][D]; gamma [D]; y may alias x. */
+nt_status nt_rmsnorm(const float* x, const float* gamma, int B, int D, float eps, float* y,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Decode step: every projection of every layer, then optionally the output projection, in
  * one submission ("A 104 microsecond floor ...": on the instrumented A100 step, roughly
  * 590 of 694 microseconds were spent across about 120 kernel boundaries rather than in

@@ -92,6 +92,16 @@ nt_status launch_embed(const int8_t* T, const float* s, int V, int K, const int3
 nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit, int32_t* n_emit,
                         cudaStream_t st);
 
+// Attention side of a layer (nt_attention.cu): head dimension 128.
+// The workspace's counters (after the partial results) must be zero before the first call;
+// every call leaves them zero.
+size_t attention_ws_bytes(int B, int Hq, int Hkv, int T);
+nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* vc, int B, int Hq, int Hkv, int T,
+                           int ts, float* out, void* ws, cudaStream_t st);
+nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
+                             float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st);
+nt_status launch_rmsnorm(const float* x, const float* gamma, int B, int D, float eps, float* y, cudaStream_t st);
+
 // Tensor-core ternary GEMM (tcgen05, bf16 operands, exact fp32 accumulation) for
 // prefill-shaped batches of at least kTcMinBatch vectors.
 constexpr int kTcMinBatch = 64;

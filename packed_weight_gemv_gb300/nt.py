@@ -40,6 +40,7 @@ EXPORTS = (
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
     "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
     "nt_int8_logits_argmax_noalloc", "nt_embed_rows", "nt_verify_accept",
+    "nt_attention_workspace_size", "nt_attention_decode", "nt_rope_append", "nt_rmsnorm",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
     "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_destroy",
 )
@@ -105,6 +106,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_int8_logits_argmax_noalloc": ([vp, vp, i, i, vp, vp, i, vp, vp, vp], i),
             "nt_embed_rows": ([vp, vp, i, i, vp, i, vp, vp, vp], i),
             "nt_verify_accept": ([vp, vp, i, vp, vp, vp], i),
+            "nt_attention_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], i),
+            "nt_attention_decode": ([vp, vp, vp, i, i, i, i, i, i, vp, vp, sz, vp], i),
+            "nt_rope_append": ([vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp, vp, vp, i, vp], i),
+            "nt_rmsnorm": ([vp, vp, i, i, ctypes.c_float, vp, vp], i),
             "nt_decode_plan_create": ([ctypes.POINTER(nt_decode_desc), ctypes.POINTER(vp)], i),
             "nt_decode_step": ([vp, vp], i),
             "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
@@ -226,6 +231,33 @@ def nt_verify_accept(draft: Optional[torch.Tensor], argmax: torch.Tensor, B: int
                      emit: torch.Tensor, n_emit: torch.Tensor, stream=None):
     _check(load_library().nt_verify_accept(_ptr(draft), _ptr(argmax), B, _ptr(emit), _ptr(n_emit),
                                            _stream(stream)), "nt_verify_accept")
+
+
+def nt_attention_workspace_size(B: int, Hq: int, Hkv: int, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().nt_attention_workspace_size(B, Hq, Hkv, T, ctypes.byref(n)), "nt_attention_workspace_size")
+    return n.value
+
+
+def nt_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, B: int, Hq: int,
+                        Hkv: int, D: int, T: int, t_stride: int, out: torch.Tensor, ws: torch.Tensor,
+                        stream=None):
+    _check(load_library().nt_attention_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), B, Hq, Hkv, D, T, t_stride, _ptr(out), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)), "nt_attention_decode")
+
+
+def nt_rope_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, B: int, Hq: int, Hkv: int,
+                   D: int, pos0: int, base: float, q_out: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, t_stride: int, stream=None):
+    _check(load_library().nt_rope_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), B, Hq, Hkv, D, pos0, base, _ptr(q_out), _ptr(k_cache),
+        _ptr(v_cache), t_stride, _stream(stream)), "nt_rope_append")
+
+
+def nt_rmsnorm(x: torch.Tensor, gamma: torch.Tensor, B: int, D: int, eps: float, y: torch.Tensor,
+               stream=None):
+    _check(load_library().nt_rmsnorm(_ptr(x), _ptr(gamma), B, D, eps, _ptr(y), _stream(stream)), "nt_rmsnorm")
 
 
 class DecodePlan:

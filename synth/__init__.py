@@ -98,6 +98,11 @@ def normal(n: int, seed: int, tag: int) -> np.ndarray:
     return x
 
 
+def bf16_normal(n: int, seed: int, tag: int) -> np.ndarray:
+    """bf16 bit patterns (uint16) of N(0, 1) draws, the fp32 values' low 16 bits dropped."""
+    return (normal(n, seed, tag).view(np.uint32) >> 16).astype(np.uint16)
+
+
 def int8_uniform(n: int, seed: int, tag: int) -> np.ndarray:
     """int8 integers uniform in [-127, 127]."""
     t = np.empty(n, dtype=np.int8)

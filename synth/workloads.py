@@ -20,7 +20,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import draws, int8_uniform, normal, scales, ternary_plain
+from . import bf16_normal, draws, int8_uniform, normal, scales, ternary_plain
 
 PROJ_NAMES = ("q", "k", "v", "o", "gate", "up", "down")
 
@@ -36,7 +36,7 @@ SINGLE_N, SINGLE_K = 1536, 512
 SWEEP_BATCHES = (1, 2, 4, 8, 16)
 PREFILL_TOKENS = (2048, 8192)
 
-WL_SINGLE, WL_DECODE, WL_HEAD, WL_SWEEP, WL_PREFILL, WL_EMBED = 1, 2, 3, 4, 5, 6
+WL_SINGLE, WL_DECODE, WL_HEAD, WL_SWEEP, WL_PREFILL, WL_EMBED, WL_ATTN = 1, 2, 3, 4, 5, 6, 7
 ROLE_TRITS, ROLE_ROW_SCALE, ROLE_X, ROLE_TABLE, ROLE_TABLE_SCALE, ROLE_HIDDEN = 1, 2, 3, 4, 5, 6
 ROLE_TOKENS, ROLE_DRAFT = 7, 8
 
