@@ -17,7 +17,9 @@ Every function takes and returns numpy arrays and runs the plain loops of ``orac
 * :func:`embed_rows` -- the input-table rows of the current tokens, dequantized;
 * :func:`verify_accept` -- the longest agreeing prefix of a batched verify pass;
 * :func:`decode_chained` (``chain.py``) -- a step whose stages quantize the previous stage's
-  output (single-position attention, residual stream, gated product).
+  output (single-position attention, residual stream, gated product);
+* :func:`decode_chained_attention` (``chain.py``) -- the same with the attention side
+  (normalisations, rotary embedding, attention over a cache, SiLU; ``layer_ops.py``).
 
 Pins (``tests/test_oracle_*.py``) tie each of these to brute force, closed forms, invariants
 and hand-worked fixtures under ``tests/golden/``.
@@ -265,3 +267,9 @@ def verify_accept(draft, argmax):
 def decode_chained(layers, x0, head=None, head_dim: int = 128):
     from .chain import decode_chained as _chained
     return _chained(default(), layers, x0, head, head_dim)
+
+
+def decode_chained_attention(layers, x0, head, k_cache, v_cache, pos, norm_attn=None, norm_ffn=None,
+                             norm_final=None, base=10000.0, eps=1e-6):
+    from .chain import decode_chained_attention as _chained
+    return _chained(default(), layers, x0, head, k_cache, v_cache, pos, norm_attn, norm_ffn, norm_final, base, eps)

@@ -170,8 +170,69 @@ MUTATIONS = {
 def test_chain_mutant_is_caught(name):
     old, new = MUTATIONS[name]
     src = open(CHAIN_SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    head, sep, tail = src.partition("def decode_chained_attention")  # plant in decode_chained only
+    assert head.count(old) == 1, f"mutation anchor for {name} not unique"
     ns = {"__name__": "chain_mutant"}
-    exec(compile(src.replace(old, new), "chain_mutant.py", "exec"), ns)
+    exec(compile(head.replace(old, new) + sep + tail, "chain_mutant.py", "exec"), ns)
     caught = not check_selection_chain(ns["decode_chained"]) or not check_zero_chain(ns["decode_chained"])
     assert caught, f"mutation {name} was not caught"
+
+
+# ---- the chained step with the attention side ------------------------------------------------
+
+from oracle import layer_ops as lo  # noqa: E402
+
+SHAPES_ATT = [(256, 128), (128, 128), (128, 128), (128, 256), (192, 128), (192, 128), (128, 192)]
+
+
+def att_model(n_layers, seed, zero=False):
+    layers = []
+    for l in range(n_layers):
+        mats = []
+        for i, (N, K) in enumerate(SHAPES_ATT):
+            if zero:
+                w = np.zeros((N, K // 16), np.uint32)
+            else:
+                w = synth.ternary_plain(N, K, seed, 100 * l + i)
+            mats.append((w, synth.scales(N, np.sqrt(K), seed, 1000 + 100 * l + i), N, K))
+        layers.append(mats)
+    return layers
+
+
+def test_attention_chain_single_position_is_the_value():
+    # position 0, one vector: attention over the one cached row returns its value, so u is the
+    # key-value head's bf16 value repeated for the query heads of its group
+    layers = att_model(1, 21)
+    x0 = synth.normal(128, 21, 1).reshape(1, 128)
+    kc, vc = [np.zeros((1, 4, 128), np.float32)], [np.zeros((1, 4, 128), np.float32)]
+    out = chain_mod.decode_chained_attention(oracle.default(), layers, x0, None, kc, vc, 0)
+    y_v = out["y"][2]
+    want = np.tile(lo.bf16_round(y_v), (1, 2))  # 2 query heads, 1 key-value head
+    assert np.array_equal(out["u"][0], want)
+    assert np.array_equal(vc[0][0, 0], lo.bf16_round(y_v[0]))
+
+
+def test_attention_chain_zero_weights_average_the_cache():
+    # all projections zero: new keys and values are zero, every score is zero, so position b
+    # averages value rows 0 .. pos + b; the residual stream carries the input through
+    layers = att_model(2, 22, zero=True)
+    B, pos = 2, 5
+    x0 = synth.normal(B * 128, 22, 1).reshape(B, 128)
+    kc = [lo.bf16_round(synth.normal(128 * 8, 22, 2 + l).reshape(1, 8, 128)) for l in range(2)]
+    vc = [lo.bf16_round(synth.normal(128 * 8, 22, 4 + l).reshape(1, 8, 128)) for l in range(2)]
+    v0 = [v.copy() for v in vc]
+    V, g = 50, synth.scales(128, 1.0, 22, 9)
+    T = synth.int8_uniform(V * 128, 22, 10).reshape(V, 128)
+    s_T = synth.scales(V, 4096.0, 22, 11)
+    out = chain_mod.decode_chained_attention(oracle.default(), layers, x0, (T, s_T, V, 128), kc, vc, pos,
+                                             norm_final=g)
+    for l in range(2):
+        assert not kc[l][:, pos:pos + B].any() and not vc[l][:, pos:pos + B].any()
+        for b in range(B):
+            rows = np.concatenate([v0[l][0, :pos], np.zeros((b + 1, 128), np.float32)])
+            want = np.tile(rows.astype(np.float64).mean(axis=0), 2)
+            assert np.allclose(out["u"][l][b], want, rtol=1e-6, atol=1e-7)
+    assert np.array_equal(out["h"][-1], x0)
+    q, s = oracle.quantize(lo.rmsnorm(x0, g).astype(np.float32))
+    _, am, _ = oracle.logits_argmax(T, s_T, V, 128, q, s)
+    assert np.array_equal(out["argmax"], am)
