@@ -638,6 +638,76 @@ def run_attention(args):
 
 
 # ---------------------------------------------------------------------------------------
+# Chained decode with the attention side (not the headline line): every stage quantizes the
+# previous one's output; norms, rotary embedding, cache append, attention, SiLU gate
+# ---------------------------------------------------------------------------------------
+
+def run_layer_attention(args):
+    import torch
+
+    import oracle
+    from oracle import layer_ops as lo
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    L = args.layers
+    projs, head, dp, hd, _ = build_inputs(torch, nt, dev, L)
+    Hkv, d = 8, 4096
+    stream = torch.cuda.current_stream()
+    gam = [torch.from_numpy(wl.scales(d, 1.0, 0, wl.tag(wl.WL_ATTN, l, 4, 0))).to(dev) for l in range(2 * L + 1)]
+    for T in (4096, 16384):
+        pos = T - 1
+        kb = wl.bf16_normal(Hkv * T * 128, 0, wl.tag(wl.WL_ATTN, T, 1, 0)).reshape(Hkv, T, 128)
+        vb = wl.bf16_normal(Hkv * T * 128, 0, wl.tag(wl.WL_ATTN, T, 2, 0)).reshape(Hkv, T, 128)
+        kc = [torch.from_numpy(kb.view(np.int16)).to(dev) for _ in range(L)]
+        vc = [torch.from_numpy(vb.view(np.int16)).to(dev) for _ in range(L)]
+        att = dict(k_cache=kc, v_cache=vc, t_stride=T, pos=pos, norm_attn=gam[:L], norm_ffn=gam[L:2 * L],
+                   norm_final=gam[2 * L])
+        # parity first: the first two layers as their own chained plan against the oracle
+        L2 = min(2, L)
+        p2 = nt.DecodePlan(L2, 1, dp[:7 * L2], hd, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH,
+                           attention=dict(att, k_cache=kc[:L2], v_cache=vc[:L2], norm_attn=gam[:L2],
+                                          norm_ffn=gam[L:L + L2]))
+        p2.nt_decode_step(stream)
+        torch.cuda.synchronize()
+        layers = []
+        for l in range(L2):
+            mats = []
+            for i in range(7):
+                full = wl.projection(wl.WL_DECODE, l, i, projs[7 * l + i].N, projs[7 * l + i].K)
+                mats.append((full.w_plain, full.s_w, full.N, full.K))
+            layers.append(mats)
+        kf = [lo.from_bf16_bits(kb).copy() for _ in range(L2)]
+        vf = [lo.from_bf16_bits(vb).copy() for _ in range(L2)]
+        g_np = [g.cpu().numpy() for g in gam]
+        want = oracle.decode_chained_attention(layers, wl.projection_x(wl.WL_DECODE, 0, 0, d, 1), (head.T, head.s_T, head.V, head.K),
+                                               kf, vf, pos, g_np[:L2], g_np[L:L + L2], g_np[2 * L])
+        parity = "pass"
+        for i in range(7 * L2):
+            y = dp[i]["y"].cpu().numpy().reshape(1, -1).astype(np.float64)
+            if np.abs(y - want["y"][i]).max() > 2e-3 * np.abs(want["y"][i]).max():
+                parity = f"{projs[i].name} differs"
+        p2.close()
+        # restore the caches' new row for the timed plan (the two-layer plan rewrote it)
+        plan = nt.DecodePlan(L, 1, dp, hd, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH, attention=att)
+        for _ in range(max(3, args.warmup)):
+            plan.nt_decode_step(stream)
+        steps = max(3, min(args.steps, 100))
+        us = time_steps(torch, plan, steps, stream) / steps
+        kv = L * 2 * Hkv * T * 128 * 2
+        print(json.dumps({"metric": "chained decode with attention (graph launcher)", "context": T,
+                          "layers": L, "steps": steps, "us_per_token": round(us, 2),
+                          "weight_bytes": step_bytes(n_layers=L), "cache_bytes": kv,
+                          "GBps_weights_plus_cache": round((step_bytes(n_layers=L) + kv) / (us * 1e-6) / 1e9, 1),
+                          "launches_per_token": L * 12 + 2, "parity_first_two_layers": parity}), flush=True)
+        plan.close()
+        del kc, vc
+        torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------------------
 # Prefill (not the headline line): the 28-layer small model at M = 2048 and 8192 tokens on
 # the tensor-core GEMM
 # ---------------------------------------------------------------------------------------
@@ -753,6 +823,8 @@ def main():
                     help="speculative verify passes of 2, 4 and 8 positions (gather + step + acceptance)")
     ap.add_argument("--attention", action="store_true",
                     help="attention over the key-value cache at 4K/16K/32K context (36 layers)")
+    ap.add_argument("--layer-attention", action="store_true",
+                    help="chained decode with norms, rotary embedding and attention at 4K/16K context")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
@@ -772,6 +844,9 @@ def main():
         return
     if args.attention:
         run_attention(args)
+        return
+    if args.layer_attention:
+        run_layer_attention(args)
         return
     if args.prefill:
         run_prefill(args)

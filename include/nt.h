@@ -343,6 +343,26 @@ typedef struct nt_decode_desc {
   int32_t* verify_n;            /* [1] number of emitted tokens */
   int head_dim;                 /* NT_STEP_CHAINED: dimensions per attention head, a multiple of
                                    4 (0 selects 128, "At 26K tokens ...": 128 per head) */
+  /* NT_STEP_CHAINED with the layer's attention side (attn_k_cache != NULL; stream and graph
+     launchers -- the persistent launcher returns NT_ERR_UNSUPPORTED; head_dim must be 128).
+     Per layer, with the step's B vectors at positions pos .. pos + B - 1:
+       {q,k,v} <- Q(rmsnorm(h) * norm_attn[l]);
+       q, k rotated (nt_rope_append); k, v appended to the layer's cache at rows pos ..;
+       u = attention of the B positions over rows 0 .. pos + B - 1 (nt_attention_decode);
+       {o} <- Q(u); a = h + y_o; {gate,up} <- Q(rmsnorm(a) * norm_ffn[l]);
+       {down} <- Q(silu(y_gate) * y_up); next h = a + y_down;
+     the output projection scores Q(rmsnorm(h_last) * norm_final). A NULL weight array or
+     vector leaves that normalisation out. */
+  uint16_t* const* attn_k_cache; /* host array [n_layers] of device [Hkv][attn_t_stride][128] bf16 */
+  uint16_t* const* attn_v_cache; /* Hkv = k.N / 128; Hq = q.N / 128; Hq / Hkv in {1, 2, 4, 8} */
+  int attn_t_stride;             /* rows per head in each cache */
+  int attn_pos;                  /* position of the first vector (rows 0 .. attn_pos - 1 are filled);
+                                    nt_decode_plan_set_position changes it between steps */
+  float rope_base;               /* <= 0 selects 10000 */
+  float norm_eps;                /* <= 0 selects 1e-6 */
+  const float* const* norm_attn; /* host array [n_layers] of device [d] weights, or NULL */
+  const float* const* norm_ffn;  /* host array [n_layers] of device [d] weights, or NULL */
+  const float* norm_final;       /* device [d] weights, or NULL */
 } nt_decode_desc;
 
 typedef struct nt_decode_plan nt_decode_plan;
@@ -360,6 +380,11 @@ nt_status nt_decode_step(nt_decode_plan* plan, void* stream);
  * bounded wait inside the persistent kernel ran out (the step's outputs are then invalid
  * and the plan must be reset before reuse). Reads 4 bytes from the device (synchronous). */
 nt_status nt_decode_step_status(nt_decode_plan* plan, nt_status* device_status);
+
+/* Chained plans with attention: the position of the next step's first vector, set in stream
+ * order on `stream` (one tiny kernel; graph launchers read it at run time). pos + batch must
+ * not exceed attn_t_stride. */
+nt_status nt_decode_plan_set_position(nt_decode_plan* plan, int pos, void* stream);
 
 /* Clears the plan's device-side error word and barrier counters (synchronous). */
 nt_status nt_decode_plan_reset(nt_decode_plan* plan);

@@ -28,6 +28,7 @@ struct AttnArgs {
   float* out;          // [B][Hq][D]
   int B, Hq, Hkv, T, ts, nch, span;  // span: positions per unit (a multiple of kAttnSub)
   float scale_log2;    // log2(e) / sqrt(D)
+  const int* T_dev;    // when set, the cache length is *T_dev (T then only sized the grid)
 };
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -64,7 +65,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_unit_kernel(const AttnArgs 
   __shared__ float Wm[G][kAttnMaxSplit];
   __shared__ int s_last;
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x, lane = i & 31, w = i >> 5;
-  const int u0 = c * a.span, u1 = min(a.T, u0 + a.span);
+  const int T = a.T_dev ? *a.T_dev : a.T;
+  const int u0 = c * a.span, u1 = min(T, u0 + a.span);
   const uint16_t* kh = a.kc + (int64_t)h * a.ts * kAttnD;
   const uint32_t* vh = reinterpret_cast<const uint32_t*>(a.vc + (int64_t)h * a.ts * kAttnD);
   const int64_t head_stride = (int64_t)a.nch * kPartRow;
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_unit_kernel(const AttnArgs 
   const int dp = i & 63, vh2 = i >> 6;    // value role: dims 2dp, 2dp+1, positions 32*vh2 ..
 
   for (int b = 0; b < a.B; ++b) {
-    const int vis = min(u1, a.T - a.B + b + 1);  // positions [u0, vis) are visible to b
+    const int vis = min(u1, T - a.B + b + 1);  // positions [u0, vis) are visible to b
     const float* qg = a.q + ((int64_t)b * a.Hq + h * G) * kAttnD;
     for (int e = i; e < G * kAttnD; e += kAttnThreads) Qs[e / kAttnD][e % kAttnD] = __fmul_rn(qg[e], a.scale_log2);
     float mrun[G], lrun[G], acc[G][2];
@@ -250,10 +252,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_unit_kernel(const AttnArgs 
 // about pos * 2^-24 radians), the rotations in fp32 without contraction. Keys and values go
 // to the cache rows pos0 + b as bf16 (round to nearest even); queries to q_out in fp32.
 __global__ void rope_append_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                                   const float* __restrict__ v, int Hq, int Hkv, int pos0, double log2_base,
+                                   const float* __restrict__ v, int Hq, int Hkv, int pos0_arg, const int* pos_dev,
+                                   double log2_base,
                                    float* __restrict__ q_out, uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
                                    int ts) {
   __shared__ float cs[kAttnD / 2], sn[kAttnD / 2];
+  const int pos0 = pos_dev ? *pos_dev : pos0_arg;
   const int b = blockIdx.x, pos = pos0 + b;
   constexpr int half = kAttnD / 2;
   if (threadIdx.x < half) {
@@ -334,11 +338,11 @@ size_t attention_ws_bytes(int B, int Hq, int Hkv, int T) {
 }
 
 nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* vc, int B, int Hq, int Hkv, int T,
-                           int ts, float* out, void* ws, cudaStream_t st) {
+                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev) {
   float* part = static_cast<float*>(ws);
   unsigned int* done = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + attn_part_bytes(B, Hq, Hkv, T));
   AttnArgs a{q, kc, vc, part, done, out, B, Hq, Hkv, T, ts, attn_units(T, Hkv), attn_span(T, Hkv),
-             (float)(1.4426950408889634 / sqrt((double)kAttnD))};
+             (float)(1.4426950408889634 / sqrt((double)kAttnD)), T_dev};
   switch (Hq / Hkv) {
     case 1: return launch_attn_units<1>(a, st);
     case 2: return launch_attn_units<2>(a, st);
@@ -348,8 +352,9 @@ nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* v
 }
 
 nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
-                             float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st) {
-  rope_append_kernel<<<B, 256, 0, st>>>(q, k, v, Hq, Hkv, pos0, log2((double)base), q_out, kc, vc, ts);
+                             float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st,
+                             const int* pos_dev) {
+  rope_append_kernel<<<B, 256, 0, st>>>(q, k, v, Hq, Hkv, pos0, pos_dev, log2((double)base), q_out, kc, vc, ts);
   return check_launch("rope_append_kernel");
 }
 

@@ -82,14 +82,37 @@ __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob*
 // thread rewrites only the elements it read), then the codes to every recorded q.
 __global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
   __shared__ float red[kWarps];
+  __shared__ double redd[kWarps];
   const ChainJob j = *jobs;
   const int b = blockIdx.x, K = j.src.K;
   float* vb = j.vbuf + (int64_t)b * K;
   float m = 0.0f;
+  double ss = 0.0;
   for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
     const float4 v = chain_load4(j.src, b, k);
     *reinterpret_cast<float4*>(vb + k) = v;
     m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+  }
+  float r = 1.0f;
+  if (j.src.gamma) {  // RMS normalisation: the absmax is taken over the normalised values
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    double t = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) t += redd[i];
+    r = (float)(1.0 / sqrt(t / K + (double)j.src.eps));
+    m = 0.0f;
+    for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+      const float4 v = *reinterpret_cast<const float4*>(vb + k);
+      const float4 g = *reinterpret_cast<const float4*>(j.src.gamma + k);
+      m = fmaxf(m, fabsf(__fmul_rn(__fmul_rn(v.x, r), g.x)));
+      m = fmaxf(m, fabsf(__fmul_rn(__fmul_rn(v.y, r), g.y)));
+      m = fmaxf(m, fabsf(__fmul_rn(__fmul_rn(v.z, r), g.z)));
+      m = fmaxf(m, fabsf(__fmul_rn(__fmul_rn(v.w, r), g.w)));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -101,10 +124,16 @@ __global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* _
   const bool nz = m != 0.0f;
   const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
   if (threadIdx.x == 0)
-    for (int r = 0; r < j.n_rec; ++r) j.s[r][b] = s;
+    for (int rr = 0; rr < j.n_rec; ++rr) j.s[rr][b] = s;
   for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
-    const uint32_t c = quant4(*reinterpret_cast<const float4*>(vb + k), s, nz);
-    for (int r = 0; r < j.n_rec; ++r) *reinterpret_cast<uint32_t*>(j.q[r] + (int64_t)b * K + k) = c;
+    float4 v = *reinterpret_cast<const float4*>(vb + k);
+    if (j.src.gamma) {
+      const float4 g = *reinterpret_cast<const float4*>(j.src.gamma + k);
+      v = make_float4(__fmul_rn(__fmul_rn(v.x, r), g.x), __fmul_rn(__fmul_rn(v.y, r), g.y),
+                      __fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
+    }
+    const uint32_t c = quant4(v, s, nz);
+    for (int rr = 0; rr < j.n_rec; ++rr) *reinterpret_cast<uint32_t*>(j.q[rr] + (int64_t)b * K + k) = c;
   }
 }
 

@@ -19,11 +19,18 @@ struct QuantJob {
 //                  query head i takes value head i / grp (in0 has K / grp columns)
 //   kChainProduct  fl(in0[b][k] * in1[b][k])
 //   kChainSum      fl(in0[b][k] + in1[b][k])
-enum : int { kChainNone = 0, kChainDirect = 1, kChainHeads = 2, kChainProduct = 3, kChainSum = 4 };
+//   kChainSiluProduct fl(silu(in0[b][k]) * in1[b][k]), silu(x) = x / (1 + exp(-x)) in fp32
+// With gamma set (stream / graph launchers), the quantized vector is the RMS-normalised
+// fl(fl(v * r) * gamma[k]), r = fl32(1 / sqrt(mean(v^2) + eps)) formed in double.
+enum : int { kChainNone = 0, kChainDirect = 1, kChainHeads = 2, kChainProduct = 3, kChainSum = 4,
+             kChainSiluProduct = 5 };
 struct ChainSrc {
   const float* in0;
   const float* in1;
   int kind, K, grp, hd;
+  const float* gamma;
+  float eps;
+  int pad_;
 };
 
 // One ternary projection in the tiled layout, B activation vectors.
@@ -96,10 +103,13 @@ nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int3
 // The workspace's counters (after the partial results) must be zero before the first call;
 // every call leaves them zero.
 size_t attention_ws_bytes(int B, int Hq, int Hkv, int T);
+// T_dev / pos_dev (optional): the cache length / first new position read from device memory
+// when the kernel runs (a plan's position); T then only sizes the grid.
 nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* vc, int B, int Hq, int Hkv, int T,
-                           int ts, float* out, void* ws, cudaStream_t st);
+                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev = nullptr);
 nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
-                             float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st);
+                             float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st,
+                             const int* pos_dev = nullptr);
 nt_status launch_rmsnorm(const float* x, const float* gamma, int B, int D, float eps, float* y, cudaStream_t st);
 
 // Tensor-core ternary GEMM (tcgen05, bf16 operands, exact fp32 accumulation) for
@@ -124,6 +134,11 @@ __device__ __forceinline__ float4 chain_load4(const ChainSrc& c, int b, int k) {
   const float4 d = __ldcg(reinterpret_cast<const float4*>(c.in1 + (int64_t)b * c.K + k));
   if (c.kind == kChainProduct)
     return make_float4(__fmul_rn(a.x, d.x), __fmul_rn(a.y, d.y), __fmul_rn(a.z, d.z), __fmul_rn(a.w, d.w));
+  if (c.kind == kChainSiluProduct) {
+    auto silu = [](float x) { return __fdiv_rn(x, __fadd_rn(1.0f, expf(-x))); };
+    return make_float4(__fmul_rn(silu(a.x), d.x), __fmul_rn(silu(a.y), d.y), __fmul_rn(silu(a.z), d.z),
+                       __fmul_rn(silu(a.w), d.w));
+  }
   return make_float4(__fadd_rn(a.x, d.x), __fadd_rn(a.y, d.y), __fadd_rn(a.z, d.z), __fadd_rn(a.w, d.w));
 }
 

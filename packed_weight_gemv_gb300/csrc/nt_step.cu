@@ -42,7 +42,37 @@ nt_status validate_chain(const nt_decode_desc* d) {
   }
   if (!aligned(d->proj[0].x, 16)) return set_error(NT_ERR_ALIGNMENT, "chained: proj[0].x must be 16-byte aligned");
   if (d->head_T && d->head_K != dm) return set_error(NT_ERR_INVALID_ARG, "chained: head_K must equal proj[0].K");
+  if (d->attn_k_cache) {  // the attention side
+    if (d->launcher == NT_LAUNCH_PERSISTENT)
+      return set_error(NT_ERR_UNSUPPORTED, "chained steps with attention run on the stream or graph launcher");
+    if (hd != 128) return set_error(NT_ERR_UNSUPPORTED, "chained steps with attention need head_dim 128");
+    const int Hq = d->proj[0].N / 128, Hkv = d->proj[1].N / 128;
+    if (d->proj[0].N % 128 || d->proj[1].N % 128 || Hkv < 1 || Hq % Hkv != 0)
+      return set_error(NT_ERR_INVALID_ARG, "attention: q.N and k.N must be multiples of 128 with Hq a multiple of Hkv");
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return set_error(NT_ERR_UNSUPPORTED, "attention: Hq / Hkv must be 1, 2, 4 or 8");
+    if (!d->attn_v_cache) return set_error(NT_ERR_INVALID_ARG, "attention: attn_v_cache is NULL");
+    if (d->attn_pos < 0 || d->attn_pos + d->batch > d->attn_t_stride)
+      return set_error(NT_ERR_INVALID_ARG, "attention: need 0 <= attn_pos and attn_pos + batch <= attn_t_stride");
+    for (int l = 0; l < d->n_layers; ++l) {
+      if (d->proj[l * kProjPerLayer].N != Hq * 128 || d->proj[l * kProjPerLayer + 1].N != Hkv * 128)
+        return set_error(NT_ERR_INVALID_ARG, "attention: every layer needs the same head counts");
+      if (!d->attn_k_cache[l] || !d->attn_v_cache[l]) return set_error(NT_ERR_INVALID_ARG, "attention: NULL cache");
+      if (!aligned(d->attn_k_cache[l], 16) || !aligned(d->attn_v_cache[l], 16))
+        return set_error(NT_ERR_ALIGNMENT, "attention: caches must be 16-byte aligned");
+      if ((d->norm_attn && (!d->norm_attn[l] || !aligned(d->norm_attn[l], 16))) ||
+          (d->norm_ffn && (!d->norm_ffn[l] || !aligned(d->norm_ffn[l], 16))))
+        return set_error(NT_ERR_INVALID_ARG, "attention: normalisation weights NULL or not 16-byte aligned");
+    }
+    if (d->norm_final && !aligned(d->norm_final, 16))
+      return set_error(NT_ERR_ALIGNMENT, "attention: norm_final must be 16-byte aligned");
+  }
   return NT_OK;
+}
+
+__global__ void set_position_kernel(int* pos, int p, int B) {
+  pos[0] = p;
+  pos[1] = p + B;
 }
 
 nt_status validate_desc(const nt_decode_desc* d) {
@@ -95,6 +125,14 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
   const bool chained = p->mode == NT_STEP_CHAINED;
   for (size_t i = 0; i < p->stages.size(); ++i) {
     const PlanStage& s = p->stages[i];
+    if (p->attn && i % 4 == 1) {  // after q, k, v: rotate, append, attend
+      const int l = (int)(i / 4);
+      const MatDesc* m = p->mats.data() + l * kProjPerLayer;
+      NT_TRY(launch_rope_append(m[0].y, m[1].y, m[2].y, p->B, p->Hq, p->Hkv, 0, p->rope_base, p->d_qrot,
+                                p->k_cache[l], p->v_cache[l], p->t_stride, st, p->d_pos));
+      NT_TRY(launch_attention(p->d_qrot, p->k_cache[l], p->v_cache[l], p->B, p->Hq, p->Hkv, p->t_stride, p->t_stride,
+                              p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1));
+    }
     if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st));
     NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
                                    s.total_tiles, p->B, st));
@@ -120,6 +158,10 @@ void free_plan(nt_decode_plan* p) {
   cudaFree(p->d_resid);
   cudaFree(p->d_chain_tmp);
   cudaFree(p->d_cjobs);
+  cudaFree(p->d_pos);
+  cudaFree(p->d_qrot);
+  cudaFree(p->d_attn_out);
+  cudaFree(p->d_attn_ws);
   delete p;
 }
 
@@ -245,6 +287,31 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
       }
       cjobs.push_back(j);
     };
+    p->attn = d->attn_k_cache != nullptr;
+    if (p->attn) {
+      p->Hq = d->proj[0].N / 128;
+      p->Hkv = d->proj[1].N / 128;
+      p->t_stride = d->attn_t_stride;
+      p->rope_base = d->rope_base > 0 ? d->rope_base : 10000.0f;
+      p->k_cache.assign(d->attn_k_cache, d->attn_k_cache + d->n_layers);
+      p->v_cache.assign(d->attn_v_cache, d->attn_v_cache + d->n_layers);
+      p->attn_ws_bytes = attention_ws_bytes(B, p->Hq, p->Hkv, p->t_stride);
+      const size_t qb = sizeof(float) * (size_t)B * p->Hq * 128;
+      if ((e = cudaMalloc(&p->d_pos, 2 * sizeof(int))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&p->d_qrot, qb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&p->d_attn_out, qb)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+      if ((e = cudaMalloc(&p->d_attn_ws, p->attn_ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+      if ((e = cudaMemset(p->d_attn_ws, 0, p->attn_ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+      const int pos[2] = {d->attn_pos, d->attn_pos + B};
+      if ((e = cudaMemcpy(p->d_pos, pos, sizeof pos, cudaMemcpyHostToDevice)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy");
+    }
+    const float eps = d->norm_eps > 0 ? d->norm_eps : 1e-6f;
+    auto normed = [&](ChainSrc src, const float* gamma) {
+      src.gamma = gamma;
+      src.eps = eps;
+      return src;
+    };
     for (int l = 0; l < d->n_layers; ++l) {
       const int b = l * kProjPerLayer;
       MatDesc* m = mats.data() + b;
@@ -265,6 +332,16 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
           mats[recf[g] + i].rec_count = recn[g];
         }
       // stream / graph launchers: the residual additions happen in the stage-input jobs
+      if (p->attn) {
+        const float* ga = d->norm_attn ? d->norm_attn[l] : nullptr;
+        const float* gf = d->norm_ffn ? d->norm_ffn[l] : nullptr;
+        if (l == 0) job(normed(ChainSrc{x0, nullptr, kChainDirect, dm, 1, hd}, ga), R, b, 3);
+        else job(normed(ChainSrc{R, mats[b - 1].y, kChainSum, dm, 1, hd}, ga), R, b, 3);
+        job(ChainSrc{p->d_attn_out, nullptr, kChainDirect, m[3].K, 1, hd}, p->d_chain_tmp, b + 3, 1);
+        job(normed(ChainSrc{R, m[3].y, kChainSum, dm, 1, hd}, gf), R, b + 4, 2);
+        job(ChainSrc{m[4].y, m[5].y, kChainSiluProduct, m[6].K, 1, hd}, p->d_chain_tmp, b + 6, 1);
+        continue;
+      }
       if (l == 0) job(ChainSrc{x0, nullptr, kChainDirect, dm, 1, hd}, p->d_chain_tmp, b, 3);
       else job(ChainSrc{R, mats[b - 1].y, kChainSum, dm, 1, hd}, R, b, 3);
       job(m[3].src, p->d_chain_tmp, b + 3, 1);
@@ -275,6 +352,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     if (p->has_head) {
       ChainJob j{};
       j.src = ChainSrc{R, mats[n_proj - 1].y, kChainSum, dm, 1, hd};
+      if (p->attn) j.src = normed(j.src, d->norm_final);
       j.vbuf = R;
       j.n_rec = 1;
       j.q[0] = const_cast<int8_t*>(p->head_q);
@@ -341,6 +419,15 @@ nt_status nt_decode_step(nt_decode_plan* p, void* stream) {
     default:
       return persist_launch(p, st);
   }
+}
+
+nt_status nt_decode_plan_set_position(nt_decode_plan* p, int pos, void* stream) {
+  clear_error();
+  if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
+  if (!p->attn) return set_error(NT_ERR_INVALID_ARG, "the plan has no attention side");
+  if (pos < 0 || pos + p->B > p->t_stride) return set_error(NT_ERR_INVALID_ARG, "need 0 <= pos and pos + batch <= attn_t_stride");
+  set_position_kernel<<<1, 1, 0, as_stream(stream)>>>(p->d_pos, pos, p->B);
+  return check_launch("set_position_kernel");
 }
 
 nt_status nt_decode_step_status(nt_decode_plan* p, nt_status* device_status) {

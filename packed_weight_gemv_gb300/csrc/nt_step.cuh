@@ -87,6 +87,16 @@ struct nt_decode_plan {
   float* d_chain_tmp = nullptr;     // [B][max K] stage inputs of the stream / graph launchers
   nt::ChainJob* d_cjobs = nullptr;  // one per stage, then one for the output projection
   int n_cjobs = 0;
+  // chained steps with the attention side
+  bool attn = false;
+  int Hq = 0, Hkv = 0, t_stride = 0;
+  float rope_base = 10000.0f;
+  std::vector<uint16_t*> k_cache, v_cache;  // per layer
+  int* d_pos = nullptr;             // {position of the first vector, cache length after the append}
+  float* d_qrot = nullptr;          // [B][Hq * 128] rotated queries
+  float* d_attn_out = nullptr;      // [B][Hq * 128] attention output
+  void* d_attn_ws = nullptr;        // attention workspace (counters zero)
+  size_t attn_ws_bytes = 0;
 };
 
 namespace nt {

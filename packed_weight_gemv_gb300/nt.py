@@ -42,6 +42,7 @@ EXPORTS = (
     "nt_int8_logits_argmax_noalloc", "nt_embed_rows", "nt_verify_accept",
     "nt_attention_workspace_size", "nt_attention_decode", "nt_rope_append", "nt_rmsnorm",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
+    "nt_decode_plan_set_position",
     "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_destroy",
 )
 
@@ -72,7 +73,12 @@ class nt_decode_desc(ctypes.Structure):
                 ("embed_V", ctypes.c_int), ("embed_K", ctypes.c_int),
                 ("tokens", ctypes.c_void_p), ("embed_x", ctypes.c_void_p),
                 ("verify_draft", ctypes.c_void_p), ("verify_emit", ctypes.c_void_p),
-                ("verify_n", ctypes.c_void_p), ("head_dim", ctypes.c_int)]
+                ("verify_n", ctypes.c_void_p), ("head_dim", ctypes.c_int),
+                ("attn_k_cache", ctypes.POINTER(ctypes.c_void_p)), ("attn_v_cache", ctypes.POINTER(ctypes.c_void_p)),
+                ("attn_t_stride", ctypes.c_int), ("attn_pos", ctypes.c_int),
+                ("rope_base", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("norm_attn", ctypes.POINTER(ctypes.c_void_p)), ("norm_ffn", ctypes.POINTER(ctypes.c_void_p)),
+                ("norm_final", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -114,6 +120,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_decode_step": ([vp, vp], i),
             "nt_decode_step_status": ([vp, ctypes.POINTER(i)], i),
             "nt_decode_plan_reset": ([vp], i),
+            "nt_decode_plan_set_position": ([vp, i, vp], i),
             "nt_decode_plan_trace_layout": ([vp, ctypes.POINTER(i), ctypes.POINTER(i)], i),
             "nt_decode_plan_set_trace": ([vp, vp], i),
             "nt_decode_plan_destroy": ([vp], None),
@@ -274,9 +281,9 @@ class DecodePlan:
     def __init__(self, n_layers: int, batch: int, projs: Sequence[dict], head: Optional[dict],
                  mode: int = NT_STEP_INDEPENDENT, launcher: int = NT_LAUNCH_PERSISTENT,
                  timeout_ms: float = 0.0, test_fault: int = 0, embed: Optional[dict] = None,
-                 verify: Optional[dict] = None, head_dim: int = 0):
+                 verify: Optional[dict] = None, head_dim: int = 0, attention: Optional[dict] = None):
         lib = load_library()
-        self._keep = [projs, head, embed, verify]
+        self._keep = [projs, head, embed, verify, attention]
         arr = (nt_proj * len(projs))()
         for i, p in enumerate(projs):
             arr[i] = nt_proj(p["N"], p["K"], p["w"].data_ptr(), p["s_w"].data_ptr(),
@@ -293,6 +300,25 @@ class DecodePlan:
             d.head_argmax = head["argmax"].data_ptr()
         d.mode, d.launcher, d.timeout_ms, d.test_fault = mode, launcher, timeout_ms, test_fault
         d.head_dim = head_dim
+        if attention is not None:
+            # dict: k_cache, v_cache (lists of device tensors per layer), t_stride, pos, and
+            # optionally rope_base, eps, norm_attn / norm_ffn (lists), norm_final
+            L = n_layers
+            ptrs = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+            self._kc, self._vc = ptrs(attention["k_cache"]), ptrs(attention["v_cache"])
+            d.attn_k_cache = ctypes.cast(self._kc, ctypes.POINTER(ctypes.c_void_p))
+            d.attn_v_cache = ctypes.cast(self._vc, ctypes.POINTER(ctypes.c_void_p))
+            d.attn_t_stride, d.attn_pos = attention["t_stride"], attention["pos"]
+            d.rope_base = attention.get("rope_base", 0.0)
+            d.norm_eps = attention.get("eps", 0.0)
+            if attention.get("norm_attn") is not None:
+                self._na = ptrs(attention["norm_attn"])
+                d.norm_attn = ctypes.cast(self._na, ctypes.POINTER(ctypes.c_void_p))
+            if attention.get("norm_ffn") is not None:
+                self._nf = ptrs(attention["norm_ffn"])
+                d.norm_ffn = ctypes.cast(self._nf, ctypes.POINTER(ctypes.c_void_p))
+            if attention.get("norm_final") is not None:
+                d.norm_final = attention["norm_final"].data_ptr()
         if embed is not None:
             d.embed_T, d.embed_s = embed["T"].data_ptr(), embed["s"].data_ptr()
             d.embed_V, d.embed_K = embed["V"], embed["K"]
@@ -308,6 +334,10 @@ class DecodePlan:
 
     def nt_decode_step(self, stream=None):
         _check(load_library().nt_decode_step(self._h, _stream(stream)), "nt_decode_step")
+
+    def nt_decode_plan_set_position(self, pos: int, stream=None):
+        _check(load_library().nt_decode_plan_set_position(self._h, pos, _stream(stream)),
+               "nt_decode_plan_set_position")
 
     def nt_decode_step_status(self) -> int:
         s = ctypes.c_int(0)
