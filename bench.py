@@ -589,7 +589,7 @@ def run_attention(args):
     L, Hq, Hkv, D = args.layers, 32, 8, 128
     peak, peak_kind = measured_peak()
     stream = torch.cuda.current_stream()
-    for T in (4096, 16384, 32768):
+    for T in (args.contexts or (4096, 16384, 32768)):
         # one cache per layer, bf16 N(0,1) keys and values (the layers' contents differ only by
         # seed; the attention's cost does not depend on the values)
         kb = wl.bf16_normal(Hkv * T * D, 0, wl.tag(wl.WL_ATTN, T, 1, 0))
@@ -740,7 +740,7 @@ def run_prefill(args):
     except (OSError, KeyError, ValueError):
         pass
     stream = torch.cuda.current_stream()
-    for M in wl.PREFILL_TOKENS:
+    for M in (args.tokens or wl.PREFILL_TOKENS):
         # One fp32 input per distinct K (shared by the layers: values do not change the work),
         # quantized per token inside the timed pass, then every projection's GEMM.
         xs = {K: torch.from_numpy(wl.normal(M * K, 0, wl.tag(wl.WL_PREFILL, 99, K, wl.ROLE_X))
@@ -825,6 +825,10 @@ def main():
                     help="attention over the key-value cache at 4K/16K/32K context (36 layers)")
     ap.add_argument("--layer-attention", action="store_true",
                     help="chained decode with norms, rotary embedding and attention at 4K/16K context")
+    ap.add_argument("--tokens", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="--prefill: token counts to run (default 2048,8192)")
+    ap.add_argument("--contexts", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="--attention: context lengths to run (default 4096,16384,32768)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()

@@ -14,8 +14,8 @@
 // A call runs three kernels:
 //   1. int8 activations -> bf16 [M][K] and 2. tiled trits -> bf16 [N][K], both into the
 //      caller's workspace (operands for this call only; nothing is kept across calls);
-//   3. a persistent GEMM, one CTA per SM, looping over tiles of 128 weight rows (MMA M) x 256
-//      tokens (MMA N):
+//   3. a persistent GEMM, one CTA per SM, looping over tiles of 128 weight rows (MMA M) x TN
+//      tokens (MMA N; TN <= 256 picked per call so the tiles fill whole waves of SMs):
 //        warp 8 lane 0: 2-D TMA loads (128-byte swizzle) of both operands of each 64-wide K
 //          step into a 4-stage ring (full/empty mbarriers);
 //        warp 9: allocates 512 tensor-memory columns (two 256-column accumulators); lane 0
@@ -39,8 +39,8 @@
 namespace nt {
 namespace {
 
-constexpr int kBM = 128;             // tokens per tile (MMA M)
-constexpr int kBN = 256;             // weight rows per tile (MMA N)
+constexpr int kBM = 128;             // weight rows per tile (MMA M)
+constexpr int kBN = 256;             // largest token tile (MMA N); a call picks TN <= kBN
 constexpr int kBK = 64;              // K per stage: one 128-byte row of bf16
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KB
@@ -105,15 +105,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
+// Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major, M = 128, N = tn.
+__host__ __device__ constexpr uint32_t idesc_for(int tn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -177,7 +179,8 @@ struct TcParams {
   float* y;          // [M][N]
   int32_t* acc;      // [M][N] or null
   int M, N, K;
-  int tiles_n, tiles_m;  // 128-row weight tiles, 256-token tiles
+  int tiles_n, tiles_m;  // 128-row weight tiles, tn-token tiles
+  int tn;                // tokens per tile (MMA N): a multiple of 32, <= kBN
 };
 
 __device__ __forceinline__ void epi_sync() {
@@ -198,6 +201,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int n_tiles = p.tiles_n * p.tiles_m;
   const int ksteps = (p.K + kBK - 1) / kBK;
+  const int TN = p.tn;
   constexpr int kProducerWarp = kEpiThreads / 32, kMmaWarp = kProducerWarp + 1;
 
   if (t == 0) {
@@ -233,9 +237,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t s = it % kStages;
         if (it >= kStages && !mbar_wait(empty0 + 8 * s, ((it / kStages) - 1) & 1u, fail)) break;
         const uint32_t a = smem_u32(smem + s * kStageBytes);
-        mbar_expect_tx(full0 + 8 * s, kStageBytes);
+        mbar_expect_tx(full0 + 8 * s, kABytes + TN * kBK * 2);
         tma_load_2d(a, &tmW, ks * kBK, tn * kBM, full0 + 8 * s);
-        tma_load_2d(a + kABytes, &tmX, ks * kBK, tm * kBN, full0 + 8 * s);
+        tma_load_2d(a + kABytes, &tmX, ks * kBK, tm * TN, full0 + 8 * s);
       }
     }
     // Drain: the last copy issued into each stage must land before the CTA may exit.
@@ -248,6 +252,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == kMmaWarp && lane == 0) {
     // ---- MMA issuer ----
     uint32_t it = 0, j = 0;
+    const uint32_t idesc = idesc_for(TN);
     for (int tile = blockIdx.x; tile < n_tiles && !*fail; tile += gridDim.x, ++j) {
       const uint32_t buf = j & 1u;
       if (j >= 2 && !mbar_wait(tempty0 + 8 * buf, ((j >> 1) - 1) & 1u, fail)) break;
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t a = smem_u32(smem + s * kStageBytes), b = a + kABytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(b + kk * 32), (ks | kk) != 0);
+          mma_bf16(d, sdesc_sw128(a + kk * 32), sdesc_sw128(b + kk * 32), idesc, (ks | kk) != 0);
         mma_commit(empty0 + 8 * s);  // the stage is free once these MMAs have read it
       }
       if (!ok) break;
@@ -279,17 +284,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
       const uint32_t buf = j & 1u;
       const int tn = tile % p.tiles_n, tm = tile / p.tiles_n;
-      const int n = tn * kBM + quarter * 32 + lane, m0 = tm * kBN;
-      sxs[buf * kBN + t] = (m0 + t < p.M) ? __ldg(p.s_x + m0 + t) : 0.0f;
+      const int n = tn * kBM + quarter * 32 + lane, m0 = tm * TN;
+      sxs[buf * kBN + t] = (t < TN && m0 + t < p.M) ? __ldg(p.s_x + m0 + t) : 0.0f;
       const float sw = (n < p.N) ? __ldg(p.s_w + n) : 0.0f;
       epi_sync();  // token scales of this tile visible to every epilogue thread
       // After a failed wait the thread keeps walking the tiles (the named barrier above needs
       // every epilogue thread) and only skips the stores.
       const bool ok = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1u, fail);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t base = tmem + buf * kBN + half * (kBN / 2) + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t base = tmem + buf * kBN + half * (TN / 2) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN / 2; c0 += 16) {
+      for (int c0 = 0; c0 < TN / 2; c0 += 16) {
         uint32_t r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15;
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -299,14 +304,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             : "memory");
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         const uint32_t r[16] = {r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15};
-        const int mc = m0 + half * (kBN / 2) + c0;
+        const int mc = m0 + half * (TN / 2) + c0;
         if (ok && n < p.N) {
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int m = mc + q;
             if (m < p.M) {
               const float a = __int_as_float((int)r[q]);  // an exact integer
-              p.y[(int64_t)m * p.N + n] = __fmul_rn(__fmul_rn(a, sw), sxs[buf * kBN + half * (kBN / 2) + c0 + q]);
+              p.y[(int64_t)m * p.N + n] = __fmul_rn(__fmul_rn(a, sw), sxs[buf * kBN + half * (TN / 2) + c0 + q]);
               if (p.acc) p.acc[(int64_t)m * p.N + n] = __float2int_rn(a);
             }
           }
@@ -358,6 +363,25 @@ nt_status encode_map(CUtensorMap* map, const void* base, int rows, int K, int bo
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
+// Tokens per tile: the multiple of 32 (<= 256) that minimises (waves of tiles over the SMs) x
+// (tile width + a fixed per-tile cost of about 48 columns), so the last wave is not left
+// mostly empty (e.g. 8192 tokens x 3072 rows: 256-token tiles make 5.05 waves, 224 make 5.8).
+int pick_token_tile(int M, int N, int sms) {
+  const int64_t tiles_n = (N + kBM - 1) / kBM;
+  int best = kBN;
+  int64_t best_cost = INT64_MAX;
+  for (int tn = kBN; tn >= 32; tn -= 32) {
+    const int64_t tiles = tiles_n * ((M + tn - 1) / tn);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const int64_t cost = waves * (tn + 48);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = tn;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 bool tc_gemm_supported(int M, int K) { return M >= kTcMinBatch && K <= 131072; }
@@ -386,10 +410,11 @@ nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const
     trits_bf16_kernel<<<g, 256, 0, st>>>(w, N, K, b_bf16);
     NT_TRY(check_launch("trits_bf16_kernel"));
   }
+  const int tn = pick_token_tile(M, N, sms);
   CUtensorMap mw, mx;
   NT_TRY(encode_map(&mw, b_bf16, N, K, kBM));  // weights: MMA M side, 128-row boxes
-  NT_TRY(encode_map(&mx, a_bf16, M, K, kBN));  // tokens: MMA N side, 256-row boxes
-  TcParams p{s_w, s_x, y, acc, M, N, K, (N + kBM - 1) / kBM, (M + kBN - 1) / kBN};
+  NT_TRY(encode_map(&mx, a_bf16, M, K, tn));   // tokens: MMA N side, tn-row boxes
+  TcParams p{s_w, s_x, y, acc, M, N, K, (N + kBM - 1) / kBM, (M + tn - 1) / tn, tn};
   const int tiles = p.tiles_m * p.tiles_n;
   gemm_tc_kernel<<<std::min(tiles, sms), kThreadsTc, kSmemTc, st>>>(mw, mx, p);
   return check_launch("gemm_tc_kernel");

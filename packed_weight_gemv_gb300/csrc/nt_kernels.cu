@@ -18,6 +18,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kChainThreads = 256;  // stage-input kernel: one CTA per vector
+constexpr int kChainWarps = kChainThreads / 32;
 
 // 16-byte streaming load that bypasses L1 allocation (weights are read once per token).
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -80,15 +82,15 @@ __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob*
 // Chained stage input of vector blockIdx.x (stream / graph launchers): the fp32 values go to
 // job.vbuf with the absmax (for kChainSum vbuf is the residual stream, updated in place: each
 // thread rewrites only the elements it read), then the codes to every recorded q.
-__global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
-  __shared__ float red[kWarps];
-  __shared__ double redd[kWarps];
+__global__ void __launch_bounds__(kChainThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
+  __shared__ float red[kChainWarps];
+  __shared__ double redd[kChainWarps];
   const ChainJob j = *jobs;
   const int b = blockIdx.x, K = j.src.K;
   float* vb = j.vbuf + (int64_t)b * K;
   float m = 0.0f;
   double ss = 0.0;
-  for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+  for (int k = 4 * threadIdx.x; k < K; k += 4 * kChainThreads) {
     const float4 v = chain_load4(j.src, b, k);
     *reinterpret_cast<float4*>(vb + k) = v;
     m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -102,10 +104,10 @@ __global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* _
     __syncthreads();
     double t = 0.0;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) t += redd[i];
+    for (int i = 0; i < kChainWarps; ++i) t += redd[i];
     r = (float)(1.0 / sqrt(t / K + (double)j.src.eps));
     m = 0.0f;
-    for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+    for (int k = 4 * threadIdx.x; k < K; k += 4 * kChainThreads) {
       const float4 v = *reinterpret_cast<const float4*>(vb + k);
       const float4 g = *reinterpret_cast<const float4*>(j.src.gamma + k);
       m = fmaxf(m, fabsf(__fmul_rn(__fmul_rn(v.x, r), g.x)));
@@ -120,12 +122,12 @@ __global__ void __launch_bounds__(kThreads) chain_quant_kernel(const ChainJob* _
   __syncthreads();
   m = red[0];
 #pragma unroll
-  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
+  for (int i = 1; i < kChainWarps; ++i) m = fmaxf(m, red[i]);
   const bool nz = m != 0.0f;
   const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
   if (threadIdx.x == 0)
     for (int rr = 0; rr < j.n_rec; ++rr) j.s[rr][b] = s;
-  for (int k = 4 * threadIdx.x; k < K; k += 4 * kThreads) {
+  for (int k = 4 * threadIdx.x; k < K; k += 4 * kChainThreads) {
     float4 v = *reinterpret_cast<const float4*>(vb + k);
     if (j.src.gamma) {
       const float4 g = *reinterpret_cast<const float4*>(j.src.gamma + k);
@@ -410,7 +412,7 @@ nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cu
 }
 
 nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st) {
-  chain_quant_kernel<<<B, kThreads, 0, st>>>(d_job);
+  chain_quant_kernel<<<B, kChainThreads, 0, st>>>(d_job);
   return check_launch("chain_quant_kernel");
 }
 
