@@ -444,7 +444,7 @@ __device__ void grid_barrier(const PersistParams& P, uint32_t target, int b, vol
   consumer_sync<C>();
   stamp(P, b, 0);
   if (threadIdx.x == 0 && !*s_abort) {
-    __threadfence();
+    // the consumer barrier above orders every thread's writes before this release (cumulative)
     red_release_add(&P.ctrl->arrive, 1u);
     const uint64_t deadline = globaltimer_ns() + P.timeout_ns;
     for (uint32_t it = 0;; ++it) {
@@ -720,14 +720,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       consumer_sync<C>();  // act[buf] complete; every warp is past the previous item
       if (staged) stamp(P, (int)barriers, 2);
       prefetched = false;
-      if (i + 1 < n_items) {
+      if (i + 1 < n_items) {  // supplied inputs were quantized before any stage: prefetch across barriers too
         const WorkItem nx = get_item(P, i + 1);
-        if (!(nx.flags & kFlagStage)) {
-          int K2, nb2;
-          const int8_t* q2 = item_act(P, nx, K2, nb2);
-          load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
-          prefetched = true;
-        }
+        int K2, nb2;
+        const int8_t* q2 = item_act(P, nx, K2, nb2);
+        load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
+        prefetched = true;
       }
       abuf = ab;
     }
