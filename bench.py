@@ -748,15 +748,23 @@ def run_prefill(args):
         qs = {K: torch.empty((M, K), dtype=torch.int8, device=dev) for K in xs}
         ss = {K: torch.empty(M, dtype=torch.float32, device=dev) for K in xs}
         ys = [torch.empty((M, m["N"]), dtype=torch.float32, device=dev) for m in mats]
-        ws = torch.empty(max(nt.nt_ternary_gemm_workspace_size(m["N"], m["K"], M, nt.NT_LAYOUT_TILED)
-                             for m in mats), dtype=torch.uint8, device=dev)
+
+        # q/k/v and gate/up read one input each: one call per group (one activation conversion,
+        # one tile set); o and down alone
+        groups = []
+        for layer in range(L):
+            b = 7 * layer
+            groups += [[b, b + 1, b + 2], [b + 3], [b + 4, b + 5], [b + 6]]
+        wsg = torch.empty(max(nt.nt_ternary_gemm_multi_workspace_size([mats[i]["N"] for i in g], mats[g[0]]["K"], M)
+                              for g in groups[:4]), dtype=torch.uint8, device=dev)
 
         def one_pass():  # on the current stream (the capture stream while a graph records)
             for K in xs:
                 nt.nt_quantize_act(xs[K], qs[K], ss[K])
-            for m, y in zip(mats, ys):
-                nt.nt_ternary_gemm(m["w"], nt.NT_LAYOUT_TILED, m["s_w"], m["N"], m["K"], qs[m["K"]],
-                                   ss[m["K"]], M, y, None, ws)
+            for g in groups:
+                K = mats[g[0]]["K"]
+                nt.nt_ternary_gemm_multi([mats[i]["w"] for i in g], [mats[i]["s_w"] for i in g],
+                                         [mats[i]["N"] for i in g], K, qs[K], ss[K], M, [ys[i] for i in g], None, wsg)
 
         for _ in range(max(1, args.warmup)):
             one_pass()
@@ -804,7 +812,7 @@ def run_prefill(args):
                           "output_GBps": round(out_bytes / (ms * 1e-3) / 1e9, 1),
                           "parity": parity}), flush=True)
         del graph
-        del xs, qs, ss, ys, ws
+        del xs, qs, ss, ys, wsg
         torch.cuda.empty_cache()
 
 

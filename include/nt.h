@@ -193,6 +193,19 @@ nt_status nt_int8_logits_argmax_noalloc(const int8_t* T, const float* s_T, int V
                                         const int8_t* q, const float* s_x, int B,
                                         float* logits_opt, int32_t* argmax, void* stream);
 
+/* Several tiled projections of the same activations (q, k and v read one input, and so do
+ * gate and up): y_i = nt_ternary_gemm(w_i, NT_LAYOUT_TILED, s_w_i, N_i, K, q, s_x, B) for
+ * i < n, in one call. With B >= 64 the tensor-core path converts the activations once for all
+ * n matrices and runs one tile set over their rows (more tiles per launch, fewer launches);
+ * smaller B runs the streaming kernel per matrix. w, s_w, N, y: host arrays of n (1..8)
+ * entries (device pointers, as nt_ternary_gemm); acc_opt: NULL or a host array of n device
+ * pointers, each may be NULL. ws: device workspace of
+ * nt_ternary_gemm_multi_workspace_size(n, N, K, B) bytes (0 below 64 vectors). */
+nt_status nt_ternary_gemm_multi_workspace_size(int n, const int* N, int K, int B, size_t* bytes);
+nt_status nt_ternary_gemm_multi(int n, const void* const* w, const float* const* s_w, const int* N,
+                                int K, const int8_t* q, const float* s_x, int B, float* const* y,
+                                int32_t* const* acc_opt, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * Input-table row gather ("The file is not the traffic": of the input table only the rows of
  * the current tokens are read). x[b][k] = fl((float)T[tokens[b]][k] * s_T[tokens[b]]): the

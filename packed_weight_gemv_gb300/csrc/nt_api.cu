@@ -183,6 +183,51 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
   return launch_gemv_tiled(m, as_stream(stream));
 }
 
+nt_status nt_ternary_gemm_multi_workspace_size(int n, const int* N, int K, int B, size_t* bytes) {
+  clear_error();
+  if (!bytes || !N) return set_error(NT_ERR_INVALID_ARG, "NULL pointer");
+  if (n < 1 || n > 8 || K < 16 || K % 16 != 0 || B < 1)
+    return set_error(NT_ERR_INVALID_ARG, "need 1 <= n <= 8, B >= 1 and K a positive multiple of 16");
+  for (int i = 0; i < n; ++i)
+    if (N[i] < 1) return set_error(NT_ERR_INVALID_ARG, "every N must be >= 1");
+  *bytes = tc_gemm_supported(B, K) ? tc_gemm_multi_workspace_bytes(B, n, N, K) : 0;
+  return NT_OK;
+}
+
+nt_status nt_ternary_gemm_multi(int n, const void* const* w, const float* const* s_w, const int* N, int K,
+                                const int8_t* q, const float* s_x, int B, float* const* y,
+                                int32_t* const* acc_opt, void* ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!w || !s_w || !N || !y) return set_error(NT_ERR_INVALID_ARG, "NULL host array");
+  if (n < 1 || n > 8) return set_error(NT_ERR_INVALID_ARG, "need 1 <= n <= 8");
+  for (int i = 0; i < n; ++i) {
+    NT_TRY(validate_ternary(w[i], NT_LAYOUT_TILED, s_w[i], N[i], K, q, s_x, B, y[i]));
+    if (acc_opt && acc_opt[i] && !aligned(acc_opt[i], 4)) return set_error(NT_ERR_ALIGNMENT, "acc must be 4-byte aligned");
+  }
+  const bool tc = tc_gemm_supported(B, K);
+  if (tc && (!ws || !aligned(ws, 16) || ws_bytes < tc_gemm_multi_workspace_bytes(B, n, N, K)))
+    return set_error(NT_ERR_WORKSPACE, "tensor-core path: workspace NULL, misaligned or smaller than "
+                                       "nt_ternary_gemm_multi_workspace_size");
+  NT_TRY(check_device());
+  if (tc)
+    return launch_gemm_tc_multi(n, reinterpret_cast<const uint8_t* const*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws,
+                                as_stream(stream));
+  for (int i = 0; i < n; ++i) {  // small batches: the streaming kernel per matrix
+    MatDesc m{};
+    m.w = static_cast<const uint8_t*>(w[i]);
+    m.s_w = s_w[i];
+    m.q = q;
+    m.s_x = s_x;
+    m.y = y[i];
+    m.acc = acc_opt ? acc_opt[i] : nullptr;
+    m.N = N[i];
+    m.K = K;
+    m.B = B;
+    NT_TRY(launch_gemv_tiled(m, as_stream(stream)));
+  }
+  return NT_OK;
+}
+
 nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, float* y, int32_t* acc_opt,
                           void* stream) {

@@ -47,6 +47,7 @@ constexpr int kABytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kEpiThreads = 256;         // warps 0-7: two per tensor-memory lane quarter
+constexpr int kTcMaxMats = 8;            // matrices per call sharing the activations
 constexpr int kThreadsTc = kEpiThreads + 64;
 constexpr int kTmemCols = 2 * kBN;       // two accumulators
 constexpr uint64_t kTcTimeoutNs = 2000000000ull;
@@ -173,14 +174,19 @@ __global__ void __launch_bounds__(256) trits_bf16_kernel(const uint8_t* __restri
 // The weights are the MMA's M side (128 rows per tile) and the tokens its N side (256 per
 // tile), so tensor-memory lane = weight row and column = token: each epilogue store of one
 // column by a warp is 32 consecutive floats of one output row.
+// Several matrices sharing the activations are one tile set: matrix i owns weight tiles
+// [tile_start[i], tile_start[i + 1]) (its rows padded to whole tiles in the bf16 copy).
 struct TcParams {
-  const float* s_w;  // [N]
   const float* s_x;  // [M]
-  float* y;          // [M][N]
-  int32_t* acc;      // [M][N] or null
-  int M, N, K;
-  int tiles_n, tiles_m;  // 128-row weight tiles, tn-token tiles
+  int M, K;
+  int tiles_n, tiles_m;  // 128-row weight tiles (all matrices), tn-token tiles
   int tn;                // tokens per tile (MMA N): a multiple of 32, <= kBN
+  int n_mats;
+  int tile_start[kTcMaxMats + 1];
+  int Nm[kTcMaxMats];
+  const float* s_w[kTcMaxMats];  // [N_i]
+  float* y[kTcMaxMats];          // [M][N_i]
+  int32_t* acc[kTcMaxMats];      // [M][N_i] or null
 };
 
 __device__ __forceinline__ void epi_sync() {
@@ -284,9 +290,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++j) {
       const uint32_t buf = j & 1u;
       const int tn = tile % p.tiles_n, tm = tile / p.tiles_n;
-      const int n = tn * kBM + quarter * 32 + lane, m0 = tm * TN;
+      int mi = 0;
+      while (mi + 1 < p.n_mats && tn >= p.tile_start[mi + 1]) ++mi;
+      const int Nm = p.Nm[mi];
+      float* const y = p.y[mi];
+      int32_t* const acc = p.acc[mi];
+      const int n = (tn - p.tile_start[mi]) * kBM + quarter * 32 + lane, m0 = tm * TN;  // row of matrix mi
       sxs[buf * kBN + t] = (t < TN && m0 + t < p.M) ? __ldg(p.s_x + m0 + t) : 0.0f;
-      const float sw = (n < p.N) ? __ldg(p.s_w + n) : 0.0f;
+      const float sw = (n < Nm) ? __ldg(p.s_w[mi] + n) : 0.0f;
       epi_sync();  // token scales of this tile visible to every epilogue thread
       // After a failed wait the thread keeps walking the tiles (the named barrier above needs
       // every epilogue thread) and only skips the stores.
@@ -305,14 +316,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         const uint32_t r[16] = {r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15};
         const int mc = m0 + half * (TN / 2) + c0;
-        if (ok && n < p.N) {
+        if (ok && n < Nm) {
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const int m = mc + q;
             if (m < p.M) {
               const float a = __int_as_float((int)r[q]);  // an exact integer
-              p.y[(int64_t)m * p.N + n] = __fmul_rn(__fmul_rn(a, sw), sxs[buf * kBN + half * (TN / 2) + c0 + q]);
-              if (p.acc) p.acc[(int64_t)m * p.N + n] = __float2int_rn(a);
+              y[(int64_t)m * Nm + n] = __fmul_rn(__fmul_rn(a, sw), sxs[buf * kBN + half * (TN / 2) + c0 + q]);
+              if (acc) acc[(int64_t)m * Nm + n] = __float2int_rn(a);
             }
           }
         }
@@ -386,35 +397,68 @@ int pick_token_tile(int M, int N, int sms) {
 
 bool tc_gemm_supported(int M, int K) { return M >= kTcMinBatch && K <= 131072; }
 
-size_t tc_gemm_workspace_bytes(int M, int N, int K) {
-  return align256((size_t)M * K * 2) + align256((size_t)N * K * 2);
+int64_t tc_weight_rows(int n, const int* N) {
+  int64_t rows = 0;
+  for (int i = 0; i < n; ++i) rows += (int64_t)(N[i] + kBM - 1) / kBM * kBM;
+  return rows;
+}
+
+size_t tc_gemm_workspace_bytes(int M, int N, int K) { return tc_gemm_multi_workspace_bytes(M, 1, &N, K); }
+
+size_t tc_gemm_multi_workspace_bytes(int M, int n, const int* N, int K) {
+  return align256((size_t)M * K * 2) + align256((size_t)tc_weight_rows(n, N) * K * 2);
 }
 
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
                          int M, float* y, int32_t* acc, void* ws, cudaStream_t st) {
+  return launch_gemm_tc_multi(1, &w, &s_w, &N, K, q, s_x, M, &y, &acc, ws, st);
+}
+
+nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* const* s_w, const int* N, int K,
+                               const int8_t* q, const float* s_x, int M, float* const* y, int32_t* const* acc,
+                               void* ws, cudaStream_t st) {
+  if (n < 1 || n > kTcMaxMats) return set_error(NT_ERR_INVALID_ARG, "1 to 8 matrices per call");
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
   NT_TRY(tc_setup(dev));
   uint8_t* a_bf16 = static_cast<uint8_t*>(ws);
   uint8_t* b_bf16 = a_bf16 + align256((size_t)M * K * 2);
   const int sms = device_sm_count();
-  {
+  {  // the activations once for every matrix
     const int64_t groups = (int64_t)M * K / 16;
     const int g = (int)std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 8);
     act_bf16_kernel<<<g, 256, 0, st>>>(reinterpret_cast<const uint4*>(q), groups, reinterpret_cast<uint4*>(a_bf16));
     NT_TRY(check_launch("act_bf16_kernel"));
   }
-  {
-    const int64_t total = (int64_t)N * (K / 16);
+  TcParams p{};
+  p.s_x = s_x;
+  p.M = M;
+  p.K = K;
+  p.n_mats = n;
+  int64_t row = 0;
+  for (int i = 0; i < n; ++i) {  // each matrix's rows from a whole tile on
+    p.tile_start[i] = (int)(row / kBM);
+    p.Nm[i] = N[i];
+    p.s_w[i] = s_w[i];
+    p.y[i] = y[i];
+    p.acc[i] = acc ? acc[i] : nullptr;
+    const int64_t total = (int64_t)N[i] * (K / 16);
     const int g = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
-    trits_bf16_kernel<<<g, 256, 0, st>>>(w, N, K, b_bf16);
+    trits_bf16_kernel<<<g, 256, 0, st>>>(w[i], N[i], K, b_bf16 + row * K * 2);
     NT_TRY(check_launch("trits_bf16_kernel"));
+    const int64_t padded = (int64_t)(N[i] + kBM - 1) / kBM * kBM;
+    if (padded > N[i])  // rows past the matrix inside its last tile read as zeros
+      NT_CUDA_TRY(cudaMemsetAsync(b_bf16 + (row + N[i]) * K * 2, 0, (size_t)(padded - N[i]) * K * 2, st));
+    row += padded;
   }
-  const int tn = pick_token_tile(M, N, sms);
+  p.tile_start[n] = (int)(row / kBM);
+  p.tiles_n = p.tile_start[n];
+  const int tn = pick_token_tile(M, (int)row, sms);
   CUtensorMap mw, mx;
-  NT_TRY(encode_map(&mw, b_bf16, N, K, kBM));  // weights: MMA M side, 128-row boxes
-  NT_TRY(encode_map(&mx, a_bf16, M, K, tn));   // tokens: MMA N side, tn-row boxes
-  TcParams p{s_w, s_x, y, acc, M, N, K, (N + kBM - 1) / kBM, (M + tn - 1) / tn, tn};
+  NT_TRY(encode_map(&mw, b_bf16, (int)row, K, kBM));  // weights: MMA M side, 128-row boxes
+  NT_TRY(encode_map(&mx, a_bf16, M, K, tn));          // tokens: MMA N side, tn-row boxes
+  p.tn = tn;
+  p.tiles_m = (M + tn - 1) / tn;
   const int tiles = p.tiles_m * p.tiles_n;
   gemm_tc_kernel<<<std::min(tiles, sms), kThreadsTc, kSmemTc, st>>>(mw, mx, p);
   return check_launch("gemm_tc_kernel");

@@ -119,6 +119,11 @@ bool tc_gemm_supported(int M, int K);
 size_t tc_gemm_workspace_bytes(int M, int N, int K);
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
                          int M, float* y, int32_t* acc, void* ws, cudaStream_t st);
+// Up to 8 matrices sharing the activations: one activation conversion, one tile set.
+size_t tc_gemm_multi_workspace_bytes(int M, int n, const int* N, int K);
+nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* const* s_w, const int* N, int K,
+                               const int8_t* q, const float* s_x, int M, float* const* y, int32_t* const* acc,
+                               void* ws, cudaStream_t st);
 
 #ifdef __CUDACC__
 // Four consecutive elements k..k+3 (k % 4 == 0) of vector b of a chained stage input. The

@@ -38,7 +38,8 @@ NT_LAUNCH_STREAM = 2
 EXPORTS = (
     "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
-    "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
+    "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_ternary_gemm_multi_workspace_size",
+    "nt_ternary_gemm_multi", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
     "nt_int8_logits_argmax_noalloc", "nt_embed_rows", "nt_verify_accept",
     "nt_attention_workspace_size", "nt_attention_decode", "nt_rope_append", "nt_rmsnorm",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
@@ -107,6 +108,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_ternary_gemv": ([vp, i, vp, i, i, vp, vp, vp, vp, vp], i),
             "nt_ternary_gemm_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], i),
             "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
+            "nt_ternary_gemm_multi_workspace_size": ([i, ctypes.POINTER(i), i, i, ctypes.POINTER(sz)], i),
+            "nt_ternary_gemm_multi": ([i, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i), i, vp, vp, i,
+                                       ctypes.POINTER(vp), ctypes.POINTER(vp), vp, sz, vp], i),
             "nt_int8_logits_workspace_size": ([i, i, i, ctypes.POINTER(sz)], i),
             "nt_int8_logits_argmax": ([vp, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
             "nt_int8_logits_argmax_noalloc": ([vp, vp, i, i, vp, vp, i, vp, vp, vp], i),
@@ -200,6 +204,30 @@ def nt_ternary_gemm(w: torch.Tensor, layout: int, s_w: torch.Tensor, N: int, K: 
     _check(load_library().nt_ternary_gemm(_ptr(w), layout, _ptr(s_w), N, K, _ptr(q), _ptr(s_x), B,
                                           _ptr(y), _ptr(acc), _ptr(ws), ws_bytes, _stream(stream)),
            "nt_ternary_gemm")
+
+
+def nt_ternary_gemm_multi_workspace_size(N: Sequence[int], K: int, B: int) -> int:
+    n = ctypes.c_size_t(0)
+    arr = (ctypes.c_int * len(N))(*N)
+    _check(load_library().nt_ternary_gemm_multi_workspace_size(len(N), arr, K, B, ctypes.byref(n)),
+           "nt_ternary_gemm_multi_workspace_size")
+    return n.value
+
+
+def nt_ternary_gemm_multi(w: Sequence[torch.Tensor], s_w: Sequence[torch.Tensor], N: Sequence[int], K: int,
+                          q: torch.Tensor, s_x: torch.Tensor, B: int, y: Sequence[torch.Tensor],
+                          acc: Optional[Sequence[Optional[torch.Tensor]]] = None,
+                          ws: Optional[torch.Tensor] = None, stream=None):
+    n = len(w)
+    vp = ctypes.c_void_p
+    wa = (vp * n)(*[t.data_ptr() for t in w])
+    sa = (vp * n)(*[t.data_ptr() for t in s_w])
+    na = (ctypes.c_int * n)(*N)
+    ya = (vp * n)(*[t.data_ptr() for t in y])
+    aa = None if acc is None else (vp * n)(*[None if t is None else t.data_ptr() for t in acc])
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load_library().nt_ternary_gemm_multi(n, wa, sa, na, K, _ptr(q), _ptr(s_x), B, ya, aa, _ptr(ws),
+                                                ws_bytes, _stream(stream)), "nt_ternary_gemm_multi")
 
 
 def nt_int8_logits_workspace_size(V: int, K: int, B: int) -> int:

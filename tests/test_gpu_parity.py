@@ -317,3 +317,23 @@ def test_gemm_tensor_cores_cancellation():
                      device=DEV)
     nt.nt_ternary_gemm(tiled(w, N, K), nt.NT_LAYOUT_TILED, dev(s_w), N, K, dev(q), dev(s), M, gy, gacc, ws)
     assert np.array_equal(host(gacc), acc)
+
+
+@pytest.mark.parametrize("M,Ns,K", [(300, (200, 128, 389), 1040), (2048, (2048, 1024, 1024), 1024),
+                                    (64, (3072, 3072), 1024), (40, (100, 36, 64), 512)])
+def test_gemm_multi_shared_activations(M, Ns, K):
+    # several matrices of one input in one call: every output exact, whatever the row counts
+    # (tiles of one matrix never mix rows of another), on the tensor-core path (M >= 64) and
+    # the per-matrix path below it
+    ps = [wl.projection(17, i, len(Ns), N, K, M, seed=10) for i, N in enumerate(Ns)]
+    x = ps[0].x
+    q, s = oracle.quantize(x)
+    ws = torch.empty(max(1, nt.nt_ternary_gemm_multi_workspace_size(list(Ns), K, M)), dtype=torch.uint8, device=DEV)
+    ys = [torch.full((M, N), float("nan"), device=DEV) for N in Ns]
+    accs = [torch.empty((M, N), dtype=torch.int32, device=DEV) for N in Ns]
+    nt.nt_ternary_gemm_multi([tiled(p.w_plain, p.N, K) for p in ps], [dev(p.s_w) for p in ps], list(Ns), K, dev(q),
+                             dev(s), M, ys, accs, ws)
+    for p, gy, ga in zip(ps, ys, accs):
+        acc, y, _ = oracle.gemm(p.w_plain, p.s_w, p.N, K, q, s)
+        assert np.array_equal(host(ga), acc)
+        assert_close(host(gy), y, f"multi {p.N}")
