@@ -11,15 +11,18 @@
 // K <= 131072, so the fp32 accumulator in tensor memory holds the exact integer sum; the
 // epilogue applies the same two rounded products as every other path.
 //
-// A call runs three kernels:
-//   1. int8 activations -> bf16 [M][K] and 2. tiled trits -> bf16 [N][K], both into the
-//      caller's workspace (operands for this call only; nothing is kept across calls);
-//   3. a persistent GEMM, one CTA per SM, looping over tiles of 128 weight rows (MMA M) x TN
-//      tokens (MMA N; TN <= 256 picked per call so the tiles fill whole waves of SMs):
+// A call runs two kernels:
+//   1. preparation: int8 activations -> bf16 [M][K] (once for every matrix of the call), each
+//      matrix's tiled trits -> bf16 rows starting on a whole 128-row tile, zeros for the rows
+//      that pad a matrix to whole tiles -- all into the caller's workspace (operands for this
+//      call only; nothing is kept across calls);
+//   2. a persistent GEMM over the tiles of all matrices, one CTA per SM, looping over tiles of
+//      128 weight rows (MMA M) x TN tokens (MMA N; TN <= 256 picked per call so the tiles fill
+//      whole waves of SMs):
 //        warp 8 lane 0: 2-D TMA loads (128-byte swizzle) of both operands of each 64-wide K
 //          step into a 4-stage ring (full/empty mbarriers);
 //        warp 9: allocates 512 tensor-memory columns (two 256-column accumulators); lane 0
-//          issues tcgen05.mma (M = 128, N = 256, K = 16; 4 per K step), commits each stage's
+//          issues tcgen05.mma (M = 128, N = TN, K = 16; 4 per K step), commits each stage's
 //          release and each finished accumulator;
 //        warps 0-7: epilogue -- tcgen05.ld of a finished accumulator (lane = weight row,
 //          column = token), scales, fp32 stores that are 128-byte coalesced per warp --
@@ -143,30 +146,51 @@ __device__ __forceinline__ uint2 int8x4_bf16(uint32_t x) {
 }
 
 // ---- operand conversion --------------------------------------------------------------
-__global__ void __launch_bounds__(256) act_bf16_kernel(const uint4* __restrict__ q, int64_t groups,
-                                                       uint4* __restrict__ out) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < groups; i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4 v = __ldg(q + i);
-    const uint2 c0 = int8x4_bf16(v.x), c1 = int8x4_bf16(v.y), c2 = int8x4_bf16(v.z), c3 = int8x4_bf16(v.w);
-    out[2 * i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
-    out[2 * i + 1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
-  }
-}
+// All operand preparation of one call in one launch: the activations, every matrix's trits,
+// and zeros for the rows that pad each matrix to whole tiles (one grid-stride index space).
+struct PrepArgs {
+  const uint4* q;
+  int64_t act_groups;   // 16-byte groups of activations
+  uint4* a_out;
+  int n, K;
+  const uint8_t* w[kTcMaxMats];
+  int N[kTcMaxMats];
+  uint8_t* b_out[kTcMaxMats];        // bf16 rows of matrix i
+  int64_t word_start[kTcMaxMats + 1];  // cumulative (row, 16-trit word) counts
+  uint4* pad[kTcMaxMats];            // first padding row of matrix i
+  int64_t pad_start[kTcMaxMats + 1];   // cumulative 16-byte zero stores
+};
 
-// Tiled trits -> bf16 [N][K]: one thread per (row, 16-trit word), consecutive threads along K
-// so that each warp writes 32 consecutive 32-byte pieces of a row.
-__global__ void __launch_bounds__(256) trits_bf16_kernel(const uint8_t* __restrict__ w, int N, int K,
-                                                         uint8_t* __restrict__ out) {
-  const int kg = K / 16;
-  const int64_t Kp = padded_k(K), total = (int64_t)N * kg;
+__global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
+  const int64_t words = a.word_start[a.n], total = a.act_groups + words + a.pad_start[a.n];
+  const int kg = a.K / 16;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t n = i / kg, j = i % kg;
-    const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(w + (n >> 2) * Kp + j * 16 + (n & 3) * 4));
-    const Trits16 d = tiled_word_decode(word);
-    const uint2 a0 = trits4_bf16(d.t0), a1 = trits4_bf16(d.t1), a2 = trits4_bf16(d.t2), a3 = trits4_bf16(d.t3);
-    uint4* dst = reinterpret_cast<uint4*>(out + (n * K + j * 16) * 2);
-    dst[0] = make_uint4(a0.x, a0.y, a1.x, a1.y);
-    dst[1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+    if (i < a.act_groups) {
+      const uint4 v = __ldg(a.q + i);
+      const uint2 c0 = int8x4_bf16(v.x), c1 = int8x4_bf16(v.y), c2 = int8x4_bf16(v.z), c3 = int8x4_bf16(v.w);
+      a.a_out[2 * i] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+      a.a_out[2 * i + 1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
+      continue;
+    }
+    int64_t j = i - a.act_groups;
+    if (j < words) {
+      int mi = 0;
+      while (j >= a.word_start[mi + 1]) ++mi;
+      j -= a.word_start[mi];
+      const int64_t r = j / kg, g = j % kg;
+      const int64_t Kp = padded_k(a.K);
+      const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(a.w[mi] + (r >> 2) * Kp + g * 16 + (r & 3) * 4));
+      const Trits16 d = tiled_word_decode(word);
+      const uint2 a0 = trits4_bf16(d.t0), a1 = trits4_bf16(d.t1), a2 = trits4_bf16(d.t2), a3 = trits4_bf16(d.t3);
+      uint4* dst = reinterpret_cast<uint4*>(a.b_out[mi] + (r * a.K + g * 16) * 2);
+      dst[0] = make_uint4(a0.x, a0.y, a1.x, a1.y);
+      dst[1] = make_uint4(a2.x, a2.y, a3.x, a3.y);
+      continue;
+    }
+    j -= words;
+    int mi = 0;
+    while (j >= a.pad_start[mi + 1]) ++mi;
+    a.pad[mi][j - a.pad_start[mi]] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -424,12 +448,12 @@ nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* cons
   uint8_t* a_bf16 = static_cast<uint8_t*>(ws);
   uint8_t* b_bf16 = a_bf16 + align256((size_t)M * K * 2);
   const int sms = device_sm_count();
-  {  // the activations once for every matrix
-    const int64_t groups = (int64_t)M * K / 16;
-    const int g = (int)std::min<int64_t>((groups + 255) / 256, (int64_t)sms * 8);
-    act_bf16_kernel<<<g, 256, 0, st>>>(reinterpret_cast<const uint4*>(q), groups, reinterpret_cast<uint4*>(a_bf16));
-    NT_TRY(check_launch("act_bf16_kernel"));
-  }
+  PrepArgs pa{};
+  pa.q = reinterpret_cast<const uint4*>(q);
+  pa.act_groups = (int64_t)M * K / 16;  // the activations once for every matrix
+  pa.a_out = reinterpret_cast<uint4*>(a_bf16);
+  pa.n = n;
+  pa.K = K;
   TcParams p{};
   p.s_x = s_x;
   p.M = M;
@@ -442,14 +466,22 @@ nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* cons
     p.s_w[i] = s_w[i];
     p.y[i] = y[i];
     p.acc[i] = acc ? acc[i] : nullptr;
-    const int64_t total = (int64_t)N[i] * (K / 16);
-    const int g = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
-    trits_bf16_kernel<<<g, 256, 0, st>>>(w[i], N[i], K, b_bf16 + row * K * 2);
-    NT_TRY(check_launch("trits_bf16_kernel"));
     const int64_t padded = (int64_t)(N[i] + kBM - 1) / kBM * kBM;
-    if (padded > N[i])  // rows past the matrix inside its last tile read as zeros
-      NT_CUDA_TRY(cudaMemsetAsync(b_bf16 + (row + N[i]) * K * 2, 0, (size_t)(padded - N[i]) * K * 2, st));
+    pa.w[i] = w[i];
+    pa.N[i] = N[i];
+    pa.b_out[i] = b_bf16 + row * K * 2;
+    pa.word_start[i + 1] = pa.word_start[i] + (int64_t)N[i] * (K / 16);
+    // rows past the matrix inside its last tile must read as zeros (garbage there corrupted
+    // valid outputs on the tensor cores)
+    pa.pad[i] = reinterpret_cast<uint4*>(b_bf16 + (row + N[i]) * K * 2);
+    pa.pad_start[i + 1] = pa.pad_start[i] + (padded - N[i]) * K * 2 / 16;
     row += padded;
+  }
+  {
+    const int64_t total = pa.act_groups + pa.word_start[n] + pa.pad_start[n];
+    const int g = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
+    prep_kernel<<<g, 256, 0, st>>>(pa);
+    NT_TRY(check_launch("prep_kernel"));
   }
   p.tile_start[n] = (int)(row / kBM);
   p.tiles_n = p.tile_start[n];
