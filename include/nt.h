@@ -243,8 +243,10 @@ nt_status nt_verify_accept(const int32_t* draft, const int32_t* argmax, int B, i
  * nt_attention_decode: B new positions attend over a cache of T rows whose last B rows are
  * those positions (they were appended first, e.g. by nt_rope_append): position b sees rows
  * 0 .. T - B + b. out[b][h] = sum_t softmax_t(q[b][h] . k[g][t] / sqrt(D)) v[g][t] with
- * g = h / (Hq / Hkv). fp32 arithmetic; the result is within a few 1e-6 of the exact value
- * relative to max |v| (one launch: 128-position chunks, merged by the last chunk to finish).
+ * g = h / (Hq / Hkv). Both products on the tensor cores with bf16 operands and fp32 sums: q
+ * enters as three bf16 terms and the softmax weights as two, so the result is within a few
+ * 1e-6 of the exact value relative to max |v| (one launch: units of cache positions per
+ * key-value head, merged by the last unit to finish).
  *   q [B][Hq][D] fp32; k_cache, v_cache [Hkv][t_stride][D] bf16 bit patterns (16-byte
  *   aligned); out [B][Hq][D] fp32; Hq / Hkv in {1, 2, 4, 8}; 1 <= B <= 64; B <= T <= t_stride.
  *   ws: device workspace of nt_attention_workspace_size(B, Hq, Hkv, T) bytes (16-byte

@@ -120,8 +120,8 @@ __device__ __forceinline__ void attn_issue(const uint16_t* kh, const uint16_t* v
 // Registers of one step from its stage: keys of positions g and 8 + g (64 bytes each, dims
 // 32 i + 8 t ..), values of positions 2t, 2t + 1, 2t + 8, 2t + 9 (dims 8g .. 8g + 7 and
 // 64 + 8g ..). Value rows at or past vis read as zero (the stage holds stale rows there).
-__device__ __forceinline__ void attn_read(const uint8_t* stage, int p0, int vis, int g, int t, uint4 (&kw)[2][4],
-                                          uint4 (&vw)[4][2]) {
+__device__ __forceinline__ void attn_read(const uint8_t* stage, int p0, int vis, bool full, int g, int t,
+                                          uint4 (&kw)[2][4], uint4 (&vw)[4][2]) {
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     const uint8_t* row = stage + (8 * nt + g) * kRowPitch + 16 * t;
@@ -134,15 +134,22 @@ __device__ __forceinline__ void attn_read(const uint8_t* stage, int p0, int vis,
     const uint8_t* row = stage + (kAttnStep + pr) * kRowPitch + 16 * g;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf)
-      vw[r][hf] = p0 + pr < vis ? *reinterpret_cast<const uint4*>(row + 128 * hf) : make_uint4(0u, 0u, 0u, 0u);
+      vw[r][hf] = full || p0 + pr < vis ? *reinterpret_cast<const uint4*>(row + 128 * hf) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
+__device__ __forceinline__ float ex2(float x) {  // 2^x (MUFU; 2^-inf = +0)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One warp step: scores, softmax update and weighted values of positions p0 .. p0 + 15.
+// `full`: all 16 positions are below vis (the same in every lane).
 template <int G, int HG>
 __device__ __forceinline__ void attn_compute(const uint32_t (&qa)[HG][8][4], float (&O)[HG][8][4],
                                              float (&mref)[HG][4], float (&lsum)[HG], const uint4 (&kw)[2][4],
-                                             const uint4 (&vw)[4][2], int p0, int vis, int g, int t) {
+                                             const uint4 (&vw)[4][2], int p0, int vis, bool full, int g, int t) {
   const int hl = g & 3;
 #pragma unroll
   for (int grp = 0; grp < HG; ++grp) {
@@ -150,34 +157,34 @@ __device__ __forceinline__ void attn_compute(const uint32_t (&qa)[HG][8][4], flo
     float s[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // two chains
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_16816(d, qa[grp][j][0], qa[grp][j][1], qa[grp][j][2], qa[grp][j][3],
-                  word(kw[nt][j >> 1], 2 * (j & 1)), word(kw[nt][j >> 1], 2 * (j & 1) + 1));
-      const float x0 = d[0] + d[2], x1 = d[1] + d[3];
+      for (int j = 0; j < 8; j += 2) {
+        mma_16816(d0, qa[grp][j][0], qa[grp][j][1], qa[grp][j][2], qa[grp][j][3], word(kw[nt][j >> 1], 0),
+                  word(kw[nt][j >> 1], 1));
+        mma_16816(d1, qa[grp][j + 1][0], qa[grp][j + 1][1], qa[grp][j + 1][2], qa[grp][j + 1][3],
+                  word(kw[nt][j >> 1], 2), word(kw[nt][j >> 1], 3));
+      }
+      const float x0 = (d0[0] + d1[0]) + (d0[2] + d1[2]), x1 = (d0[1] + d1[1]) + (d0[3] + d1[3]);
       s[nt][0] = x0 + __shfl_xor_sync(0xffffffffu, x0, 16);
       s[nt][1] = x1 + __shfl_xor_sync(0xffffffffu, x1, 16);
+      if (!full || (G < 4 && !used)) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-        if (!used || p0 + 8 * nt + 2 * t + e >= vis) s[nt][e] = -INFINITY;
+        for (int e = 0; e < 2; ++e)
+          if (!used || p0 + 8 * nt + 2 * t + e >= vis) s[nt][e] = -INFINITY;
+      }
     }
-    float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    float sm[4];
-    bool up = false;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      sm[k] = __shfl_sync(0xffffffffu, mx, 4 * k);
-      up |= sm[k] > mref[grp][k] + kAttnLazy;
-    }
-    if (up) {  // the same in every lane
+    float my = pick(mref[grp], hl);
+    const float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    if (__any_sync(0xffffffffu, mx > my + kAttnLazy)) {  // rare after the first step
+      float m4 = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      m4 = fmaxf(m4, __shfl_xor_sync(0xffffffffu, m4, 2));
       float corr[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float mn = fmaxf(mref[grp][k], sm[k]);
-        corr[k] = mn == mref[grp][k] ? 1.0f : exp2f(mref[grp][k] - mn);
+        const float sm = __shfl_sync(0xffffffffu, m4, 4 * k);
+        const float mn = fmaxf(mref[grp][k], sm);
+        corr[k] = mn == mref[grp][k] ? 1.0f : ex2(mref[grp][k] - mn);
         mref[grp][k] = mn;
       }
       const float c0 = (t & 1) ? corr[2] : corr[0], c1 = (t & 1) ? corr[3] : corr[1];
@@ -189,21 +196,17 @@ __device__ __forceinline__ void attn_compute(const uint32_t (&qa)[HG][8][4], flo
         O[grp][mt][3] *= c1;
       }
       lsum[grp] *= pick(corr, hl);
+      my = pick(mref[grp], hl);
     }
-    const float my = pick(mref[grp], hl);
     uint32_t pb[2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      float term[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float p = used ? exp2f(s[nt][e] - my) : 0.0f;
-        const float phi = bf16_rn(p);
-        const float plo = bf16_rn(__fsub_rn(p, phi));
-        lsum[grp] += phi + plo;
-        term[e] = g < 4 ? phi : plo;
-      }
-      pb[nt] = pack_bf16(term[0], term[1]);
+      const float q0 = used ? ex2(s[nt][0] - my) : 0.0f, q1 = used ? ex2(s[nt][1] - my) : 0.0f;
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(q0, q1);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(__fsub_rn(q0, __low2float(hi)), __fsub_rn(q1, __high2float(hi)));
+      lsum[grp] += q0 + q1;
+      const __nv_bfloat162 term = g < 4 ? hi : lo;
+      pb[nt] = *reinterpret_cast<const uint32_t*>(&term);
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -216,19 +219,21 @@ __device__ __forceinline__ void attn_compute(const uint32_t (&qa)[HG][8][4], flo
   }
 }
 
-// One CTA of 4 warps per (unit of `span` cache positions, key-value head). Each warp walks
-// 16-position steps of the unit (warp w takes steps w, w + 4, ...) with both products on the
-// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
+// One CTA of 4 warps per (unit of `span` cache positions, key-value head), two CTAs per SM.
+// Each warp walks 16-position steps of the unit (warp w takes steps w, w + 4, ...): its lane 0
+// keeps three steps of key and value rows in flight (bulk copies into the warp's ring in shared
+// memory, completing on one mbarrier per stage), and both products run on the tensor cores
+// (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
 //
 // * scores S[16 x 8] = Q[16 x 128] K^T per 8 positions. The rows of Q are the group's 4 query
 //   heads, each split into three bf16 terms (hi, mid, lo: q = hi + mid + lo to ~2^-26
-//   relative), row = 4 * term + head; K enters as the MMA's column operand straight from the
-//   cache rows, so lane (g, t) loads 16 contiguous bytes of position g per 16 dimensions (the
-//   dimension order inside the MMA is permuted; Q uses the same permutation). The three terms'
-//   rows are added in fp32, one shuffle joining the lanes that hold them.
+//   relative), row = 4 * term + head; K is the MMA's column operand, lane (g, t) reading 16
+//   contiguous bytes of position g per 32 dimensions (the dimension order inside the MMA is
+//   permuted; Q uses the same permutation). The three terms' rows are added in fp32, one
+//   shuffle joining the lanes that hold them.
 // * softmax: scores are in log2 units (q carries log2(e) / sqrt(D)); a running reference max per
-//   head is raised only when a score exceeds it by more than 2^8 (weights stay <= 256, so no
-//   overflow), and the accumulators are rescaled then.
+//   head is raised only when a score exceeds it by more than 2^8 (a warp vote; weights stay
+//   <= 256, so nothing overflows), and the accumulators are rescaled then.
 // * weighted values O^T[128 x 8] += V^T[128 x 16] P^T[16 x 8]. The columns of P^T are the 4
 //   heads' weights split into two bf16 terms (hi, lo: p = hi + lo to ~2^-17 relative); the score
 //   tile's register layout is exactly the B operand's, so the weights never leave their lanes.
@@ -237,7 +242,8 @@ __device__ __forceinline__ void attn_compute(const uint32_t (&qa)[HG][8][4], flo
 //
 // Keys and values are exact in bf16, so every product is exact; the sums run in fp32. The 4
 // warps' (weighted sums, reference max, weight sum) are merged in shared memory into the unit's
-// partial result; the last CTA of each (b, key-value head) merges all units into out.
+// partial result; the last CTA of each (b, key-value head) to finish merges all units into out
+// in one pass.
 template <int G>
 __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kernel(const AttnArgs a) {
   constexpr int HG = (G + 3) / 4;  // groups of 4 query heads
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
   float (*Acc)[G][kAttnD] = reinterpret_cast<float (*)[G][kAttnD]>(attn_smem);
   __shared__ __align__(8) uint64_t bars[kAttnWarps][kAttnStages];
   __shared__ float mw[kAttnWarps][G], lw[kAttnWarps][G];
-  __shared__ int s_last, s_fail;
+  __shared__ int s_last;
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x, lane = i & 31, w = i >> 5;
   const int g = lane >> 2, t = lane & 3, hl = g & 3;
   const int T = a.T_dev ? *a.T_dev : a.T;
@@ -264,11 +270,10 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8u * st) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();  // barriers initialised, s_fail cleared
+  __syncwarp();  // this warp's barriers are initialised
   // steps this warp has issued and consumed (step n: stage n % S, phase parity (n / S) & 1)
   uint32_t used_steps = 0, issued_steps = 0;
   bool ok = true;  // false once a copy has not completed within the time limit
-  if (i == 0) s_fail = 0;
 
   for (int b = 0; b < a.B; ++b) {
     const int vis = min(u1, T - a.B + b + 1);  // positions [u0, vis) are visible to b
@@ -338,8 +343,9 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
         break;
       }
       uint4 kw[2][4], vw[4][2];
-      attn_read(attn_smem + (size_t)w * kAttnStages * kStageBytes + st * kStageBytes, p0, vis, g, t, kw, vw);
-      attn_compute<G, HG>(qa, O, mref, lsum, kw, vw, p0, vis, g, t);
+      const bool full = p0 + kAttnStep <= vis;
+      attn_read(attn_smem + (size_t)w * kAttnStages * kStageBytes + st * kStageBytes, p0, vis, full, g, t, kw, vw);
+      attn_compute<G, HG>(qa, O, mref, lsum, kw, vw, p0, vis, full, g, t);
       __syncwarp();  // every lane's reads of the stage are done (their values fed the MMAs)
       const int pn = p0 + kAttnStages * kStride;
       if (pn < vis) {
@@ -351,9 +357,10 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
       for (uint32_t n = used_steps; n < issued_steps; ++n)
         if (!mbar_wait_bounded(bar0 + 8u * (n % kAttnStages), (n / kAttnStages) & 1u)) break;
       used_steps = issued_steps;
-      s_fail = 1;
     }
-    __syncthreads();  // every warp's ring is idle: it holds Acc from here on
+    // every warp's ring is idle: it holds Acc from here on; a failed wait anywhere in the CTA
+    // marks the unit's result
+    const bool fail = __syncthreads_or(!ok);
     // the warp's result: weight sums over the lanes of a head, the two weight terms added
     // (columns 2t, 2t + 1 and 2t + 4, 2t + 5 hold the same heads), into shared memory
 #pragma unroll
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
       pb[k * head_stride + i] = o;
       if (i == 0) {
         pb[k * head_stride + kAttnD] = M;
-        pb[k * head_stride + kAttnD + 1] = s_fail ? __int_as_float(0x7fc00000) : L;  // NaN marks a failed unit
+        pb[k * head_stride + kAttnD + 1] = fail ? __int_as_float(0x7fc00000) : L;  // NaN marks a failed unit
       }
     }
     // The last unit of this (b, key-value head) to finish merges all units in one pass: warp w
