@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
   __shared__ int s_last;
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x, lane = i & 31, w = i >> 5;
   const int g = lane >> 2, t = lane & 3, hl = g & 3;
+  dependent_launch_wait();
   const int T = a.T_dev ? *a.T_dev : a.T;
   const int u0 = c * a.span, u1 = min(T, u0 + a.span);
   const uint16_t* kh = a.kc + (int64_t)h * a.ts * kAttnD;
@@ -493,6 +494,7 @@ __global__ void rope_append_kernel(const float* __restrict__ q, const float* __r
                                    float* __restrict__ q_out, uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
                                    int ts) {
   __shared__ float cs[kAttnD / 2], sn[kAttnD / 2];
+  dependent_launch_wait();
   const int pos0 = pos_dev ? *pos_dev : pos0_arg;
   const int b = blockIdx.x, pos = pos0 + b;
   constexpr int half = kAttnD / 2;
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
 }
 
 template <int G>
-nt_status launch_attn_units(const AttnArgs& a, cudaStream_t st) {
+nt_status launch_attn_units(const AttnArgs& a, cudaStream_t st, bool pdl) {
   static std::atomic<int> attr_set[64];  // per device: the ring's dynamic shared memory allowed
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
@@ -556,7 +558,7 @@ nt_status launch_attn_units(const AttnArgs& a, cudaStream_t st) {
     NT_CUDA_TRY(cudaFuncSetAttribute(attn_unit_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes));
     attr_set[dev].store(1, std::memory_order_release);
   }
-  attn_unit_kernel<G><<<dim3(a.nch, a.Hkv), kAttnThreads, kRingBytes, st>>>(a);
+  NT_CUDA_TRY(launch_kernel(attn_unit_kernel<G>, dim3(a.nch, a.Hkv), dim3(kAttnThreads), kRingBytes, st, pdl, a));
   return check_launch("attn_unit_kernel");
 }
 
@@ -584,24 +586,25 @@ size_t attention_ws_bytes(int B, int Hq, int Hkv, int T) {
 }
 
 nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* vc, int B, int Hq, int Hkv, int T,
-                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev) {
+                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev, bool pdl) {
   float* part = static_cast<float*>(ws);
   unsigned int* done = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + attn_part_bytes(B, Hq, Hkv, T));
   const int G = Hq / Hkv;
   AttnArgs a{q, kc, vc, part, done, out, B, Hq, Hkv, T, ts, attn_units(T, Hkv, G), attn_span(T, Hkv, G),
              (float)(1.4426950408889634 / sqrt((double)kAttnD)), T_dev};
   switch (G) {
-    case 1: return launch_attn_units<1>(a, st);
-    case 2: return launch_attn_units<2>(a, st);
-    case 4: return launch_attn_units<4>(a, st);
-    default: return launch_attn_units<8>(a, st);
+    case 1: return launch_attn_units<1>(a, st, pdl);
+    case 2: return launch_attn_units<2>(a, st, pdl);
+    case 4: return launch_attn_units<4>(a, st, pdl);
+    default: return launch_attn_units<8>(a, st, pdl);
   }
 }
 
 nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
                              float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st,
-                             const int* pos_dev) {
-  rope_append_kernel<<<B, 256, 0, st>>>(q, k, v, Hq, Hkv, pos0, pos_dev, log2((double)base), q_out, kc, vc, ts);
+                             const int* pos_dev, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(rope_append_kernel, dim3(B), dim3(256), 0, st, pdl, q, k, v, Hq, Hkv, pos0, pos_dev,
+                            log2((double)base), q_out, kc, vc, ts));
   return check_launch("rope_append_kernel");
 }
 

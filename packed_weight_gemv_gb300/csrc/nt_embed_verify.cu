@@ -15,6 +15,7 @@ namespace {
 __global__ void __launch_bounds__(256) embed_kernel(const int8_t* __restrict__ T, const float* __restrict__ s,
                                                    int V, int K, const int32_t* __restrict__ tokens,
                                                    float* __restrict__ x, uint32_t* __restrict__ n_bad) {
+  dependent_launch_wait();
   const int b = blockIdx.x;
   const int t = tokens[b];
   const bool ok = t >= 0 && t < V;
@@ -36,20 +37,21 @@ __global__ void __launch_bounds__(256) embed_kernel(const int8_t* __restrict__ T
 
 __global__ void verify_kernel(const int32_t* __restrict__ draft, const int32_t* __restrict__ argmax, int B,
                               int32_t* __restrict__ emit, int32_t* __restrict__ n_emit) {
+  dependent_launch_wait();
   if (threadIdx.x == 0 && blockIdx.x == 0) *n_emit = verify_accept_device(draft, argmax, B, emit);
 }
 
 }  // namespace
 
 nt_status launch_embed(const int8_t* T, const float* s, int V, int K, const int32_t* tokens, int B, float* x,
-                       uint32_t* n_bad, cudaStream_t st) {
-  embed_kernel<<<B, 256, 0, st>>>(T, s, V, K, tokens, x, n_bad);
+                       uint32_t* n_bad, cudaStream_t st, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(embed_kernel, dim3(B), dim3(256), 0, st, pdl, T, s, V, K, tokens, x, n_bad));
   return check_launch("embed_kernel");
 }
 
 nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit, int32_t* n_emit,
-                        cudaStream_t st) {
-  verify_kernel<<<1, 32, 0, st>>>(draft, argmax, B, emit, n_emit);
+                        cudaStream_t st, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(verify_kernel, dim3(1), dim3(32), 0, st, pdl, draft, argmax, B, emit, n_emit));
   return check_launch("verify_kernel");
 }
 

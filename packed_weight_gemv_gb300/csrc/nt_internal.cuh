@@ -37,6 +37,26 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 // Checks a kernel launch (configuration errors only; faults surface at the next sync).
 nt_status check_launch(const char* what);
 
+// Launches kern<<<grid, block, smem, st>>>(args...); with pdl the launch may begin while the
+// previous kernel in the stream is still running (programmatic dependent launch). Every kernel
+// launched this way starts with dependent_launch_wait(), so only its launch and scheduling
+// overlap the previous kernel: none of its memory accesses do.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------------------
 // Layout constants of the tiled ternary layout (see nt.h).
 // ---------------------------------------------------------------------------------------
@@ -135,6 +155,14 @@ __device__ __forceinline__ int verify_accept_device(const int32_t* draft, const 
   }
   emit[j] = argmax[j];
   return j + 1;
+}
+
+// First statement of a kernel that may be launched as a programmatic dependent: waits until the
+// previous kernel in the stream has completed and its writes are visible (returns at once when
+// the launch had no such dependency), then lets the next kernel's launch begin.
+__device__ __forceinline__ void dependent_launch_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

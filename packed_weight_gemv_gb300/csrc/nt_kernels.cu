@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
 
 __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob* __restrict__ jobs,
                                                                  int max_B) {
+  dependent_launch_wait();
   const QuantJob j = jobs[blockIdx.x];
   const int b = blockIdx.y;
   if (b >= j.B) return;
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob*
 __global__ void __launch_bounds__(kChainThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
   __shared__ float red[kChainWarps];
   __shared__ double redd[kChainWarps];
+  dependent_launch_wait();
   const ChainJob j = *jobs;
   const int b = blockIdx.x, K = j.src.K;
   float* vb = j.vbuf + (int64_t)b * K;
@@ -283,6 +285,7 @@ __global__ void __launch_bounds__(kThreads) gemv_tiled_kernel(const MatDesc m) {
 template <int NB>
 __global__ void __launch_bounds__(kThreads) gemv_tiled_group_kernel(
     const MatDesc* __restrict__ mats, const int64_t* __restrict__ prefix, int n, int64_t total) {
+  dependent_launch_wait();
   const int lane = threadIdx.x & 31;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < total;
        t += (int64_t)gridDim.x * kWarps) {
@@ -406,13 +409,13 @@ nt_status launch_quantize(const float* x, int B, int K, int8_t* q, float* s, cud
   return check_launch("quantize_kernel");
 }
 
-nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st) {
-  quantize_jobs_kernel<<<dim3(n_jobs, max_B), kThreads, 0, st>>>(d_jobs, max_B);
+nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(quantize_jobs_kernel, dim3(n_jobs, max_B), dim3(kThreads), 0, st, pdl, d_jobs, max_B));
   return check_launch("quantize_jobs_kernel");
 }
 
-nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st) {
-  chain_quant_kernel<<<B, kChainThreads, 0, st>>>(d_job);
+nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(chain_quant_kernel, dim3(B), dim3(kChainThreads), 0, st, pdl, d_job));
   return check_launch("chain_quant_kernel");
 }
 
@@ -447,13 +450,12 @@ nt_status launch_gemv_tiled(const MatDesc& m, cudaStream_t st) {
 }
 
 nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_prefix, int n,
-                                  int64_t total, int max_B, cudaStream_t st) {
+                                  int64_t total, int max_B, cudaStream_t st, bool pdl) {
   const int g = grid_for(total, 8);
-  if (max_B == 1) gemv_tiled_group_kernel<1><<<g, kThreads, 0, st>>>(d_mats, d_prefix, n, total);
-  else if (max_B == 2) gemv_tiled_group_kernel<2><<<g, kThreads, 0, st>>>(d_mats, d_prefix, n, total);
-  else if (max_B <= 4) gemv_tiled_group_kernel<4><<<g, kThreads, 0, st>>>(d_mats, d_prefix, n, total);
-  else if (max_B <= 8) gemv_tiled_group_kernel<8><<<g, kThreads, 0, st>>>(d_mats, d_prefix, n, total);
-  else gemv_tiled_group_kernel<16><<<g, kThreads, 0, st>>>(d_mats, d_prefix, n, total);
+  auto kern = max_B == 1 ? gemv_tiled_group_kernel<1> : max_B == 2 ? gemv_tiled_group_kernel<2>
+            : max_B <= 4 ? gemv_tiled_group_kernel<4> : max_B <= 8 ? gemv_tiled_group_kernel<8>
+                         : gemv_tiled_group_kernel<16>;
+  NT_CUDA_TRY(launch_kernel(kern, dim3(g), dim3(kThreads), 0, st, pdl, d_mats, d_prefix, n, total));
   return check_launch("gemv_tiled_group_kernel");
 }
 

@@ -77,7 +77,7 @@ inline size_t head_ws_bytes(int B) { return 16 + sizeof(HeadPartial) * (size_t)k
 
 // Launchers (asynchronous on `st`; they return launch-configuration errors only).
 nt_status launch_quantize(const float* x, int B, int K, int8_t* q, float* s, cudaStream_t st);
-nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st);
+nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st, bool pdl = false);
 nt_status launch_repack(const uint32_t* w, int N, int K, uint8_t* out, uint32_t* n_invalid,
                         cudaStream_t st);
 nt_status launch_gemv_plain(const uint32_t* w, const float* s_w, int N, int K, const int8_t* q,
@@ -86,18 +86,18 @@ nt_status launch_gemv_tiled(const MatDesc& m, cudaStream_t st);
 // Several tiled projections in one launch: d_mats[n] in device memory, d_tile_prefix[n+1]
 // their cumulative tile counts.
 nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_tile_prefix, int n,
-                                  int64_t total_tiles, int max_B, cudaStream_t st);
+                                  int64_t total_tiles, int max_B, cudaStream_t st, bool pdl = false);
 nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
                       cudaStream_t st);
 
 // Quantizes one chained stage input per vector (one CTA per vector).
-nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st);
+nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st, bool pdl = false);
 
 nt_status launch_embed(const int8_t* T, const float* s, int V, int K, const int32_t* tokens, int B, float* x,
-                       uint32_t* n_bad, cudaStream_t st);
+                       uint32_t* n_bad, cudaStream_t st, bool pdl = false);
 nt_status launch_verify(const int32_t* draft, const int32_t* argmax, int B, int32_t* emit, int32_t* n_emit,
-                        cudaStream_t st);
+                        cudaStream_t st, bool pdl = false);
 
 // Attention side of a layer (nt_attention.cu): head dimension 128.
 // The workspace's counters (after the partial results) must be zero before the first call;
@@ -106,10 +106,11 @@ size_t attention_ws_bytes(int B, int Hq, int Hkv, int T);
 // T_dev / pos_dev (optional): the cache length / first new position read from device memory
 // when the kernel runs (a plan's position); T then only sizes the grid.
 nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* vc, int B, int Hq, int Hkv, int T,
-                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev = nullptr);
+                           int ts, float* out, void* ws, cudaStream_t st, const int* T_dev = nullptr,
+                           bool pdl = false);
 nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
                              float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st,
-                             const int* pos_dev = nullptr);
+                             const int* pos_dev = nullptr, bool pdl = false);
 nt_status launch_rmsnorm(const float* x, const float* gamma, int B, int D, float eps, float* y, cudaStream_t st);
 
 // Tensor-core ternary GEMM (tcgen05, bf16 operands, exact fp32 accumulation) for

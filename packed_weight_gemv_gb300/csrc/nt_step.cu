@@ -117,11 +117,15 @@ nt_status validate_desc(const nt_decode_desc* d) {
   return NT_OK;
 }
 
-// Issues the per-stage launches of one step on `st` (stream and graph launchers).
+// Issues the per-stage launches of one step on `st` (stream and graph launchers). Every launch
+// but the output projection's is a programmatic dependent launch: the kernel is scheduled while
+// its predecessor finishes and waits for it before its first memory access.
 nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
+  constexpr bool pdl = true;
   if (p->embed_T)
-    NT_TRY(launch_embed(p->embed_T, p->embed_s, p->embed_V, p->embed_K, p->tokens, p->B, p->embed_x, nullptr, st));
-  if (p->n_qjobs) NT_TRY(launch_quantize_jobs(p->d_qjobs, p->n_qjobs, p->B, st));
+    NT_TRY(launch_embed(p->embed_T, p->embed_s, p->embed_V, p->embed_K, p->tokens, p->B, p->embed_x, nullptr, st,
+                        pdl));
+  if (p->n_qjobs) NT_TRY(launch_quantize_jobs(p->d_qjobs, p->n_qjobs, p->B, st, pdl));
   const bool chained = p->mode == NT_STEP_CHAINED;
   for (size_t i = 0; i < p->stages.size(); ++i) {
     const PlanStage& s = p->stages[i];
@@ -129,19 +133,20 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
       const int l = (int)(i / 4);
       const MatDesc* m = p->mats.data() + l * kProjPerLayer;
       NT_TRY(launch_rope_append(m[0].y, m[1].y, m[2].y, p->B, p->Hq, p->Hkv, 0, p->rope_base, p->d_qrot,
-                                p->k_cache[l], p->v_cache[l], p->t_stride, st, p->d_pos));
+                                p->k_cache[l], p->v_cache[l], p->t_stride, st, p->d_pos, pdl));
       NT_TRY(launch_attention(p->d_qrot, p->k_cache[l], p->v_cache[l], p->B, p->Hq, p->Hkv, p->t_stride, p->t_stride,
-                              p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1));
+                              p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1, pdl));
     }
-    if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st));
+    if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st, pdl));
     NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
-                                   s.total_tiles, p->B, st));
+                                   s.total_tiles, p->B, st, pdl));
   }
-  if (p->has_head && chained) NT_TRY(launch_chain_quant(p->d_cjobs + p->stages.size(), p->B, st));
+  if (p->has_head && chained) NT_TRY(launch_chain_quant(p->d_cjobs + p->stages.size(), p->B, st, pdl));
   if (p->has_head)
     NT_TRY(launch_head(p->head_T, p->head_s, p->head_V, p->head_K, p->head_q, p->head_sx, p->B,
                        p->head_logits, p->head_argmax, p->d_head_ws, st));
-  if (p->verify_emit) NT_TRY(launch_verify(p->verify_draft, p->head_argmax, p->B, p->verify_emit, p->verify_n, st));
+  if (p->verify_emit)
+    NT_TRY(launch_verify(p->verify_draft, p->head_argmax, p->B, p->verify_emit, p->verify_n, st, pdl));
   return NT_OK;
 }
 
