@@ -693,11 +693,6 @@ def run_layer_attention(args):
                    norm_final=gam[2 * L])
         # parity first: the first two layers as their own chained plan against the oracle
         L2 = min(2, L)
-        p2 = nt.DecodePlan(L2, 1, dp[:7 * L2], hd, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH,
-                           attention=dict(att, k_cache=kc[:L2], v_cache=vc[:L2], norm_attn=gam[:L2],
-                                          norm_ffn=gam[L:L + L2]))
-        p2.nt_decode_step(stream)
-        torch.cuda.synchronize()
         layers = []
         for l in range(L2):
             mats = []
@@ -705,30 +700,38 @@ def run_layer_attention(args):
                 full = wl.projection(wl.WL_DECODE, l, i, projs[7 * l + i].N, projs[7 * l + i].K)
                 mats.append((full.w_plain, full.s_w, full.N, full.K))
             layers.append(mats)
+        g_np = [g.cpu().numpy() for g in gam]
         kf = [lo.from_bf16_bits(kb).copy() for _ in range(L2)]
         vf = [lo.from_bf16_bits(vb).copy() for _ in range(L2)]
-        g_np = [g.cpu().numpy() for g in gam]
         want = oracle.decode_chained_attention(layers, wl.projection_x(wl.WL_DECODE, 0, 0, d, 1), (head.T, head.s_T, head.V, head.K),
                                                kf, vf, pos, g_np[:L2], g_np[L:L + L2], g_np[2 * L])
-        parity = "pass"
-        for i in range(7 * L2):
-            y = dp[i]["y"].cpu().numpy().reshape(1, -1).astype(np.float64)
-            if np.abs(y - want["y"][i]).max() > 2e-3 * np.abs(want["y"][i]).max():
-                parity = f"{projs[i].name} differs"
-        p2.close()
-        # restore the caches' new row for the timed plan (the two-layer plan rewrote it)
-        plan = nt.DecodePlan(L, 1, dp, hd, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH, attention=att)
-        for _ in range(max(3, args.warmup)):
-            plan.nt_decode_step(stream)
-        steps = max(3, min(args.steps, 100))
-        us = time_steps(torch, plan, steps, stream) / steps
+        line = {"metric": "chained decode with attention", "context": T, "layers": L}
         kv = L * 2 * Hkv * T * 128 * 2
-        print(json.dumps({"metric": "chained decode with attention (graph launcher)", "context": T,
-                          "layers": L, "steps": steps, "us_per_token": round(us, 2),
-                          "weight_bytes": step_bytes(n_layers=L), "cache_bytes": kv,
+        for name, launcher, launches in (("persistent", nt.NT_LAUNCH_PERSISTENT, 3 * L + 1),
+                                         ("graph", nt.NT_LAUNCH_GRAPH, L * 12 + 2)):
+            p2 = nt.DecodePlan(L2, 1, dp[:7 * L2], hd, nt.NT_STEP_CHAINED, launcher,
+                               attention=dict(att, k_cache=kc[:L2], v_cache=vc[:L2], norm_attn=gam[:L2],
+                                              norm_ffn=gam[L:L + L2]))
+            p2.nt_decode_step(stream)
+            torch.cuda.synchronize()
+            parity = "pass"
+            for i in range(7 * L2):
+                y = dp[i]["y"].cpu().numpy().reshape(1, -1).astype(np.float64)
+                if np.abs(y - want["y"][i]).max() > 2e-3 * np.abs(want["y"][i]).max():
+                    parity = f"{projs[i].name} differs"
+            p2.close()
+            # the caches' row at pos is rewritten by every step with the same values
+            plan = nt.DecodePlan(L, 1, dp, hd, nt.NT_STEP_CHAINED, launcher, attention=att)
+            for _ in range(max(3, args.warmup)):
+                plan.nt_decode_step(stream)
+            steps = max(3, min(args.steps, 100))
+            us = time_steps(torch, plan, steps, stream) / steps
+            line[name] = {"us_per_token": round(us, 2), "launches_per_token": launches,
                           "GBps_weights_plus_cache": round((step_bytes(n_layers=L) + kv) / (us * 1e-6) / 1e9, 1),
-                          "launches_per_token": L * 12 + 2, "parity_first_two_layers": parity}), flush=True)
-        plan.close()
+                          "parity_first_two_layers": parity}
+            plan.close()
+        line.update(steps=steps, weight_bytes=step_bytes(n_layers=L), cache_bytes=kv)
+        print(json.dumps(line), flush=True)
         del kc, vc
         torch.cuda.empty_cache()
 

@@ -260,7 +260,8 @@ nt_status nt_attention_decode(const float* q, const uint16_t* k_cache, const uin
 
 /* Rotary embedding of B new positions pos0 .. pos0 + B - 1 and their append to the cache.
  * Rotate-half pairing (dimension i with i + D/2) by the angle pos * base^(-2i/D), the angles
- * formed in double precision, the rotations in fp32. q_out[b][h] = rotated q[b][h] (fp32);
+ * formed and reduced modulo 2 pi in double precision, their sine and cosine and the rotations
+ * in fp32. q_out[b][h] = rotated q[b][h] (fp32);
  * k_cache[g][pos0 + b] = bf16(rotated k_new[b][g]); v_cache[g][pos0 + b] = bf16(v_new[b][g])
  * (round to nearest even). q [B][Hq][D], k_new / v_new [B][Hkv][D] fp32; base > 1 (10000 is
  * the textbook value); pos0 + B <= t_stride. q_out may alias q. */
@@ -358,8 +359,11 @@ typedef struct nt_decode_desc {
   int32_t* verify_n;            /* [1] number of emitted tokens */
   int head_dim;                 /* NT_STEP_CHAINED: dimensions per attention head, a multiple of
                                    4 (0 selects 128, "At 26K tokens ...": 128 per head) */
-  /* NT_STEP_CHAINED with the layer's attention side (attn_k_cache != NULL; stream and graph
-     launchers -- the persistent launcher returns NT_ERR_UNSUPPORTED; head_dim must be 128).
+  /* NT_STEP_CHAINED with the layer's attention side (attn_k_cache != NULL; head_dim must be
+     128). The persistent launcher runs one cooperative launch per segment of stages between
+     two attention sides ({q,k,v} of layer 0; then {o},{gate,up},{down} of layer l with
+     {q,k,v} of layer l + 1; the last segment ends with the output projection), the rotation,
+     cache append and attention launches in between: 3 launches per layer.
      Per layer, with the step's B vectors at positions pos .. pos + B - 1:
        {q,k,v} <- Q(rmsnorm(h) * norm_attn[l]);
        q, k rotated (nt_rope_append); k, v appended to the layer's cache at rows pos ..;

@@ -485,8 +485,9 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
 
 
 // Rotary embedding of position pos0 + blockIdx.x: the angles pos * base^(-2i/D) are formed
-// and reduced in double precision (a float angle of a large position would carry an error of
-// about pos * 2^-24 radians), the rotations in fp32 without contraction. Keys and values go
+// and reduced modulo 2 pi in double precision (a float angle of a large position would carry an
+// error of about pos * 2^-24 radians), their sine and cosine taken in fp32, the rotations in fp32
+// without contraction. Keys and values go
 // to the cache rows pos0 + b as bf16 (round to nearest even); queries to q_out in fp32.
 __global__ void rope_append_kernel(const float* __restrict__ q, const float* __restrict__ k,
                                    const float* __restrict__ v, int Hq, int Hkv, int pos0_arg, const int* pos_dev,
@@ -499,9 +500,16 @@ __global__ void rope_append_kernel(const float* __restrict__ q, const float* __r
   const int b = blockIdx.x, pos = pos0 + b;
   constexpr int half = kAttnD / 2;
   if (threadIdx.x < half) {
+    // the angle in double, reduced to [-pi, pi] in double (one fused multiply-add by the
+    // double nearest 2 pi: the reduction error is below 1e-11 rad for positions up to 10^6),
+    // then sine and cosine in fp32 (FP64 transcendentals are slow on this part)
     const double ang = (double)pos * exp2(-2.0 * threadIdx.x / kAttnD * log2_base);
-    cs[threadIdx.x] = (float)cos(ang);
-    sn[threadIdx.x] = (float)sin(ang);
+    const double two_pi = 6.283185307179586;
+    const float red = (float)fma(-rint(ang / two_pi), two_pi, ang);
+    float sv, cv;
+    sincosf(red, &sv, &cv);
+    cs[threadIdx.x] = cv;
+    sn[threadIdx.x] = sv;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {

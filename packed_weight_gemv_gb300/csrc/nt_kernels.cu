@@ -85,29 +85,31 @@ __global__ void __launch_bounds__(kThreads) quantize_jobs_kernel(const QuantJob*
 // thread rewrites only the elements it read), then the codes to every recorded q.
 __global__ void __launch_bounds__(kChainThreads) chain_quant_kernel(const ChainJob* __restrict__ jobs) {
   __shared__ float red[kChainWarps];
-  __shared__ double redd[kChainWarps];
+  __shared__ float s_r;
   dependent_launch_wait();
   const ChainJob j = *jobs;
   const int b = blockIdx.x, K = j.src.K;
   float* vb = j.vbuf + (int64_t)b * K;
-  float m = 0.0f;
-  double ss = 0.0;
+  float m = 0.0f, sf = 0.0f;
   for (int k = 4 * threadIdx.x; k < K; k += 4 * kChainThreads) {
     const float4 v = chain_load4(j.src, b, k);
     *reinterpret_cast<float4*>(vb + k) = v;
     m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
-    ss += (double)v.x * v.x + (double)v.y * v.y + (double)v.z * v.z + (double)v.w * v.w;
+    sf = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, sf))));  // a few squares in fp32
   }
   float r = 1.0f;
   if (j.src.gamma) {  // RMS normalisation: the absmax is taken over the normalised values
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if ((threadIdx.x & 31) == 0) redd[threadIdx.x >> 5] = ss;
+    for (int o = 16; o > 0; o >>= 1) sf += __shfl_xor_sync(0xffffffffu, sf, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sf;
     __syncthreads();
-    double t = 0.0;
-#pragma unroll
-    for (int i = 0; i < kChainWarps; ++i) t += redd[i];
-    r = (float)(1.0 / sqrt(t / K + (double)j.src.eps));
+    if (threadIdx.x == 0) {  // the warps' sums added and r formed in double by one thread
+      double t = 0.0;
+      for (int i = 0; i < kChainWarps; ++i) t += red[i];
+      s_r = (float)(1.0 / sqrt(t / K + (double)j.src.eps));
+    }
+    __syncthreads();  // s_r visible; red[] is reused for the maximum
+    r = s_r;
     m = 0.0f;
     for (int k = 4 * threadIdx.x; k < K; k += 4 * kChainThreads) {
       const float4 v = *reinterpret_cast<const float4*>(vb + k);

@@ -20,8 +20,9 @@ struct QuantJob {
 //   kChainProduct  fl(in0[b][k] * in1[b][k])
 //   kChainSum      fl(in0[b][k] + in1[b][k])
 //   kChainSiluProduct fl(silu(in0[b][k]) * in1[b][k]), silu(x) = x / (1 + exp(-x)) in fp32
-// With gamma set (stream / graph launchers), the quantized vector is the RMS-normalised
-// fl(fl(v * r) * gamma[k]), r = fl32(1 / sqrt(mean(v^2) + eps)) formed in double.
+// With gamma set, the quantized vector is the RMS-normalised fl(fl(v * r) * gamma[k]),
+// r = fl32(1 / sqrt(mean(v^2) + eps)): the squares summed in fp32 within each warp, the warps'
+// sums added and r formed in double by one thread.
 enum : int { kChainNone = 0, kChainDirect = 1, kChainHeads = 2, kChainProduct = 3, kChainSum = 4,
              kChainSiluProduct = 5 };
 struct ChainSrc {

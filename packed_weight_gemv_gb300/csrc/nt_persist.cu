@@ -83,7 +83,7 @@ struct PersistParams {
   int chunk_b;   // vectors per pass (<= kChunkBatch)
   int nslots;    // ring slots per consumer warp (<= kMaxSlots)
   int act_k;     // bytes per activation vector in shared memory
-  uint32_t launch_idx;
+  uint32_t barrier_base;    // grid-barrier arrivals of all earlier launches on this plan (mod 2^32)
   uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
   uint64_t timeout_ns;
   unsigned long long* trace;  // optional timeline: [grid][n_barriers + 1][4]
@@ -119,7 +119,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int a
   L.bars = L.act + 2 * chunk_b * act_k;
   L.hbest = L.bars + 2 * C::BARS * 8;
   L.red = L.hbest + C::CW * kStepMaxBatch * (int)sizeof(HeadPartial);
-  L.abort_flag = L.red + C::CW * 4;
+  L.abort_flag = L.red + C::CW * 4 + (C::CHAINED ? 16 : 0);  // chained: the norm factor after the warps' values
   L.chain_s = L.abort_flag + 16;
   L.total = L.chain_s + kStepMaxBatch * 4;
   return L;
@@ -402,10 +402,41 @@ template <class C>
 __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, uint8_t* abuf, float* s_chain,
                                float* red, bool record, const MatDesc* rec, int n_rec, int8_t* hq, float* hs) {
   const int t = threadIdx.x;
+  // the value quantized at k: the stage input, RMS-normalised with gamma when the source has
+  // one (fl(fl(v * r) * gamma[k]), r = fl32(1 / sqrt(mean(v^2) + eps)): the squares summed in
+  // fp32 within each warp, the warps' sums added and r formed in double by one thread)
+  auto value4 = [&](int b, int k, float r) {
+    float4 v = chain_load4(cs, b, k);
+    if (cs.gamma) {
+      const float4 g = __ldg(reinterpret_cast<const float4*>(cs.gamma + k));
+      v = make_float4(__fmul_rn(__fmul_rn(v.x, r), g.x), __fmul_rn(__fmul_rn(v.y, r), g.y),
+                      __fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
+    }
+    return v;
+  };
   for (int b = 0; b < nb; ++b) {
+    float r = 1.0f;
+    if (cs.gamma) {
+      float sf = 0.0f;  // this thread's few squares in fp32 (FP64 is slow on this part)
+      for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
+        const float4 v = chain_load4(cs, b0 + b, k);
+        sf = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, sf))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sf += __shfl_xor_sync(0xffffffffu, sf, o);
+      if ((t & 31) == 0) red[t >> 5] = sf;
+      consumer_sync<C>();
+      if (t == 0) {  // the warps' sums added in double by one thread; r broadcast in red[CW]
+        double tot = 0.0;
+        for (int i = 0; i < C::CW; ++i) tot += red[i];
+        red[C::CW] = (float)(1.0 / sqrt(tot / cs.K + (double)cs.eps));
+      }
+      consumer_sync<C>();
+      r = red[C::CW];
+    }
     float m = 0.0f;
     for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
-      const float4 v = chain_load4(cs, b0 + b, k);
+      const float4 v = value4(b0 + b, k, r);
       m = fmaxf(fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
     }
 #pragma unroll
@@ -418,7 +449,7 @@ __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, ui
     const bool nz = m != 0.0f;
     const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
     for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
-      const uint32_t c = quant4(chain_load4(cs, b0 + b, k), s, nz);
+      const uint32_t c = quant4(value4(b0 + b, k, r), s, nz);
       *reinterpret_cast<uint32_t*>(abuf + b * act_k + k) = c;
       if (record) {
         const int64_t o = (int64_t)(b0 + b) * cs.K + k;
@@ -654,7 +685,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   Ring rg{ring + cw * P.nslots * kSlotBytes, full0 + 8u * cw * kMaxSlots, empty0 + 8u * cw * kMaxSlots,
           0u, 0u, P.nslots};
   HeadPartial* wbest = hbest + cw * kStepMaxBatch;
-  const uint32_t barrier_base = P.launch_idx * (uint32_t)P.n_barriers * gridDim.x;
+  const uint32_t barrier_base = P.barrier_base;
   uint32_t barriers = 0, seq = 0;
 
   if (P.embed_T) {  // input-table rows of the step's tokens; quantization may read them
@@ -888,6 +919,9 @@ nt_status persist_prepare(nt_decode_plan* p) {
   p->grid = grid;
 
   std::vector<std::vector<WorkItem>> per_cta(grid);
+  std::vector<std::vector<std::vector<WorkItem>>> seg_cta;  // segmented plans
+  p->seg_barriers.clear();
+  p->seg_off_bytes.clear();
   const int n_proj = (int)p->mats.size();
   auto ternary = [&](int mi) {
     return Unitset{kItemTernary, mi, padded_rows(p->mats[mi].N) / 4, padded_k(p->mats[mi].K)};
@@ -903,6 +937,35 @@ nt_status persist_prepare(nt_decode_plan* p) {
       for (int i = 0; i < n_proj; ++i) all.push_back(ternary(i));
       partition_stage(all, grid, b0, false, per_cta);
       if (p->has_head) partition_stage({head}, grid, b0, false, per_cta);
+    }
+  } else if (chained && p->attn) {
+    // one launch per segment; the attention side runs between segments
+    const int L = p->n_layers;
+    auto stage_into = [&](std::vector<std::vector<WorkItem>>& pc, bool& first, int& nbar,
+                          const std::vector<Unitset>& sets) {
+      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) partition_stage(sets, grid, b0, !first && b0 == 0, pc);
+      nbar += first ? 0 : 1;
+      first = false;
+    };
+    for (int sg = 0; sg <= L; ++sg) {
+      std::vector<std::vector<WorkItem>> pc(grid);
+      bool first = true;
+      int nbar = sg == 0 ? barriers : 0;  // the first segment also gathers / quantizes the inputs
+      if (sg > 0) {
+        const int b = (sg - 1) * kProjPerLayer;
+        stage_into(pc, first, nbar, {ternary(b + 3)});
+        stage_into(pc, first, nbar, {ternary(b + 4), ternary(b + 5)});
+        stage_into(pc, first, nbar, {ternary(b + 6)});
+      }
+      if (sg < L) {
+        const int b = sg * kProjPerLayer;
+        stage_into(pc, first, nbar, {ternary(b), ternary(b + 1), ternary(b + 2)});
+      } else if (p->has_head) {
+        stage_into(pc, first, nbar, {head});
+      }
+      seg_cta.push_back(std::move(pc));
+      p->seg_barriers.push_back(nbar);
+      barriers = std::max(barriers, nbar);
     }
   } else {
     bool first = true;
@@ -925,19 +988,27 @@ nt_status persist_prepare(nt_decode_plan* p) {
   }
   p->n_barriers = barriers;
 
+  // every segment's per-CTA items, then each segment's (grid + 1) offsets into the items
+  std::vector<std::vector<std::vector<WorkItem>>> segs;
+  if (p->seg_barriers.empty()) segs.push_back(std::move(per_cta));
+  else segs = std::move(seg_cta);
   std::vector<WorkItem> items;
-  std::vector<int> off(grid + 1, 0);
-  for (int c = 0; c < grid; ++c) {
-    off[c] = (int)items.size();
-    items.insert(items.end(), per_cta[c].begin(), per_cta[c].end());
+  std::vector<int> off;
+  for (const auto& pc : segs) {
+    for (int c = 0; c < grid; ++c) {
+      off.push_back((int)items.size());
+      items.insert(items.end(), pc[c].begin(), pc[c].end());
+    }
+    off.push_back((int)items.size());
   }
-  off[grid] = (int)items.size();
   const size_t item_bytes = sizeof(WorkItem) * std::max<size_t>(items.size(), 1);
   NT_CUDA_TRY(cudaMalloc(&p->d_sched, item_bytes + sizeof(int) * off.size()));
   if (!items.empty()) NT_CUDA_TRY(cudaMemcpy(p->d_sched, items.data(), sizeof(WorkItem) * items.size(), cudaMemcpyHostToDevice));
   NT_CUDA_TRY(cudaMemcpy(reinterpret_cast<uint8_t*>(p->d_sched) + item_bytes, off.data(), sizeof(int) * off.size(),
                          cudaMemcpyHostToDevice));
   p->sched_item_bytes = item_bytes;
+  for (size_t s = 0; s < p->seg_barriers.size(); ++s)
+    p->seg_off_bytes.push_back(item_bytes + sizeof(int) * (grid + 1) * s);
   return NT_OK;
 }
 
@@ -964,7 +1035,6 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.chunk_b = p->chunk_b;
   P.nslots = p->nslots;
   P.act_k = p->act_stride;
-  P.launch_idx = (uint32_t)p->launches;
   P.barrier_extra = p->test_fault == 1 ? 1u : 0u;
   P.timeout_ns = p->timeout_ns;
   P.trace = p->trace;
@@ -978,13 +1048,46 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.verify_emit = p->verify_emit;
   P.verify_n = p->verify_n;
   P.head_src = p->head_src;
-  void* args[] = {&P};
   int threads = 0;
   const void* kern = kernel_for(p->B, p->mode == NT_STEP_CHAINED, &threads);
-  const cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p->grid), dim3(threads), args, p->smem_bytes, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return set_error(NT_ERR_CUDA, std::string("persistent launch: ") + cudaGetErrorString(e));
+  auto launch = [&](int n_barriers) -> nt_status {
+    P.n_barriers = n_barriers;
+    P.barrier_base = p->barrier_count * (uint32_t)p->grid;
+    void* args[] = {&P};
+    const cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p->grid), dim3(threads), args, p->smem_bytes, st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return set_error(NT_ERR_CUDA, std::string("persistent launch: ") + cudaGetErrorString(e));
+    }
+    p->barrier_count += (uint32_t)n_barriers;
+    return NT_OK;
+  };
+  if (p->seg_barriers.empty()) {
+    NT_TRY(launch(p->n_barriers));
+  } else {
+    // one launch per segment, the layer's rotation, cache append and attention in between;
+    // input gathering and quantization belong to the first segment, the output projection
+    // (and the verify acceptance) to the last
+    const int nseg = (int)p->seg_barriers.size();
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(p->d_sched);
+    P.trace = nullptr;
+    for (int sg = 0; sg < nseg; ++sg) {
+      const bool last = sg == nseg - 1;
+      P.item_off = reinterpret_cast<const int*>(base + p->seg_off_bytes[sg]);
+      P.n_qjobs = sg == 0 ? p->n_qjobs : 0;
+      P.embed_T = sg == 0 ? p->embed_T : nullptr;
+      P.has_head = last && p->has_head ? 1 : 0;
+      P.verify_emit = last ? p->verify_emit : nullptr;
+      NT_TRY(launch(p->seg_barriers[sg]));
+      if (!last) {
+        const int l = sg;
+        const MatDesc* m = p->mats.data() + l * kProjPerLayer;
+        NT_TRY(launch_rope_append(m[0].y, m[1].y, m[2].y, p->B, p->Hq, p->Hkv, 0, p->rope_base, p->d_qrot,
+                                  p->k_cache[l], p->v_cache[l], p->t_stride, st, p->d_pos, true));
+        NT_TRY(launch_attention(p->d_qrot, p->k_cache[l], p->v_cache[l], p->B, p->Hq, p->Hkv, p->t_stride,
+                                p->t_stride, p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1, true));
+      }
+    }
   }
   ++p->launches;
   return NT_OK;

@@ -43,8 +43,6 @@ nt_status validate_chain(const nt_decode_desc* d) {
   if (!aligned(d->proj[0].x, 16)) return set_error(NT_ERR_ALIGNMENT, "chained: proj[0].x must be 16-byte aligned");
   if (d->head_T && d->head_K != dm) return set_error(NT_ERR_INVALID_ARG, "chained: head_K must equal proj[0].K");
   if (d->attn_k_cache) {  // the attention side
-    if (d->launcher == NT_LAUNCH_PERSISTENT)
-      return set_error(NT_ERR_UNSUPPORTED, "chained steps with attention run on the stream or graph launcher");
     if (hd != 128) return set_error(NT_ERR_UNSUPPORTED, "chained steps with attention need head_dim 128");
     const int Hq = d->proj[0].N / 128, Hkv = d->proj[1].N / 128;
     if (d->proj[0].N % 128 || d->proj[1].N % 128 || Hkv < 1 || Hq % Hkv != 0)
@@ -340,6 +338,11 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
       if (p->attn) {
         const float* ga = d->norm_attn ? d->norm_attn[l] : nullptr;
         const float* gf = d->norm_ffn ? d->norm_ffn[l] : nullptr;
+        // persistent launcher: normalised inputs, the attention output for o, the SiLU gate
+        for (int i = 0; i < 3; ++i) m[i].src = normed(ChainSrc{h, nullptr, kChainDirect, dm, 1, hd}, ga);
+        m[3].src = ChainSrc{p->d_attn_out, nullptr, kChainDirect, m[3].K, 1, hd};
+        for (int i = 4; i < 6; ++i) m[i].src = normed(ChainSrc{R, nullptr, kChainDirect, dm, 1, hd}, gf);
+        m[6].src = ChainSrc{m[4].y, m[5].y, kChainSiluProduct, m[6].K, 1, hd};
         if (l == 0) job(normed(ChainSrc{x0, nullptr, kChainDirect, dm, 1, hd}, ga), R, b, 3);
         else job(normed(ChainSrc{R, mats[b - 1].y, kChainSum, dm, 1, hd}, ga), R, b, 3);
         job(ChainSrc{p->d_attn_out, nullptr, kChainDirect, m[3].K, 1, hd}, p->d_chain_tmp, b + 3, 1);
@@ -354,6 +357,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
       job(m[6].src, p->d_chain_tmp, b + 6, 1);
     }
     p->head_src = ChainSrc{R, nullptr, kChainDirect, dm, 1, hd};
+    if (p->attn) p->head_src = normed(p->head_src, d->norm_final);
     if (p->has_head) {
       ChainJob j{};
       j.src = ChainSrc{R, mats[n_proj - 1].y, kChainSum, dm, 1, hd};
@@ -457,6 +461,7 @@ nt_status nt_decode_plan_reset(nt_decode_plan* p) {
   NT_CUDA_TRY(cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl)));
   if (p->d_head_ws) NT_CUDA_TRY(cudaMemset(p->d_head_ws, 0, head_ws_bytes(p->B)));
   p->launches = 0;
+  p->barrier_count = 0;
   NT_CUDA_TRY(cudaDeviceSynchronize());
   return NT_OK;
 }

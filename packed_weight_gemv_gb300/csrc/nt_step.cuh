@@ -79,6 +79,12 @@ struct nt_decode_plan {
   int act_stride = 0;               // bytes of one activation vector in shared memory
   int nslots = 0, chunk_b = 0;      // ring slots per consumer warp; vectors per pass
   uint64_t launches = 0;
+  uint32_t barrier_count = 0;       // grid barriers passed by all launches so far (mod 2^32)
+  // chained plans with the attention side: one persistent launch per segment (the stages
+  // between two attention sides: [A_0], [B_l C_l D_l A_l+1] ..., [B_L-1 C_L-1 D_L-1 head]),
+  // each with its own grid barriers and per-CTA item offsets in d_sched
+  std::vector<int> seg_barriers;
+  std::vector<size_t> seg_off_bytes;
   unsigned long long* trace = nullptr;  // optional step timeline (nt_decode_plan_set_trace)
   // chained steps (NT_STEP_CHAINED)
   int head_dim = 128;

@@ -1,6 +1,7 @@
 """GPU parity of chained steps with the attention side (RMS norms, rotary embedding and
 cache append, attention over the cache, SiLU gate) against the oracle's float64 layer on the
-same seeded inputs, on the stream and graph launchers.
+same seeded inputs, on the stream, graph and persistent launchers (the persistent launcher runs
+one cooperative launch per segment of stages between two attention sides).
 
 The kernels compute norms, rotations, attention and SiLU in fp32 where the oracle uses float64,
 so a value that lies within a rounding step of an int8 boundary can quantize one code apart.
@@ -43,7 +44,7 @@ def close(got, want, what, rel=2e-3):
     assert err <= rel * scale, f"{what}: max error {err:.3g} vs {rel * scale:.3g}"
 
 
-@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_STREAM, nt.NT_LAUNCH_GRAPH])
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_STREAM, nt.NT_LAUNCH_GRAPH, nt.NT_LAUNCH_PERSISTENT])
 @pytest.mark.parametrize("B,pos,norms", [(1, 0, True), (1, 300, True), (3, 130, True), (2, 64, False)])
 def test_chained_attention_step(launcher, B, pos, norms):
     L, Hkv, ts = 2, 2, 512
@@ -88,23 +89,24 @@ def test_chained_attention_step(launcher, B, pos, norms):
     plan.close()
 
 
-def test_chained_attention_position_advances_and_persistent_is_refused():
-    L, B, Hkv, ts = 1, 1, 2, 256
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_GRAPH, nt.NT_LAUNCH_PERSISTENT])
+def test_chained_attention_position_advances(launcher):
+    L, B, Hkv, ts = 2, 1, 2, 256
     projs = wl.decoder_projections(L, SHAPES, B=B, seed=44, workload=41)
     dp, _ = plan_inputs(projs, None, B=B)
-    kc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV)]
-    vc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV)]
+    kc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV) for _ in range(L)]
+    vc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV) for _ in range(L)]
     att = dict(k_cache=kc, v_cache=vc, t_stride=ts, pos=0)
-    with pytest.raises(nt.NtError) as ei:
-        nt.DecodePlan(L, B, dp, None, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_PERSISTENT, attention=att)
-    assert ei.value.status == nt.NT_ERR_UNSUPPORTED
-    plan = nt.DecodePlan(L, B, dp, None, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_GRAPH, attention=att)
-    for p in range(3):  # three tokens: rows 0, 1, 2 of the cache fill in order
+    plan = nt.DecodePlan(L, B, dp, None, nt.NT_STEP_CHAINED, launcher, attention=att)
+    for p in range(3):  # three tokens: rows 0, 1, 2 of every layer's cache fill in order
         plan.nt_decode_plan_set_position(p)
         plan.nt_decode_step()
     torch.cuda.synchronize()
-    rows = host(kc[0]).view(np.uint16)
-    assert rows[:, :3].any(axis=(0, 2)).all() and not rows[:, 3:].any()
+    for l in range(L):
+        rows = host(kc[l]).view(np.uint16)
+        assert rows[:, :3].any(axis=(0, 2)).all() and not rows[:, 3:].any()
+    if launcher == nt.NT_LAUNCH_PERSISTENT:
+        assert plan.nt_decode_step_status() == nt.NT_OK
     with pytest.raises(nt.NtError):
         plan.nt_decode_plan_set_position(ts)
     plan.close()
