@@ -341,11 +341,68 @@ def run_ours(args, rank, world):
         if pl.nt_decode_step_status() != nt.NT_OK:
             raise RuntimeError(f"{name}: step reported a timeout")
         pl.close()
+    # Components of the step, each timed alone (CUDA events, inputs larger than L2): the ternary
+    # weight stream without the output projection, the output projection on its own (the
+    # standalone call), and the offline repack of the largest matrix shape.
+    peak, peak_kind = measured_peak()
+    comp = {}
+
+    def frac(nbytes_, us_):
+        gbs = nbytes_ / (us_ * 1e-6) / 1e9
+        return {"us": round(us_, 2), "bytes": int(nbytes_), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    pl = nt.DecodePlan(L, 1, dp, None, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+    for _ in range(3):
+        pl.nt_decode_step(stream)
+    us_stream = time_steps(torch, pl, n_extra, stream) / n_extra
+    if pl.nt_decode_step_status() != nt.NT_OK:
+        raise RuntimeError("weight stream: step reported a timeout")
+    pl.close()
+    stream_bytes = wl.packed_bytes_per_token(n_layers=L) + 4 * sum(p.K for p in projs)
+    comp["weight_stream"] = dict(frac(stream_bytes, us_stream), kernel="persist_kernel",
+                                 what=f"{L} layers x 7 ternary projections, inputs quantized in the step")
+    hws = torch.empty(nt.nt_int8_logits_workspace_size(head.V, head.K, 1), dtype=torch.uint8, device=dev)
+    nt.nt_quantize_act(hd["x"], hd["q"], hd["sx"], stream)
+
+    def head_call():
+        nt.nt_int8_logits_argmax(hd["T"], hd["s"], head.V, head.K, hd["q"], hd["sx"], 1, hd["logits"],
+                                 hd["argmax"], hws, stream)
+
+    for _ in range(3):
+        head_call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_extra):
+        head_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    comp["lm_head"] = dict(frac(wl.head_bytes(B=1), e0.elapsed_time(e1) * 1e3 / n_extra),
+                           kernel="persist_kernel (implicit schedule)",
+                           what=f"int8 table {head.V}x{head.K}, fp32 logits, greedy arg-max")
+    rN, rK = wl.DECODER_8B["gate"]
+    r1 = torch.randint(-2 ** 31, 2 ** 31 - 1, (rN * rK // 16,), dtype=torch.int32, device=dev)
+    r2 = torch.randint(-2 ** 31, 2 ** 31 - 1, (rN * rK // 16,), dtype=torch.int32, device=dev)
+    low = r1 & 0x55555555
+    w_plain = low | ((low & r2) << 1)  # fields 00 / 01 / 11 only (no invalid 10)
+    del r1, r2, low
+    w_t = torch.empty(nt.nt_repack_size(rN, rK), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        nt.nt_repack_ternary(w_plain, rN, rK, w_t, stream=stream)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(20):
+        nt.nt_repack_ternary(w_plain, rN, rK, w_t, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    comp["repack"] = dict(frac(2 * rN * rK // 4, e0.elapsed_time(e1) * 1e3 / 20), kernel="repack_kernel",
+                          what=f"plain -> tiled, {rN}x{rK} trits (read + write)")
+    del w_plain, w_t, hws
+
     plan.nt_decode_step(stream)  # chained plans rewrote the codes: requantize the supplied inputs
     torch.cuda.synchronize()
     parity_after = parity_gate(oracle, projs, head, dp, hd, layers=(L // 2,)) if rank == 0 else "pass"
 
-    peak, peak_kind = measured_peak()
     nbytes = step_bytes(n_layers=L)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     cpu = cpu_baseline(oracle) if (rank == 0 and world == 1) else None
@@ -379,6 +436,7 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "parity": parity if parity_after == "pass" else f"after timing: {parity_after}",
         "breakdown": extra,
+        "components": comp,
     }
     plan.close()
     if rank == 0:

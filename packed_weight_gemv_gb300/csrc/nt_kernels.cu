@@ -145,40 +145,56 @@ __global__ void __launch_bounds__(kChainThreads) chain_quant_kernel(const ChainJ
 
 // ---------------------------------------------------------------------------------------
 // Repack plain -> tiled. Word (row n, group g) of the tiled layout holds the same 16 trits
-// as plain word g of row n, re-coded as 8 pair codes; one thread per tiled word.
+// as plain word g of row n, re-coded as 8 pair codes. One thread per 16-byte tiled group (the
+// 4 rows of a tile at one group): its 4 plain reads are coalesced across the warp (consecutive
+// threads take consecutive groups of a row) and its 16-byte store too.
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ int plain_field_value(uint32_t w, int j) {
+// Pair code of trits (a, b), by index (a + 1) * 3 + (b + 1), one nibble each: 7, 2, 5, 14, 0,
+// 3, 6, 1, 4 (see the pools in nt_internal.cuh).
+constexpr uint64_t kPairCodes = 0x41630E527ull;
+
+// Index a + 1 of a plain field (00 -> 1, 01 -> 2, 11 -> 0; the invalid 10 reads as 0 -> 1).
+__device__ __forceinline__ uint32_t field_index(uint32_t w, int j) {
   const uint32_t c = (w >> (2 * j)) & 3u;
-  return c == 1u ? 1 : (c == 3u ? -1 : 0);
+  return c == 1u ? 2u : (c == 3u ? 0u : 1u);
 }
 
-// Pair code of (a, b), indexed by (a + 1) * 3 + (b + 1).
-__constant__ uint8_t kPairCode[9] = {7, 2, 5, 14, 0, 3, 6, 1, 4};
+__device__ __forceinline__ uint32_t tiled_word(uint32_t src) {
+  uint32_t word = 0;
+#pragma unroll
+  for (int i4 = 0; i4 < 4; ++i4) {
+    const uint32_t lo = (uint32_t)(kPairCodes >> (4 * (field_index(src, i4) * 3 + field_index(src, 4 + i4)))) & 15u;
+    const uint32_t hi = (uint32_t)(kPairCodes >> (4 * (field_index(src, 8 + i4) * 3 + field_index(src, 12 + i4)))) & 15u;
+    word |= lo << (4 * i4);
+    word |= hi << (4 * (4 + i4));
+  }
+  return word;
+}
 
 __global__ void __launch_bounds__(kThreads) repack_kernel(const uint32_t* __restrict__ w, int N,
                                                           int K, uint32_t* __restrict__ out,
                                                           uint32_t* __restrict__ n_invalid) {
-  const int64_t Np = padded_rows(N), groups = padded_k(K) / 16, kw = K / 16;
-  const int64_t total = Np * groups;  // tiled words
+  const int64_t groups = padded_k(K) / 16, kw = K / 16;
+  const int64_t total = padded_rows(N) / 4 * groups;  // tiled groups, in memory order
   unsigned int bad = 0;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    // i enumerates output words in memory order: tile, group, row-in-tile.
-    const int64_t tile = i / (groups * 4), rem = i % (groups * 4);
-    const int64_t g = rem / 4, n = tile * 4 + rem % 4;
-    uint32_t src = 0;
-    if (n < N && g < kw) src = w[n * kw + g];
-    uint32_t word = 0;
+    const int64_t tile = i / groups, g = i - tile * groups;
+    uint32_t src[4];
 #pragma unroll
-    for (int f = 0; f < 16; ++f) bad += ((src >> (2 * f)) & 3u) == 2u;
-#pragma unroll
-    for (int i4 = 0; i4 < 4; ++i4) {
-      const uint32_t lo = kPairCode[(plain_field_value(src, i4) + 1) * 3 + plain_field_value(src, 4 + i4) + 1];
-      const uint32_t hi = kPairCode[(plain_field_value(src, 8 + i4) + 1) * 3 + plain_field_value(src, 12 + i4) + 1];
-      word |= lo << (4 * i4);
-      word |= hi << (4 * (4 + i4));
+    for (int r = 0; r < 4; ++r) {
+      const int64_t n = tile * 4 + r;
+      src[r] = (n < N && g < kw) ? __ldg(w + n * kw + g) : 0u;
     }
-    out[i] = word;
+    uint4 o;
+    uint32_t* ow = &o.x;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+      for (int f = 0; f < 16; ++f) bad += ((src[r] >> (2 * f)) & 3u) == 2u;
+      ow[r] = tiled_word(src[r]);
+    }
+    reinterpret_cast<uint4*>(out)[i] = o;
   }
   if (n_invalid) {
     bad = __reduce_add_sync(0xffffffffu, bad);
@@ -423,7 +439,7 @@ nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st, bool
 
 nt_status launch_repack(const uint32_t* w, int N, int K, uint8_t* out, uint32_t* n_invalid,
                         cudaStream_t st) {
-  const int64_t total = padded_rows(N) * (padded_k(K) / 16);
+  const int64_t total = padded_rows(N) / 4 * (padded_k(K) / 16);  // one thread per 16-byte group
   int64_t g = (total + kThreads - 1) / kThreads;
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (g > cap) g = cap;
