@@ -484,55 +484,46 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
 }
 
 
-// Rotary embedding of position pos0 + blockIdx.x: the angles pos * base^(-2i/D) are formed
+// Rotary embedding of head blockIdx.x (query heads, then key-value heads) at position
+// pos0 + blockIdx.y, one thread per rotated pair: the angles pos * base^(-2i/D) are formed
 // and reduced modulo 2 pi in double precision (a float angle of a large position would carry an
 // error of about pos * 2^-24 radians), their sine and cosine taken in fp32, the rotations in fp32
-// without contraction. Keys and values go
-// to the cache rows pos0 + b as bf16 (round to nearest even); queries to q_out in fp32.
-__global__ void rope_append_kernel(const float* __restrict__ q, const float* __restrict__ k,
-                                   const float* __restrict__ v, int Hq, int Hkv, int pos0_arg, const int* pos_dev,
-                                   double log2_base,
-                                   float* __restrict__ q_out, uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
-                                   int ts) {
-  __shared__ float cs[kAttnD / 2], sn[kAttnD / 2];
+// without contraction. Keys and values go to the cache rows pos0 + b as bf16 (round to nearest
+// even); queries to q_out in fp32.
+__global__ void __launch_bounds__(kAttnD / 2) rope_append_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v, int Hq, int Hkv,
+    int pos0_arg, const int* pos_dev, double log2_base, float* __restrict__ q_out, uint16_t* __restrict__ kc,
+    uint16_t* __restrict__ vc, int ts) {
   dependent_launch_wait();
   const int pos0 = pos_dev ? *pos_dev : pos0_arg;
-  const int b = blockIdx.x, pos = pos0 + b;
+  const int hh = blockIdx.x, b = blockIdx.y, pos = pos0 + b, j = threadIdx.x;  // pair (j, j + D/2)
   constexpr int half = kAttnD / 2;
-  if (threadIdx.x < half) {
-    // the angle in double, reduced to [-pi, pi] in double (one fused multiply-add by the
-    // double nearest 2 pi: the reduction error is below 1e-11 rad for positions up to 10^6),
-    // then sine and cosine in fp32 (FP64 transcendentals are slow on this part)
-    const double ang = (double)pos * exp2(-2.0 * threadIdx.x / kAttnD * log2_base);
-    const double two_pi = 6.283185307179586;
-    const float red = (float)fma(-rint(ang / two_pi), two_pi, ang);
-    float sv, cv;
-    sincosf(red, &sv, &cv);
-    cs[threadIdx.x] = cv;
-    sn[threadIdx.x] = sv;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < (Hq + Hkv) * half; idx += blockDim.x) {
-    const int hh = idx / half, j = idx % half;
-    const bool isq = hh < Hq;
-    const float* x = isq ? q + ((int64_t)b * Hq + hh) * kAttnD : k + ((int64_t)b * Hkv + (hh - Hq)) * kAttnD;
-    const float lo = x[j], hi = x[j + half];
-    const float ylo = __fsub_rn(__fmul_rn(lo, cs[j]), __fmul_rn(hi, sn[j]));
-    const float yhi = __fadd_rn(__fmul_rn(hi, cs[j]), __fmul_rn(lo, sn[j]));
-    if (isq) {
-      float* y = q_out + ((int64_t)b * Hq + hh) * kAttnD;
-      y[j] = ylo;
-      y[j + half] = yhi;
-    } else {
-      uint16_t* row = kc + ((int64_t)(hh - Hq) * ts + pos) * kAttnD;
-      row[j] = __bfloat16_as_ushort(__float2bfloat16_rn(ylo));
-      row[j + half] = __bfloat16_as_ushort(__float2bfloat16_rn(yhi));
-    }
-  }
-  for (int idx = threadIdx.x; idx < Hkv * kAttnD; idx += blockDim.x) {
-    const int hh = idx / kAttnD, d = idx % kAttnD;
-    vc[((int64_t)hh * ts + pos) * kAttnD + d] =
-        __bfloat16_as_ushort(__float2bfloat16_rn(v[((int64_t)b * Hkv + hh) * kAttnD + d]));
+  // the angle in double, reduced to [-pi, pi] in double (one fused multiply-add by the double
+  // nearest 2 pi: the reduction error is below 1e-11 rad for positions up to 10^6), then sine
+  // and cosine in fp32 (FP64 transcendentals are slow on this part)
+  const double ang = (double)pos * exp2(-2.0 * j / kAttnD * log2_base);
+  const double two_pi = 6.283185307179586;
+  const float red = (float)fma(-rint(ang * (1.0 / two_pi)), two_pi, ang);
+  float sn, cs;
+  sincosf(red, &sn, &cs);
+  const bool isq = hh < Hq;
+  const float* x = isq ? q + ((int64_t)b * Hq + hh) * kAttnD : k + ((int64_t)b * Hkv + (hh - Hq)) * kAttnD;
+  const float lo = x[j], hi = x[j + half];
+  const float ylo = __fsub_rn(__fmul_rn(lo, cs), __fmul_rn(hi, sn));
+  const float yhi = __fadd_rn(__fmul_rn(hi, cs), __fmul_rn(lo, sn));
+  if (isq) {
+    float* y = q_out + ((int64_t)b * Hq + hh) * kAttnD;
+    y[j] = ylo;
+    y[j + half] = yhi;
+  } else {
+    const int g = hh - Hq;
+    uint16_t* row = kc + ((int64_t)g * ts + pos) * kAttnD;
+    row[j] = __bfloat16_as_ushort(__float2bfloat16_rn(ylo));
+    row[j + half] = __bfloat16_as_ushort(__float2bfloat16_rn(yhi));
+    const float* vr = v + ((int64_t)b * Hkv + g) * kAttnD;
+    uint16_t* vrow = vc + ((int64_t)g * ts + pos) * kAttnD;
+    vrow[j] = __bfloat16_as_ushort(__float2bfloat16_rn(vr[j]));
+    vrow[j + half] = __bfloat16_as_ushort(__float2bfloat16_rn(vr[j + half]));
   }
 }
 
@@ -611,8 +602,8 @@ nt_status launch_attention(const float* q, const uint16_t* kc, const uint16_t* v
 nt_status launch_rope_append(const float* q, const float* k, const float* v, int B, int Hq, int Hkv, int pos0,
                              float base, float* q_out, uint16_t* kc, uint16_t* vc, int ts, cudaStream_t st,
                              const int* pos_dev, bool pdl) {
-  NT_CUDA_TRY(launch_kernel(rope_append_kernel, dim3(B), dim3(256), 0, st, pdl, q, k, v, Hq, Hkv, pos0, pos_dev,
-                            log2((double)base), q_out, kc, vc, ts));
+  NT_CUDA_TRY(launch_kernel(rope_append_kernel, dim3(Hq + Hkv, B), dim3(kAttnD / 2), 0, st, pdl, q, k, v, Hq, Hkv,
+                            pos0, pos_dev, log2((double)base), q_out, kc, vc, ts));
   return check_launch("rope_append_kernel");
 }
 
@@ -659,8 +650,9 @@ nt_status nt_rope_append(const float* q, const float* k_new, const float* v_new,
   clear_error();
   if (!q || !k_new || !v_new || !q_out || !k_cache || !v_cache) return set_error(NT_ERR_INVALID_ARG, "NULL pointer");
   if (D != kAttnD) return set_error(NT_ERR_UNSUPPORTED, "head dimension must be 128");
-  if (B < 1 || Hq < 1 || Hkv < 1 || pos0 < 0 || pos0 + B > t_stride || !(base > 1.0f))
-    return set_error(NT_ERR_INVALID_ARG, "need B, Hq, Hkv >= 1, 0 <= pos0, pos0 + B <= t_stride and base > 1");
+  if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || pos0 < 0 || pos0 + B > t_stride || !(base > 1.0f))
+    return set_error(NT_ERR_INVALID_ARG,
+                     "need 1 <= B <= 65535, Hq, Hkv >= 1, 0 <= pos0, pos0 + B <= t_stride and base > 1");
   if (!aligned(q, 4) || !aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(q_out, 4) || !aligned(k_cache, 2) ||
       !aligned(v_cache, 2))
     return set_error(NT_ERR_ALIGNMENT, "misaligned pointer");
