@@ -255,7 +255,16 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
   __shared__ int s_last;
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x, lane = i & 31, w = i >> 5;
   const int g = lane >> 2, t = lane & 3, hl = g & 3;
-  dependent_launch_wait();
+  // In a dependent-launch chain the previous kernel appends the new positions' rows and rotates
+  // the queries; everything older (the cache rows before them, the cache length) was written by
+  // kernels that completed before this one could start. So the copies of steps that hold only
+  // older rows go out before the wait for the previous kernel, and the rest after it.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  bool waited = false;
+  auto wait_previous = [&]() {
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    waited = true;
+  };
   const int T = a.T_dev ? *a.T_dev : a.T;
   const int u0 = c * a.span, u1 = min(T, u0 + a.span);
   const uint16_t* kh = a.kc + (int64_t)h * a.ts * kAttnD;
@@ -286,10 +295,12 @@ __global__ void __launch_bounds__(kAttnThreads, attn_resident(G)) attn_unit_kern
       const int p = pw + k * kStride;
       const uint32_t n = used_steps + k, st = n % kAttnStages;
       if (ok && p < vis) {
+        if (p + kAttnStep > T - a.B) wait_previous();  // the step holds new rows (warp-uniform)
         attn_issue(kh, vh, p, vis, ring + st * kStageBytes, bar0 + 8u * st, pol, lane);
         ++issued_steps;
       }
     }
+    wait_previous();  // before the queries are read
     // Q fragments: lane (g, t) holds dimensions 32 i + 8 t .. + 7 (i = 0..3) of head hl of each
     // group; rows g and g + 8 of the MMA are terms (hi, lo) for g < 4, (mid, zero) for g >= 4.
     uint32_t qa[HG][8][4];
