@@ -414,6 +414,80 @@ __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, ui
     }
     return v;
   };
+  // Vectors of up to 4 * kPer * CT values (the model width) stay in registers: one pass of
+  // loads through L2, the reductions and the codes from the registers.
+  constexpr int kPer = 2;
+  if (cs.K <= 4 * kPer * C::CT) {
+    for (int b = 0; b < nb; ++b) {
+      float4 v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int k = 4 * t + 4 * C::CT * i;
+        v[i] = k < cs.K ? chain_load4(cs, b0 + b, k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (cs.gamma) {
+        float sf = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+          sf = fmaf(v[i].x, v[i].x, fmaf(v[i].y, v[i].y, fmaf(v[i].z, v[i].z, fmaf(v[i].w, v[i].w, sf))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sf += __shfl_xor_sync(0xffffffffu, sf, o);
+        if ((t & 31) == 0) red[t >> 5] = sf;
+        consumer_sync<C>();
+        if (t == 0) {  // the warps' sums added in double by one thread; r broadcast in red[CW]
+          double tot = 0.0;
+          for (int i = 0; i < C::CW; ++i) tot += red[i];
+          red[C::CW] = (float)(1.0 / sqrt(tot / cs.K + (double)cs.eps));
+        }
+        consumer_sync<C>();
+        const float r = red[C::CW];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int k = 4 * t + 4 * C::CT * i;
+          if (k < cs.K) {
+            const float4 g = __ldg(reinterpret_cast<const float4*>(cs.gamma + k));
+            v[i] = make_float4(__fmul_rn(__fmul_rn(v[i].x, r), g.x), __fmul_rn(__fmul_rn(v[i].y, r), g.y),
+                               __fmul_rn(__fmul_rn(v[i].z, r), g.z), __fmul_rn(__fmul_rn(v[i].w, r), g.w));
+          }
+        }
+      }
+      float m = 0.0f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        m = fmaxf(fmaxf(m, fmaxf(fabsf(v[i].x), fabsf(v[i].y))), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if ((t & 31) == 0) red[t >> 5] = m;
+      consumer_sync<C>();
+      m = red[0];
+#pragma unroll
+      for (int i = 1; i < C::CW; ++i) m = fmaxf(m, red[i]);
+      const bool nz = m != 0.0f;
+      const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int k = 4 * t + 4 * C::CT * i;
+        if (k < cs.K) {
+          const uint32_t c = quant4(v[i], s, nz);
+          *reinterpret_cast<uint32_t*>(abuf + b * act_k + k) = c;
+          if (record) {
+            const int64_t o = (int64_t)(b0 + b) * cs.K + k;
+            if (hq) *reinterpret_cast<uint32_t*>(hq + o) = c;
+            for (int rr = 0; rr < n_rec; ++rr) *reinterpret_cast<uint32_t*>(const_cast<int8_t*>(rec[rr].q) + o) = c;
+          }
+        }
+      }
+      if (t == 0) {
+        s_chain[b] = s;
+        if (record) {
+          if (hs) hs[b0 + b] = s;
+          for (int rr = 0; rr < n_rec; ++rr) const_cast<float*>(rec[rr].s_x)[b0 + b] = s;
+        }
+      }
+      consumer_sync<C>();  // red[] is reused by the next vector
+    }
+    return;
+  }
   for (int b = 0; b < nb; ++b) {
     float r = 1.0f;
     if (cs.gamma) {
