@@ -741,7 +741,7 @@ def run_layer_attention(args):
     Hkv, d = 8, 4096
     stream = torch.cuda.current_stream()
     gam = [torch.from_numpy(wl.scales(d, 1.0, 0, wl.tag(wl.WL_ATTN, l, 4, 0))).to(dev) for l in range(2 * L + 1)]
-    for T in (4096, 16384):
+    for T in (args.contexts or (4096, 16384)):
         pos = T - 1
         kb = wl.bf16_normal(Hkv * T * 128, 0, wl.tag(wl.WL_ATTN, T, 1, 0)).reshape(Hkv, T, 128)
         vb = wl.bf16_normal(Hkv * T * 128, 0, wl.tag(wl.WL_ATTN, T, 2, 0)).reshape(Hkv, T, 128)
@@ -765,8 +765,8 @@ def run_layer_attention(args):
                                                kf, vf, pos, g_np[:L2], g_np[L:L + L2], g_np[2 * L])
         line = {"metric": "chained decode with attention", "context": T, "layers": L}
         kv = L * 2 * Hkv * T * 128 * 2
-        for name, launcher, launches in (("persistent", nt.NT_LAUNCH_PERSISTENT, 3 * L + 1),
-                                         ("graph", nt.NT_LAUNCH_GRAPH, L * 12 + 2)):
+        arms = (("persistent", nt.NT_LAUNCH_PERSISTENT, 3 * L + 1), ("graph", nt.NT_LAUNCH_GRAPH, L * 12 + 2))
+        for name, launcher, launches in [a for a in arms if a[0] in args.launchers]:
             p2 = nt.DecodePlan(L2, 1, dp[:7 * L2], hd, nt.NT_STEP_CHAINED, launcher,
                                attention=dict(att, k_cache=kc[:L2], v_cache=vc[:L2], norm_attn=gam[:L2],
                                               norm_ffn=gam[L:L + L2]))
@@ -923,7 +923,9 @@ def main():
     ap.add_argument("--tokens", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="--prefill: token counts to run (default 2048,8192)")
     ap.add_argument("--contexts", type=lambda v: [int(x) for x in v.split(",")], default=None,
-                    help="--attention: context lengths to run (default 4096,16384,32768)")
+                    help="--attention / --layer-attention: context lengths to run")
+    ap.add_argument("--launchers", type=lambda v: v.split(","), default=["persistent", "graph"],
+                    help="--layer-attention: launchers to time (persistent,graph)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
