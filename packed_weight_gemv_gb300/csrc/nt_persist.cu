@@ -45,7 +45,8 @@ constexpr int kMaxSmem = 232448;                     // 227 KB per CTA on sm_103
 // Kernel configuration: CW consumer warps and up to NBMAX activation vectors per pass. Batch 1
 // runs 16 consumer warps (17 warps, registers capped at 96 by the 5 warps one SM
 // sub-partition holds); batched plans need more registers for 4 vectors' accumulators and run
-// 15 (16 warps, up to 128 registers).
+// 15 (16 warps, up to 128 registers), and so do chained batch-1 plans, which hold a stage input
+// of up to 28 values per thread in registers while they quantize it.
 template <int CW_, int NBMAX_, bool CHAINED_ = false>
 struct KCfg {
   static constexpr bool CHAINED = CHAINED_;  // NT_STEP_CHAINED plans (a separate instance)
@@ -57,7 +58,7 @@ struct KCfg {
 };
 using Cfg1 = KCfg<16, 1>;
 using CfgB = KCfg<15, kChunkBatch>;
-using Cfg1C = KCfg<16, 1, true>;
+using Cfg1C = KCfg<15, 1, true>;
 using CfgBC = KCfg<15, kChunkBatch, true>;
 
 enum : unsigned int { kErrFullWait = 1, kErrEmptyWait = 2, kErrGridBarrier = 3, kErrDrain = 4 };
@@ -414,9 +415,9 @@ __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, ui
     }
     return v;
   };
-  // Vectors of up to 4 * kPer * CT values (the model width) stay in registers: one pass of
+  // Vectors of up to 4 * kPer * CT values (13,440 at batch 1) stay in registers: one pass of
   // loads through L2, the reductions and the codes from the registers.
-  constexpr int kPer = 2;
+  constexpr int kPer = C::NBMAX == 1 ? 7 : 2;
   if (cs.K <= 4 * kPer * C::CT) {
     for (int b = 0; b < nb; ++b) {
       float4 v[kPer];
@@ -969,9 +970,11 @@ nt_status configure_kernel(int device) {
 // The kernel instance and block size for a batch and step mode.
 const void* kernel_for(int B, bool chained, int* threads) {
   *threads = B == 1 ? Cfg1::THREADS : CfgB::THREADS;
-  if (chained)
+  if (chained) {
+    *threads = B == 1 ? Cfg1C::THREADS : CfgBC::THREADS;
     return B == 1 ? reinterpret_cast<const void*>(persist_kernel<Cfg1C>)
                   : reinterpret_cast<const void*>(persist_kernel<CfgBC>);
+  }
   return B == 1 ? reinterpret_cast<const void*>(persist_kernel<Cfg1>)
                 : reinterpret_cast<const void*>(persist_kernel<CfgB>);
 }
