@@ -629,6 +629,12 @@ __device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDe
   const int pieces = (int)(padded_k(m.K) / 512);
   const int64_t n = tile * 4 + (lane >> 3);
   const float sw = ((lane & 7) == 0 && n < m.N) ? __ldg(m.s_w + n) : 0.0f;
+  float rin[NB];  // chained: the residual stream's values, loaded early like the row scale
+  if constexpr (CH) {
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      rin[b] = (m.res_out && (lane & 7) == 0 && n < m.N) ? __ldcg(m.res_in + (int64_t)(b0 + b) * m.N + n) : 0.0f;
+  }
   int acc[NB][4];
 #pragma unroll
   for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = acc[b][2] = acc[b][3] = 0;
@@ -653,7 +659,7 @@ __device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDe
       const float yv = scale_out(total, sw, sx[b]);
       m.y[o] = yv;
       if constexpr (CH) {  // chained: the residual stream
-        if (m.res_out) m.res_out[o] = __fadd_rn(__ldcg(m.res_in + o), yv);
+        if (m.res_out) m.res_out[o] = __fadd_rn(rin[b], yv);
       }
     }
   }
