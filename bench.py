@@ -281,36 +281,45 @@ def run_ours(args, rank, world):
     value = us / (args.steps * world)
 
     # End to end through the same public call, with pinned host buffers: every step copies its
-    # fp32 inputs host->device, runs the step and reads the emitted token back. The inputs are
-    # double-buffered: step i+1's copy (on its own stream) overlaps step i's compute, and waits
-    # until step i-1 has finished reading the buffer it overwrites.
+    # fp32 inputs host->device, runs the step and reads the emitted token back. Inputs and
+    # token are double-buffered: step i+1's copy (on its own stream) overlaps step i's compute
+    # and waits until step i-1 has finished with the buffers it overwrites; the token is read
+    # back on a third stream.
     x_host = torch.empty(x_all.numel(), dtype=torch.float32, pin_memory=True)
     x_host.copy_(x_all.cpu())
-    am_host = torch.empty(1, dtype=torch.int32, pin_memory=True)
     x_alt = torch.empty_like(x_all)
     dp_alt, off = [], 0
     for d in dp:
         dp_alt.append(dict(d, x=x_alt[off:off + d["K"]]))
         off += d["K"]
-    hd_alt = dict(hd, x=x_alt[off:off + head.K])
+    hd_alt = dict(hd, x=x_alt[off:off + head.K], argmax=torch.empty_like(hd["argmax"]))
     plans = [plan, nt.DecodePlan(L, 1, dp_alt, hd_alt, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)]
-    bufs = [x_all, x_alt]
-    copy_stream = torch.cuda.Stream()
+    bufs, am_dev = [x_all, x_alt], [hd["argmax"], hd_alt["argmax"]]
+    am_host = torch.empty(2, dtype=torch.int32, pin_memory=True)
+    copy_stream, read_stream = torch.cuda.Stream(), torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
     for k in range(2):
         consumed[k].record(stream)
+        read[k].record(stream)
 
     def e2e_step(i):
+        # inputs of step i into buffer set k on the copy stream once step i - 2 has consumed
+        # them; the token read back on its own stream, so the next step never waits for it
         k = i % 2
         copy_stream.wait_event(consumed[k])
         with torch.cuda.stream(copy_stream):
             bufs[k].copy_(x_host, non_blocking=True)
             copied[k].record(copy_stream)
         stream.wait_event(copied[k])
+        stream.wait_event(read[k])
         plans[k].nt_decode_step(stream)
         consumed[k].record(stream)
-        am_host.copy_(hd["argmax"], non_blocking=True)
+        read_stream.wait_event(consumed[k])
+        with torch.cuda.stream(read_stream):
+            am_host[k:k + 1].copy_(am_dev[k], non_blocking=True)
+            read[k].record(read_stream)
 
     e2e_steps = max(1, min(args.steps, 2000))
     for i in range(4):
