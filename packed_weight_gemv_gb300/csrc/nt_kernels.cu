@@ -247,10 +247,12 @@ __global__ void __launch_bounds__(kThreads) gemv_plain_kernel(
 // ---------------------------------------------------------------------------------------
 // Tiled-layout projection: one warp per tile (4 rows). Lane l reads 16-byte groups
 // l, l+32, ... (4 rows x 16 trits each) and the matching 16 activation bytes; each group
-// costs one shift, four byte permutes and four dp4a per row.
+// costs one shift, four byte permutes and four dp4a per row. The weight loads of U groups
+// per lane go out together, so a warp keeps U x 512 bytes in flight.
 // ---------------------------------------------------------------------------------------
 template <int NB>
 __device__ __forceinline__ void tiled_tile(const MatDesc& m, int64_t tile, int lane) {
+  constexpr int U = NB <= 4 ? 4 : 2;
   const int64_t Kp = padded_k(m.K);
   const int groups = (int)(Kp / 16), kgroups = m.K / 16;
   const uint8_t* tbase = m.w + tile * Kp;
@@ -260,17 +262,26 @@ __device__ __forceinline__ void tiled_tile(const MatDesc& m, int64_t tile, int l
     for (int b = 0; b < NB; ++b)
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[b][r] = 0;
-    for (int g = lane; g < groups; g += 32) {
-      const uint4 wv = ld_stream(tbase + 16 * (int64_t)g);
-      if (g < kgroups) {
+    for (int g0 = lane; g0 < groups; g0 += 32 * U) {
+      uint4 wv[U];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          if (b0 + b < m.B) {
-            const uint4 a = *reinterpret_cast<const uint4*>(m.q + (int64_t)(b0 + b) * m.K + 16 * g);
-            acc[b][0] = tiled_word_dot(wv.x, a.x, a.y, a.z, a.w, acc[b][0]);
-            acc[b][1] = tiled_word_dot(wv.y, a.x, a.y, a.z, a.w, acc[b][1]);
-            acc[b][2] = tiled_word_dot(wv.z, a.x, a.y, a.z, a.w, acc[b][2]);
-            acc[b][3] = tiled_word_dot(wv.w, a.x, a.y, a.z, a.w, acc[b][3]);
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u;
+        wv[u] = g < groups ? ld_stream(tbase + 16 * (int64_t)g) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int g = g0 + 32 * u;
+        if (g < kgroups) {
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            if (b0 + b < m.B) {
+              const uint4 a = *reinterpret_cast<const uint4*>(m.q + (int64_t)(b0 + b) * m.K + 16 * g);
+              acc[b][0] = tiled_word_dot(wv[u].x, a.x, a.y, a.z, a.w, acc[b][0]);
+              acc[b][1] = tiled_word_dot(wv[u].y, a.x, a.y, a.z, a.w, acc[b][1]);
+              acc[b][2] = tiled_word_dot(wv[u].z, a.x, a.y, a.z, a.w, acc[b][2]);
+              acc[b][3] = tiled_word_dot(wv[u].w, a.x, a.y, a.z, a.w, acc[b][3]);
+            }
           }
         }
       }
