@@ -370,6 +370,58 @@ def run_ours(args, rank, world):
     stream_bytes = wl.packed_bytes_per_token(n_layers=L) + 4 * sum(p.K for p in projs)
     comp["weight_stream"] = dict(frac(stream_bytes, us_stream), kernel="persist_kernel",
                                  what=f"{L} layers x 7 ternary projections, inputs quantized in the step")
+    # the per-call API: one nt_ternary_gemv per projection (inputs already quantized by the step)
+    def gemv_calls():
+        st = torch.cuda.current_stream()  # the capture stream inside torch.cuda.graph
+        for d in dp:
+            nt.nt_ternary_gemv(d["w"], nt.NT_LAYOUT_TILED, d["s_w"], d["N"], d["K"], d["q"], d["s_x"], d["y"],
+                               stream=st)
+
+    for _ in range(3):
+        gemv_calls()
+    torch.cuda.synchronize()
+    gemv_graph = torch.cuda.CUDAGraph()  # replayed, so the host's per-call cost is not timed
+    with torch.cuda.graph(gemv_graph):
+        gemv_calls()
+    gemv_graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(10):
+        gemv_graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    del gemv_graph
+    comp["gemv_per_call"] = dict(frac(wl.packed_bytes_per_token(n_layers=L), e0.elapsed_time(e1) * 1e3 / 10),
+                                 kernel="gemv_tiled_kernel",
+                                 what=f"{len(dp)} nt_ternary_gemv calls, batch 1, replayed as a CUDA graph "
+                                      "(each call a separate kernel: latency-bound for 1-12 MB matrices)")
+    # one large per-call GEMV (268 MB of packed trits, more than L2): the kernel's streaming rate
+    bN, bK = 65536, 16384
+    r1 = torch.randint(-2 ** 31, 2 ** 31 - 1, (bN * bK // 16,), dtype=torch.int32, device=dev)
+    r2 = torch.randint(-2 ** 31, 2 ** 31 - 1, (bN * bK // 16,), dtype=torch.int32, device=dev)
+    low = r1 & 0x55555555
+    big_plain = low | ((low & r2) << 1)  # fields 00 / 01 / 11 only
+    del r1, r2, low
+    big_w = torch.empty(nt.nt_repack_size(bN, bK), dtype=torch.uint8, device=dev)
+    nt.nt_repack_ternary(big_plain, bN, bK, big_w, stream=stream)
+    del big_plain
+    big_q = torch.randint(-127, 128, (bK,), dtype=torch.int8, device=dev)
+    big_sw = torch.full((bN,), 0.01, dtype=torch.float32, device=dev)
+    big_sx = torch.full((1,), 0.02, dtype=torch.float32, device=dev)
+    big_y = torch.empty(bN, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        nt.nt_ternary_gemv(big_w, nt.NT_LAYOUT_TILED, big_sw, bN, bK, big_q, big_sx, big_y, stream=stream)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(10):
+        nt.nt_ternary_gemv(big_w, nt.NT_LAYOUT_TILED, big_sw, bN, bK, big_q, big_sx, big_y, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    big_bytes = bN * bK // 4 + 4 * bN + bK + 4 * bN + 4
+    comp["gemv_per_call_large"] = dict(frac(big_bytes, e0.elapsed_time(e1) * 1e3 / 10), kernel="gemv_tiled_kernel",
+                                       what=f"one nt_ternary_gemv call, {bN}x{bK} trits (268 MB), batch 1")
+    del big_w, big_q, big_sw, big_sx, big_y
     hws = torch.empty(nt.nt_int8_logits_workspace_size(head.V, head.K, 1), dtype=torch.uint8, device=dev)
     nt.nt_quantize_act(hd["x"], hd["q"], hd["sx"], stream)
 
@@ -379,7 +431,6 @@ def run_ours(args, rank, world):
 
     for _ in range(3):
         head_call()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for _ in range(n_extra):
