@@ -136,8 +136,12 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
                               p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1, pdl));
     }
     if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st, pdl));
-    NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
-                                   s.total_tiles, p->B, st, pdl));
+    if (p->d_mma)
+      NT_TRY(launch_gemv_mma(p->d_mma + s.first_mat, s.n_mats, p->d_mma_tab + s.mma_tab_off, s.mma_ctas, p->B, st,
+                             pdl));
+    else
+      NT_TRY(launch_gemv_tiled_group(p->d_mats + s.first_mat, p->d_prefix + s.prefix_off, s.n_mats,
+                                     s.total_tiles, p->B, st, pdl));
   }
   if (p->has_head && chained) NT_TRY(launch_chain_quant(p->d_cjobs + p->stages.size(), p->B, st, pdl));
   if (p->has_head)
@@ -154,6 +158,9 @@ void free_plan(nt_decode_plan* p) {
   if (p->graph) cudaGraphDestroy(p->graph);
   cudaFree(p->d_mats);
   cudaFree(p->d_prefix);
+  cudaFree(p->d_mma);
+  cudaFree(p->d_mma_ws);
+  cudaFree(p->d_mma_tab);
   cudaFree(p->d_qjobs);
   cudaFree(p->d_head_ws);
   cudaFree(p->d_ctrl);
@@ -380,6 +387,57 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
   if ((e = cudaMalloc(&p->d_prefix, sizeof(int64_t) * prefix.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
   if ((e = cudaMemcpy(p->d_prefix, prefix.data(), sizeof(int64_t) * prefix.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy");
+  if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch) {
+    // batched plans on the stream / graph launchers: the tensor-core path. Every stage's
+    // matrices take disjoint parts of one workspace ([B][N] int32 sums of each matrix, then
+    // the unit counters); stages run one after another and leave it zero.
+    std::vector<MmaMat> mm(mats.size());
+    std::vector<int64_t> acc_off(mats.size()), cnt_off(mats.size());
+    std::vector<uint16_t> tab;  // every stage's CTA -> matrix (index within the stage)
+    size_t ws_bytes = 0;
+    for (PlanStage& st : p->stages) {
+      if (st.n_mats > 65535) return fail(set_error(NT_ERR_INVALID_ARG, "too many projections in one stage"));
+      st.mma_tab_off = (int64_t)tab.size();
+      int64_t ctas = 0, rows = 0, units = 0;
+      for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) {
+        const MatDesc& d = mats[i];
+        MmaMat& x = mm[i];
+        x = MmaMat{};
+        x.w = d.w;
+        x.s_w = d.s_w;
+        x.q = d.q;
+        x.s_x = d.s_x;
+        x.y = d.y;
+        x.acc = d.acc;
+        x.N = d.N;
+        x.K = d.K;
+        x.B = d.B;
+        mma_geometry(x);
+        x.cta_begin = ctas;
+        ctas += mma_ctas(x);
+        tab.insert(tab.end(), (size_t)mma_ctas(x), (uint16_t)(i - st.first_mat));
+        acc_off[i] = rows * d.B;
+        rows += d.N;
+        cnt_off[i] = units;
+        units += x.units16;
+      }
+      for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) cnt_off[i] += rows * p->B;  // in 4-byte words
+      st.mma_ctas = ctas;
+      ws_bytes = std::max(ws_bytes, mma_ws_bytes(rows, units, p->B));
+    }
+    if ((e = cudaMalloc(&p->d_mma_ws, ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(p->d_mma_ws, 0, ws_bytes)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    for (size_t i = 0; i < mm.size(); ++i) {
+      mm[i].acc_ws = static_cast<int32_t*>(p->d_mma_ws) + acc_off[i];
+      mm[i].cnt = static_cast<unsigned int*>(p->d_mma_ws) + cnt_off[i];
+    }
+    if ((e = cudaMalloc(&p->d_mma_tab, sizeof(uint16_t) * tab.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemcpy(p->d_mma_tab, tab.data(), sizeof(uint16_t) * tab.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy");
+    if ((e = cudaMalloc(&p->d_mma, sizeof(MmaMat) * mm.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemcpy(p->d_mma, mm.data(), sizeof(MmaMat) * mm.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy");
+  }
   if (!jobs.empty()) {
     if ((e = cudaMalloc(&p->d_qjobs, sizeof(QuantJob) * jobs.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemcpy(p->d_qjobs, jobs.data(), sizeof(QuantJob) * jobs.size(), cudaMemcpyHostToDevice)) != cudaSuccess)

@@ -14,6 +14,8 @@ struct PlanStage {
   int first_mat, n_mats;
   int64_t prefix_off;   // into the plan's prefix array
   int64_t total_tiles;
+  int64_t mma_ctas;     // batched plans on the tensor-core path: CTAs of the stage's launch
+  int64_t mma_tab_off;  //   and the offset of its CTA -> matrix table in the plan's table
 };
 
 // Device control word of a plan: error word of the bounded waits and the grid-barrier
@@ -47,6 +49,11 @@ struct nt_decode_plan {
   std::vector<nt::PlanStage> stages;
   nt::MatDesc* d_mats = nullptr;
   int64_t* d_prefix = nullptr;
+  // stream / graph launchers of batched plans: the tensor-core path's matrices (step order,
+  // each stage's CTAs numbered from 0) and its int32 workspace (reused by every stage)
+  nt::MmaMat* d_mma = nullptr;
+  void* d_mma_ws = nullptr;
+  uint16_t* d_mma_tab = nullptr;
   nt::QuantJob* d_qjobs = nullptr;
   int n_qjobs = 0;
   bool has_head = false;
