@@ -10,14 +10,20 @@
 // digits, was built first: on this part it executes as about 13 instructions per MMA against
 // about 1 for f16, which left it issue-bound.)
 //
-// Work: a warp takes 4 (16-row unit, 1,024-trit chunk) items, a CTA 32 units of one chunk. The
-// CTA converts the chunk's activations of all vectors to f16 in shared memory, laid out as the
-// MMA's B operand; each lane then reads the packed words of its two rows straight from the
-// tiled layout (two 4-byte words per 64 trits, coalesced in 64-byte runs), decodes them with
-// the pair-code pools into the f16 high bytes and spreads those into the A operand. Partial
-// int32 sums of a chunk go to an int32 workspace with atomics; the warp that completes a
-// unit's last chunk applies the fp32 epilogue (as the other paths: fl(fl(acc) * s_w) * s_x)
-// and clears the workspace and its counter for the next call.
+// Decode: two byte permutes per 16-bit half word look the pair codes up in two pools that hold
+// the f16 high bytes of +1 / -1 / 0, giving quads (4 trits as 4 high bytes); two more byte
+// permutes per quad place its bytes 0, 1 and 2, 3 over zero low bytes as two f16x2 operands.
+// The byte-permute (ALU) pipe is the kernel's busiest: about 7.5 of its instructions per MMA.
+//
+// Work: a CTA of 8 warps takes one 1,024-trit chunk of K and up to 32 units of 32 rows (8
+// tiles); it first converts the chunk's activations of all vectors to f16 in shared memory, laid
+// out as the MMA's B operand. A lane owns one tile of its warp's unit and reads 16 bytes at a
+// time (4 rows x 16 trits), coalesced in 64-byte runs; the tile's rows 0/1 form the rows g / g + 8
+// of one 16-row MMA tile and rows 2/3 those of a second, so both share every B fragment. Loads
+// run one step (512 trits) ahead in registers, across unit boundaries. A unit's int32 sums of a
+// chunk go to an int32 workspace with atomics; the CTA that completes a unit group's last chunk
+// applies the fp32 epilogue (as the other paths: fl(fl(acc) * s_w) * s_x) and clears the
+// workspace and the group's counter for the next call.
 #include <cuda_fp16.h>
 
 #include "nt_kernels.cuh"
@@ -27,10 +33,13 @@ namespace {
 
 constexpr int kMmaWarps = 8;
 constexpr int kMmaThreads = 32 * kMmaWarps;
-constexpr int kUnitsPerWarp = 4;         // 16-row units per warp and chunk
+constexpr int kUnitRows = 32;            // rows per warp unit: 8 tiles, one per lane group
+constexpr int kUnitsPerWarp = 2;         // units per warp and chunk
 constexpr int kUnitsPerCta = kMmaWarps * kUnitsPerWarp;
-constexpr int kChunkK = 1024;            // trits per work item
+constexpr int kChunkK = 1024;            // trits of K per CTA
 constexpr int kChunkBlocks = kChunkK / 16;  // k16 blocks of the f16 MMA
+constexpr int kStepSpans = 8;            // 64-trit spans per load step (a 16-byte load per lane each)
+constexpr int kStepK = 64 * kStepSpans;
 
 // f16 pair-code pools: the tiled layout's codes select the high byte of +1 / -1 / 0 as 0x3C /
 // 0xBC / 0x00 (the low byte of all three is 0). Code 14 (the pair (0, -1)) reads byte 6 in
@@ -68,17 +77,38 @@ __device__ __forceinline__ uint2 f16x4(uint32_t x) {
   return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
 }
 
-__device__ __forceinline__ uint32_t ld_word(const uint8_t* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];\n" : "=r"(v) : "l"(p));
+// One 16-trit group of a tile: its 4 rows' words (streamed once, no L1 allocation).
+__device__ __forceinline__ uint4 ld_group(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
-// NT tiles of 8 vectors (B <= 8 NT). Grid: one CTA per (matrix, chunk, 32 units).
+// Unit sums of one chunk into the workspace: lane (g, t) holds, per 16-row tile mt and vector
+// tile nt, rows 4 g + 2 mt (+1) of its unit and vectors 8 nt + 2 t (+1).
 template <int NT>
-__global__ void __launch_bounds__(kMmaThreads) gemv_mma_kernel(const MmaMat* __restrict__ mats, int n_mats,
-                                                              const uint16_t* __restrict__ cta_mat) {
+__device__ __forceinline__ void flush_unit(float (&c)[2][NT][4], const MmaMat& m, int u, int g, int t) {
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int acc = __float2int_rn(c[mt][nt][e]);
+        c[mt][nt][e] = 0.0f;
+        const int64_t n = (int64_t)kUnitRows * u + 4 * g + 2 * mt + (e >> 1);
+        const int v = 8 * nt + 2 * t + (e & 1);
+        if (n < m.N && v < m.B && acc != 0) atomicAdd(m.acc_ws + (int64_t)v * m.N + n, acc);
+      }
+}
+
+// NT tiles of 8 vectors (B <= 8 NT). Grid: one CTA per (matrix, chunk, group of 16 units).
+template <int NT>
+__global__ void __launch_bounds__(kMmaThreads, 2) gemv_mma_kernel(const MmaMat* __restrict__ mats, int n_mats,
+                                                                 const uint16_t* __restrict__ cta_mat) {
   __shared__ __align__(16) uint2 sB[NT][kChunkBlocks][32];  // per lane: 4 f16 activations
+  __shared__ int s_last;
   dependent_launch_wait();
   int lo = 0, hi = n_mats - 1;  // this CTA's matrix: from the table, else the last whose first CTA <= it
   if (cta_mat) {
@@ -94,12 +124,66 @@ __global__ void __launch_bounds__(kMmaThreads) gemv_mma_kernel(const MmaMat* __r
   const int chunk = li / m.ugroups, ug = li - chunk * m.ugroups;
   const int64_t Kp = padded_k(m.K);
   const int k0 = chunk * kChunkK;
-  const int spans = (int)(Kp - k0 < kChunkK ? Kp - k0 : kChunkK) / 64;  // 8 or 16 spans of 64 trits
+  const int steps = (int)(Kp - k0 < kChunkK ? Kp - k0 : kChunkK) / kStepK;  // 1 or 2 steps per unit
+
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int64_t ntiles = padded_rows(m.N) / 4;
+  const int ubase = ug * kUnitsPerCta + w;  // the warp's units: ubase + 8 j
+  const int rem = m.units32 - ubase;
+  const int items = rem <= 0 ? 0 : min(kUnitsPerWarp, (rem + kMmaWarps - 1) / kMmaWarps);
+  const int sh = steps == 2 ? 1 : 0;
+  const int total = items << sh;  // load steps of this warp: unit s >> sh, half s & (steps - 1)
+
+  // step s: lane (g, t) reads tile 8 u + g at trits k0 + 512 half + 64 sp + 16 t, sp = 0..7
+  auto load = [&](uint4 (&b)[kStepSpans], int s) {
+    const int64_t T = (int64_t)(kUnitRows / 4) * (ubase + kMmaWarps * (s >> sh)) + g;
+    const bool ok = s < total && T < ntiles;
+    const uint8_t* p = m.w + T * Kp + k0 + kStepK * (s & (steps - 1)) + 16 * t;
+#pragma unroll
+    for (int sp = 0; sp < kStepSpans; ++sp) b[sp] = ok ? ld_group(p + 64 * sp) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  // one chunk's sums stay exact in fp32: |sum| <= 127 * 1024
+  float c[2][NT][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[mt][nt][e] = 0.0f;
+  auto compute = [&](const uint4 (&b)[kStepSpans], int s) {
+    const int half = s & (steps - 1);
+#pragma unroll
+    for (int sp = 0; sp < kStepSpans; ++sp) {
+      uint32_t r0[4], r1[4], r2[4], r3[4];  // tile rows 0..3: trits 4 i .. 4 i + 3 of the group in [i]
+      word_hi_bytes(b[sp].x, r0);
+      word_hi_bytes(b[sp].y, r1);
+      word_hi_bytes(b[sp].z, r2);
+      word_hi_bytes(b[sp].w, r3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // block i of the span: logical k 2t, 2t + 1 / 2t + 8, 2t + 9 are
+        const int blk = (kStepK / 16) * half + 4 * sp + i;  // the lane's trits 4 i, 4 i + 1 / 4 i + 2, 4 i + 3
+        const uint32_t a0 = f16x2_lo(r0[i]), a1 = f16x2_lo(r1[i]), a2 = f16x2_hi(r0[i]), a3 = f16x2_hi(r1[i]);
+        const uint32_t e0 = f16x2_lo(r2[i]), e1 = f16x2_lo(r3[i]), e2 = f16x2_hi(r2[i]), e3 = f16x2_hi(r3[i]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 bv = sB[nt][blk][lane];
+          mma_f16(c[0][nt], a0, a1, a2, a3, bv.x, bv.y);
+          mma_f16(c[1][nt], e0, e1, e2, e3, bv.x, bv.y);
+        }
+      }
+    }
+    if (half == steps - 1) flush_unit<NT>(c, m, ubase + kMmaWarps * (s >> sh), g, t);
+  };
+  // loads run one step ahead of the decode, across unit boundaries
+  uint4 ba[kStepSpans], bb[kStepSpans];
+  load(ba, 0);  // in flight while the activations are converted
 
   // the chunk's activations of every vector as f16 in the B operand's order: 4 bytes k4 of
   // vector v (chunk trits 4 k4 .. 4 k4 + 3) are lane (v % 8, (k4 % 16) / 4)'s operand of block
   // 4 (k4 / 16) + k4 % 4 in vector tile v / 8
-  for (int e = threadIdx.x; e < NT * 8 * (kChunkK / 4); e += kMmaThreads) {
+#pragma unroll
+  for (int r = 0; r < NT * 8 * (kChunkK / 4) / kMmaThreads; ++r) {
+    const int e = threadIdx.x + r * kMmaThreads;
     const int v = e / (kChunkK / 4), k4 = e - v * (kChunkK / 4);
     const int k = k0 + 4 * k4;
     uint32_t qv = 0u;
@@ -109,96 +193,48 @@ __global__ void __launch_bounds__(kMmaThreads) gemv_mma_kernel(const MmaMat* __r
   }
   __syncthreads();
 
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int64_t ntiles = padded_rows(m.N) / 4;
 #pragma unroll 1
-  for (int j = 0; j < kUnitsPerWarp; ++j) {
-    const int u = ug * kUnitsPerCta + j * kMmaWarps + w;
-    if (u >= m.units16) return;
-    const int64_t T0 = 4 * (int64_t)u + (g >> 2), T1 = T0 + 2;  // tiles of rows g and g + 8
-    const uint8_t* r0 = m.w + T0 * Kp + 4 * (g & 3);
-    const uint8_t* r1 = m.w + T1 * Kp + 4 * (g & 3);
-    const bool ok0 = T0 < ntiles, ok1 = T1 < ntiles;
-
-    // every load of the chunk first: span s, lane t: the 16 trits k0 + 64 s + 16 t .. of each row
-    uint32_t w0[16], w1[16];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const int64_t off = (int64_t)(k0 + 64 * s + 16 * t);  // a multiple of 16: the word's group
-      w0[s] = (s < spans && ok0) ? ld_word(r0 + off) : 0u;
-      w1[s] = (s < spans && ok1) ? ld_word(r1 + off) : 0u;
-    }
-    // one chunk's sums stay exact in fp32: |sum| <= 127 * 1024
-    float c[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) c[nt][e] = 0.0f;
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      if (s < spans) {  // the same in every lane
-        uint32_t a[4], b[4];
-        word_hi_bytes(w0[s], a);  // row g: trits 16 t + 4 i .. + 3 of the span in a[i]
-        word_hi_bytes(w1[s], b);  // row g + 8
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {  // block 4 s + i: logical k 2t, 2t + 1 / 2t + 8, 2t + 9 are
-          const int blk = 4 * s + i;   // the lane's trits 4 i, 4 i + 1 / 4 i + 2, 4 i + 3
-          const uint32_t a0 = f16x2_lo(a[i]), a1 = f16x2_lo(b[i]), a2 = f16x2_hi(a[i]), a3 = f16x2_hi(b[i]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 bv = sB[nt][blk][lane];
-            mma_f16(c[nt], a0, a1, a2, a3, bv.x, bv.y);
-          }
-        }
-      }
-    }
-
-    // the chunk's sums: lane (g, t) holds rows g, g + 8 x vectors 2t, 2t + 1 of each tile
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int acc = __float2int_rn(c[nt][e]);
-        const int64_t n = 16 * (int64_t)u + g + 8 * (e >> 1);
-        const int v = 8 * nt + 2 * t + (e & 1);
-        if (n < m.N && v < m.B && acc != 0) atomicAdd(m.acc_ws + (int64_t)v * m.N + n, acc);
-      }
-    __syncwarp();
-    unsigned int last = 0;
-    if (lane == 0) {
-      __threadfence();  // this warp's sums are visible before the unit's counter moves
-      last = atomicAdd(m.cnt + u, 1u) == (unsigned)(m.kchunks - 1);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      for (int i = lane; i < 16 * m.B; i += 32) {  // the unit's epilogue, then clear for the next call
-        const int64_t n = 16 * (int64_t)u + (i & 15);
-        const int v = i >> 4;
-        if (n >= m.N) continue;
-        int32_t* a = m.acc_ws + (int64_t)v * m.N + n;
-        const int total = __ldcg(a);
-        m.y[(int64_t)v * m.N + n] = scale_out(total, __ldg(m.s_w + n), __ldg(m.s_x + v));
-        if (m.acc) m.acc[(int64_t)v * m.N + n] = total;
-        *a = 0;
-      }
-      if (lane == 0) m.cnt[u] = 0u;
+  for (int s = 0; s < total; s += 2) {
+    load(bb, s + 1);
+    compute(ba, s);
+    if (s + 1 < total) {  // the same in every lane
+      load(ba, s + 2);
+      compute(bb, s + 1);
     }
   }
+
+  // the group's epilogue by the CTA that completes its last chunk
+  __threadfence();  // this thread's sums are visible before the group's counter moves
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(m.cnt + ug, 1u) == (unsigned)(m.kchunks - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int64_t n0 = (int64_t)kUnitRows * kUnitsPerCta * ug;
+  const int64_t n1 = m.N < n0 + kUnitRows * kUnitsPerCta ? m.N : n0 + kUnitRows * kUnitsPerCta;
+  for (int v = 0; v < m.B; ++v)
+    for (int64_t n = n0 + threadIdx.x; n < n1; n += kMmaThreads) {
+      int32_t* a = m.acc_ws + (int64_t)v * m.N + n;
+      const int sum = __ldcg(a);
+      m.y[(int64_t)v * m.N + n] = scale_out(sum, __ldg(m.s_w + n), __ldg(m.s_x + v));
+      if (m.acc) m.acc[(int64_t)v * m.N + n] = sum;
+      *a = 0;
+    }
+  if (threadIdx.x == 0) m.cnt[ug] = 0u;
 }
 
 }  // namespace
 
-// Geometry of one matrix on the tensor-core batched path: its 16-row units, 1,024-trit chunks
-// and CTAs (32 units of one chunk each).
+// Geometry of one matrix on the tensor-core batched path: its 32-row units, 1,024-trit chunks,
+// groups of 32 units and CTAs (one per chunk and group).
 void mma_geometry(MmaMat& m) {
-  m.units16 = (int)((padded_rows(m.N) + 15) / 16);
+  m.units32 = (int)((padded_rows(m.N) + kUnitRows - 1) / kUnitRows);
   m.kchunks = (int)((padded_k(m.K) + kChunkK - 1) / kChunkK);
-  m.ugroups = (m.units16 + kUnitsPerCta - 1) / kUnitsPerCta;
+  m.ugroups = (m.units32 + kUnitsPerCta - 1) / kUnitsPerCta;
 }
 int64_t mma_ctas(const MmaMat& m) { return (int64_t)m.kchunks * m.ugroups; }
-size_t mma_ws_bytes(int64_t rows, int64_t units16, int B) {
-  return sizeof(int32_t) * (size_t)(B * rows) + sizeof(unsigned int) * (size_t)units16;
+size_t mma_ws_bytes(int64_t rows, int64_t groups, int B) {
+  return sizeof(int32_t) * (size_t)(B * rows) + sizeof(unsigned int) * (size_t)groups;
 }
 
 nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,

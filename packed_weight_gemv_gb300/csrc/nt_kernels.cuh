@@ -86,7 +86,7 @@ nt_status launch_gemv_plain(const uint32_t* w, const float* s_w, int N, int K, c
 nt_status launch_gemv_tiled(const MatDesc& m, cudaStream_t st);
 // Several tiled projections in one launch: d_mats[n] in device memory, d_tile_prefix[n+1]
 // their cumulative tile counts.
-// Batched projections on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, e4m3 digits.
+// Batched projections on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, f16 MMA.
 constexpr int kMmaMinBatch = 2, kMmaMaxBatch = 16;
 struct MmaMat {
   const uint8_t* w;  // tiles (nt_repack_ternary output)
@@ -96,14 +96,14 @@ struct MmaMat {
   float* y;          // [B][N]
   int32_t* acc;      // [B][N] or null
   int32_t* acc_ws;   // [B][N] int32 workspace, zero between calls
-  unsigned int* cnt; // [units16] chunk counters, zero between calls
+  unsigned int* cnt; // [ugroups] chunk counters of each unit group, zero between calls
   int N, K, B;
-  int units16, kchunks, ugroups;  // set by mma_geometry
+  int units32, kchunks, ugroups;  // set by mma_geometry
   int64_t cta_begin;              // first CTA of this matrix in its launch
 };
 void mma_geometry(MmaMat& m);
 int64_t mma_ctas(const MmaMat& m);
-size_t mma_ws_bytes(int64_t rows, int64_t units16, int B);
+size_t mma_ws_bytes(int64_t rows, int64_t groups, int B);
 nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,
                           cudaStream_t st, bool pdl = false);
 nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_tile_prefix, int n,

@@ -390,7 +390,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
   if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch) {
     // batched plans on the stream / graph launchers: the tensor-core path. Every stage's
     // matrices take disjoint parts of one workspace ([B][N] int32 sums of each matrix, then
-    // the unit counters); stages run one after another and leave it zero.
+    // the unit groups' counters); stages run one after another and leave it zero.
     std::vector<MmaMat> mm(mats.size());
     std::vector<int64_t> acc_off(mats.size()), cnt_off(mats.size());
     std::vector<uint16_t> tab;  // every stage's CTA -> matrix (index within the stage)
@@ -419,7 +419,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
         acc_off[i] = rows * d.B;
         rows += d.N;
         cnt_off[i] = units;
-        units += x.units16;
+        units += x.ugroups;
       }
       for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) cnt_off[i] += rows * p->B;  // in 4-byte words
       st.mma_ctas = ctas;
