@@ -491,6 +491,8 @@ nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_prefix
 nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
                       cudaStream_t st) {
+  if (B >= kMmaMinBatch && B <= kMmaMaxBatch)  // one pass over T on the tensor cores
+    return launch_head_mma(T, s_T, V, K, q, s_x, B, logits, argmax, ws, st);
   if (persist_head_fits(K, B))  // the streaming kernel (bulk copies into per-warp rings)
     return persist_launch_head(T, s_T, V, K, q, s_x, B, logits, argmax, ws, st);
   int g = grid_for(V, 4);

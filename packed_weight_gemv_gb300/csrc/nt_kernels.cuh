@@ -96,16 +96,19 @@ struct MmaMat {
   float* y;          // [B][N]
   int32_t* acc;      // [B][N] or null
   int32_t* acc_ws;   // [B][N] int32 workspace, zero between calls
-  unsigned int* cnt; // [ugroups] chunk counters of each unit group, zero between calls
+  unsigned int* cnt; // [ugroups] part counters of each unit group, zero between calls
   int N, K, B;
-  int units32, kchunks, ugroups;  // set by mma_geometry
+  int units32, kchunks, ugroups, cpp, nparts;  // set by mma_geometry (cpp: chunks per part)
   int64_t cta_begin;              // first CTA of this matrix in its launch
 };
-void mma_geometry(MmaMat& m);
+void mma_geometry(MmaMat& m, int parts);
 int64_t mma_ctas(const MmaMat& m);
 size_t mma_ws_bytes(int64_t rows, int64_t groups, int B);
 nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,
                           cudaStream_t st, bool pdl = false);
+// Output projection on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, one pass over T.
+nt_status launch_head_mma(const int8_t* T, const float* s_T, int V, int K, const int8_t* q, const float* s_x,
+                          int B, float* logits, int32_t* argmax, HeadWs* ws, cudaStream_t st);
 nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_tile_prefix, int n,
                                   int64_t total_tiles, int max_B, cudaStream_t st, bool pdl = false);
 nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,

@@ -8,6 +8,7 @@
 //   NT_LAUNCH_GRAPH      the same launches captured once into a CUDA graph, replayed per step;
 //   NT_LAUNCH_PERSISTENT one cooperative kernel streams the whole step (nt_persist.cu).
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -398,6 +399,34 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     for (PlanStage& st : p->stages) {
       if (st.n_mats > 65535) return fail(set_error(NT_ERR_INVALID_ARG, "too many projections in one stage"));
       st.mma_tab_off = (int64_t)tab.size();
+      // K parts: every matrix of the stage is cut into parts as long as the shortest K (so
+      // the CTAs do equal work), then all parts are halved while the stage has fewer than 8
+      // waves of CTAs; the parts meet in the workspace, unsplit matrices write y straight
+      // from the sums
+      std::vector<int> chunks_of;
+      int64_t min_chunks = INT64_MAX;
+      for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) {
+        MmaMat g{};
+        g.N = mats[i].N;
+        g.K = mats[i].K;
+        mma_geometry(g, 1);
+        chunks_of.push_back(g.kchunks);
+        min_chunks = std::min<int64_t>(min_chunks, g.kchunks);
+      }
+      auto stage_ctas = [&](int64_t mult) {
+        int64_t n = 0;
+        for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) {
+          MmaMat g{};
+          g.N = mats[i].N;
+          g.K = mats[i].K;
+          const int64_t c = chunks_of[i - st.first_mat];
+          mma_geometry(g, (int)(mult * ((c + min_chunks - 1) / min_chunks)));
+          n += mma_ctas(g);
+        }
+        return n;
+      };
+      int64_t mult = 1;
+      while (mult < min_chunks && stage_ctas(mult) < 8LL * device_sm_count()) mult *= 2;
       int64_t ctas = 0, rows = 0, units = 0;
       for (int i = st.first_mat; i < st.first_mat + st.n_mats; ++i) {
         const MatDesc& d = mats[i];
@@ -412,7 +441,8 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
         x.N = d.N;
         x.K = d.K;
         x.B = d.B;
-        mma_geometry(x);
+        const int64_t c = chunks_of[i - st.first_mat];
+        mma_geometry(x, (int)(mult * ((c + min_chunks - 1) / min_chunks)));
         x.cta_begin = ctas;
         ctas += mma_ctas(x);
         tab.insert(tab.end(), (size_t)mma_ctas(x), (uint16_t)(i - st.first_mat));

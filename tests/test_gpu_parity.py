@@ -140,7 +140,7 @@ def _head_call(T, s_T, V, K, q, s, B, ws=None):
     return host(logits), host(am), ws
 
 
-@pytest.mark.parametrize("B", [1, 3, 16, 17])
+@pytest.mark.parametrize("B", [1, 2, 3, 8, 16, 17])
 def test_head_small(B):
     h = wl.head(V=5000, K=4096, B=B, seed=3)
     q, s = oracle.quantize(h.x)
@@ -166,6 +166,40 @@ def test_head_planted_max_and_ties(plant):
     assert am[0] == min(plant, tie)
     _, ga, _ = _head_call(T, s_T, V, K, q, s, 1)
     assert ga[0] == am[0]
+
+
+@pytest.mark.parametrize("B,K", [(2, 4144), (9, 1040), (16, 48)])
+def test_head_batched_ragged_k_and_extremes(B, K):
+    # 2..16 vectors take the tensor-core pass: K not a multiple of 64 (a partial last span and
+    # chunk), rows of -128 / 127 against activations of +-127 (the largest chunk sums), and
+    # planted ties between rows for every vector.
+    V = 3001
+    T = synth.int8_uniform(V * K, 11, B).reshape(V, K).copy()
+    T[7] = -128
+    T[8] = 127
+    T[2990] = 127
+    h = wl.head(V=V, K=K, B=B, seed=12)
+    q, s = oracle.quantize(h.x)
+    q[0] = 127
+    q[-1] = -127
+    s_T = np.ones(V, dtype=np.float32)
+    s_T[::3] = 0.5
+    logits, am, _ = oracle.logits_argmax(T, s_T, V, K, q, s)
+    gl, ga, ws = _head_call(T, s_T, V, K, q, s, B)
+    assert_close(gl, logits, "head logits")
+    assert np.array_equal(ga, am)
+    gl2, ga2, _ = _head_call(T, s_T, V, K, q, s, B, ws)
+    assert np.array_equal(ga2, am) and np.array_equal(gl2, gl)
+
+
+def test_head_full_table_batched():
+    # The full table for 8 vectors in one tensor-core pass.
+    h = wl.head(B=8)
+    q, s = oracle.quantize(h.x)
+    logits, am, _ = oracle.logits_argmax(h.T, h.s_T, h.V, h.K, q, s)
+    gl, ga, _ = _head_call(h.T, h.s_T, h.V, h.K, q, s, 8)
+    assert_close(gl, logits, "head full batched")
+    assert np.array_equal(ga, am)
 
 
 def test_head_full_table():
@@ -240,6 +274,22 @@ def test_decode_step_batched_8b_down_projection_shape():
     torch.cuda.synchronize()
     assert plan.nt_decode_step_status() == nt.NT_OK
     _check_step(projs, None, dp, None, B=4)
+    plan.close()
+
+
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_GRAPH, nt.NT_LAUNCH_STREAM])
+@pytest.mark.parametrize("B", [3, 11])
+def test_decode_step_batched_wide_stage(launcher, B):
+    # A stage with enough rows for four CTAs per SM takes K unsplit on the tensor-core batched
+    # path: the sums go from registers straight to y (the split path meets in a workspace).
+    shapes = dict(SMALL, gate=(81920, 1024), up=(81917, 1024))
+    projs = wl.decoder_projections(1, shapes, B=B, seed=9, workload=16)
+    dp, _ = plan_inputs(projs, None, B=B)
+    plan = nt.DecodePlan(1, B, dp, None, nt.NT_STEP_INDEPENDENT, launcher)
+    for _ in range(2):
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    _check_step(projs, None, dp, None, B=B)
     plan.close()
 
 
