@@ -633,7 +633,7 @@ def run_sweep(args):
         print(json.dumps({"metric": "batched decode sweep", "batch": B, "steps": steps,
                           **res[best], "launcher": best, "peak_GBps": peak, "peak_source": peak_kind,
                           "bytes_per_step": nbytes, "by_launcher": res,
-                          "projections": "dp4a (persistent); e4m3 tensor cores (graph, B >= 2)"}), flush=True)
+                          "projections": "dp4a (persistent); f16 mma.sync tensor cores for projections and output projection (graph, B >= 2)"}), flush=True)
 
 
 # ---------------------------------------------------------------------------------------

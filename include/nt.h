@@ -168,6 +168,9 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
  *   ws: nt_int8_logits_workspace_size(V, K, B) bytes of device memory that is zero-filled
  *       before its first use; every call returns it to that state. Calls that share one
  *       workspace must not overlap on the device.
+ * B = 1 streams T through the persistent dp4a kernel; 2 <= B <= 16 reads T once on the
+ * tensor cores (f16 MMA of exactly converted int8 with exact int32 sums); larger B takes
+ * several passes of 16. Logits and arg-max are the same in every case.
  */
 nt_status nt_int8_logits_workspace_size(int V, int K, int B, size_t* bytes);
 nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
