@@ -579,7 +579,7 @@ def run_sweep(args):
     projs, head, dp, hd, _ = build_inputs(torch, nt, dev, L)
     stream = torch.cuda.current_stream()
     peak, peak_kind = measured_peak()
-    for B in (1, 2, 4, 8, 16):
+    for B in args.batches:
         dpB, hosts = [], []
         for p, d in zip(projs, dp):
             layer, name = p.name.split(".")
@@ -597,6 +597,8 @@ def run_sweep(args):
                    argmax=torch.empty(B, dtype=torch.int32, device=dev))
         res = {}
         for lname, launcher in (("persistent", nt.NT_LAUNCH_PERSISTENT), ("graph", nt.NT_LAUNCH_GRAPH)):
+            if lname not in args.launchers:
+                continue
             for d in dpB:
                 d["y"].zero_()
             hdB["logits"].zero_()
@@ -980,6 +982,8 @@ def main():
                          "for small profiling captures)")
     ap.add_argument("--sweep", action="store_true",
                     help="batched sweep B = 1, 2, 4, 8, 16 (one JSON line per batch)")
+    ap.add_argument("--batches", type=lambda v: [int(x) for x in v.split(",")], default=[1, 2, 4, 8, 16],
+                    help="--sweep: batch sizes to run")
     ap.add_argument("--verify", action="store_true",
                     help="speculative verify passes of 2, 4 and 8 positions (gather + step + acceptance)")
     ap.add_argument("--attention", action="store_true",
@@ -991,7 +995,7 @@ def main():
     ap.add_argument("--contexts", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="--attention / --layer-attention: context lengths to run")
     ap.add_argument("--launchers", type=lambda v: v.split(","), default=["persistent", "graph"],
-                    help="--layer-attention: launchers to time (persistent,graph)")
+                    help="--layer-attention, --sweep: launchers to time (persistent,graph)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
     args = ap.parse_args()
