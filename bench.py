@@ -421,7 +421,30 @@ def run_ours(args, rank, world):
     big_bytes = bN * bK // 4 + 4 * bN + bK + 4 * bN + 4
     comp["gemv_per_call_large"] = dict(frac(big_bytes, e0.elapsed_time(e1) * 1e3 / 10), kernel="gemv_tiled_kernel",
                                        what=f"one nt_ternary_gemv call, {bN}x{bK} trits (268 MB), batch 1")
-    del big_w, big_q, big_sw, big_sx, big_y
+    # the same matrix for 8 vectors in one nt_ternary_gemm call: with a workspace on the tensor
+    # cores, without one on the dp4a kernel
+    gB = 8
+    g_q = torch.randint(-127, 128, (gB, bK), dtype=torch.int8, device=dev)
+    g_sx = torch.full((gB,), 0.02, dtype=torch.float32, device=dev)
+    g_y = torch.empty((gB, bN), dtype=torch.float32, device=dev)
+    g_ws = torch.zeros(nt.nt_ternary_gemm_workspace_size(bN, bK, gB, nt.NT_LAYOUT_TILED), dtype=torch.uint8, device=dev)
+    g_us = {}
+    for label, ws in (("tc", g_ws), ("dp4a", None)):
+        for _ in range(3):
+            nt.nt_ternary_gemm(big_w, nt.NT_LAYOUT_TILED, big_sw, bN, bK, g_q, g_sx, gB, g_y, ws=ws, stream=stream)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(10):
+            nt.nt_ternary_gemm(big_w, nt.NT_LAYOUT_TILED, big_sw, bN, bK, g_q, g_sx, gB, g_y, ws=ws, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        g_us[label] = e0.elapsed_time(e1) * 1e3 / 10
+    g_bytes = bN * bK // 4 + 4 * bN + gB * bK + 4 * gB * bN + 4 * gB
+    comp["gemm_per_call_large_b8"] = dict(frac(g_bytes, g_us["tc"]), kernel="gemv_mma_kernel",
+                                          dp4a_us=round(g_us["dp4a"], 2),
+                                          what=f"one nt_ternary_gemm call, {bN}x{bK} trits, batch {gB}, with a "
+                                               "workspace (tensor cores); dp4a_us: the same call without one")
+    del big_w, big_q, big_sw, big_sx, big_y, g_q, g_sx, g_y, g_ws
     hws = torch.empty(nt.nt_int8_logits_workspace_size(head.V, head.K, 1), dtype=torch.uint8, device=dev)
     nt.nt_quantize_act(hd["x"], hd["q"], hd["sx"], stream)
 

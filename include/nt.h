@@ -149,8 +149,14 @@ nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, in
  * With NT_LAYOUT_TILED, B >= 64 and K <= 131072 the call runs on the tensor cores and needs
  * a workspace of nt_ternary_gemm_workspace_size bytes (16-byte aligned device memory; its
  * contents are scratch: bf16 copies of this call's activations and weights, overwritten by
- * the next call that uses it; calls sharing it must not overlap). Otherwise the size is 0
- * and ws may be NULL. A missing or short workspace returns NT_ERR_WORKSPACE.
+ * the next call that uses it; calls sharing it must not overlap). A missing or short
+ * workspace returns NT_ERR_WORKSPACE.
+ * With NT_LAYOUT_TILED and 2 <= B <= 16 the workspace is optional: given one of at least
+ * nt_ternary_gemm_workspace_size bytes (16-byte aligned, zero-filled before its first use;
+ * every call leaves it zero; calls sharing it must not overlap) the call runs on the tensor
+ * cores (f16 MMA of exactly decoded trits, int32 partial sums of K parts meeting in the
+ * workspace); with ws NULL or short it runs the dp4a kernel. Otherwise the size is 0 and ws
+ * may be NULL.
  */
 nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes);
 nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,

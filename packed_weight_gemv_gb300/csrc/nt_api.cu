@@ -150,7 +150,9 @@ nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t
     return set_error(NT_ERR_INVALID_ARG, "need N >= 1, B >= 1 and K a positive multiple of 16");
   if (layout != NT_LAYOUT_PLAIN && layout != NT_LAYOUT_TILED)
     return set_error(NT_ERR_INVALID_ARG, "layout must be NT_LAYOUT_PLAIN or NT_LAYOUT_TILED");
-  *bytes = (layout == NT_LAYOUT_TILED && tc_gemm_supported(B, K)) ? tc_gemm_workspace_bytes(B, N, K) : 0;
+  *bytes = 0;
+  if (layout == NT_LAYOUT_TILED && tc_gemm_supported(B, K)) *bytes = tc_gemm_workspace_bytes(B, N, K);
+  else if (layout == NT_LAYOUT_TILED && B >= kMmaMinBatch && B <= kMmaMaxBatch) *bytes = mma_single_ws_bytes(N, K, B);
   return NT_OK;
 }
 
@@ -170,6 +172,9 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
                              as_stream(stream));
   if (tc)  // prefill-shaped batch: tensor cores
     return launch_gemm_tc(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws, as_stream(stream));
+  if (B >= kMmaMinBatch && B <= kMmaMaxBatch && ws && aligned(ws, 16) && ws_bytes >= mma_single_ws_bytes(N, K, B))
+    return launch_gemv_mma_single(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws,
+                                  as_stream(stream));  // a few vectors with a workspace: tensor cores
   MatDesc m{};
   m.w = static_cast<const uint8_t*>(w);
   m.s_w = s_w;

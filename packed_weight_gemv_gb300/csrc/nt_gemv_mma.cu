@@ -95,20 +95,20 @@ __device__ __forceinline__ uint4 ld_group(const uint8_t* p) {
 // current one is multiplied. Dynamic shared memory: two activation buffers.
 template <int NT>
 __global__ void __launch_bounds__(kMmaThreads, 2) gemv_mma_kernel(const MmaMat* __restrict__ mats, int n_mats,
-                                                                 const uint16_t* __restrict__ cta_mat) {
+                                                                 const uint16_t* __restrict__ cta_mat, const MmaMat one) {
   extern __shared__ __align__(16) uint2 sB[];  // [2][NT][kChunkBlocks][32]: per lane 4 f16 activations
   __shared__ int s_last;
   dependent_launch_wait();
   int lo = 0, hi = n_mats - 1;  // this CTA's matrix: from the table, else the last whose first CTA <= it
   if (cta_mat) {
     lo = __ldg(cta_mat + blockIdx.x);
-  } else {
+  } else if (mats) {
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (mats[mid].cta_begin <= (int64_t)blockIdx.x) lo = mid; else hi = mid - 1;
     }
   }
-  const MmaMat m = mats[lo];
+  const MmaMat m = mats ? mats[lo] : one;  // a single matrix comes by value
   const int li = (int)(blockIdx.x - m.cta_begin);
   const int part = li / m.ugroups, ug = li - part * m.ugroups;
   const int64_t Kp = padded_k(m.K);
@@ -513,24 +513,64 @@ size_t mma_ws_bytes(int64_t rows, int64_t groups, int B) {
   return sizeof(int32_t) * (size_t)(B * rows) + sizeof(unsigned int) * (size_t)groups;
 }
 
-nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,
-                          cudaStream_t st, bool pdl) {
-  if (max_B < 1 || max_B > kMmaMaxBatch) return set_error(NT_ERR_INVALID_ARG, "batched tensor-core path: 1 <= B <= 16");
-  const int nt = max_B <= 8 ? 1 : 2;
-  auto kern = nt == 1 ? gemv_mma_kernel<1> : gemv_mma_kernel<2>;
-  const size_t smem = sizeof(uint2) * 2 * nt * kChunkBlocks * 32;  // 32 KB per vector tile
-  static std::atomic<int> attr_set[64];  // per device: the activation buffers allowed for both tile counts
+// dynamic shared memory of gemv_mma_kernel<nt>: two activation buffers of 16 KB per vector tile
+static size_t gemv_smem_bytes(int nt) { return sizeof(uint2) * 2 * nt * kChunkBlocks * 32; }
+static nt_status gemv_mma_attrs() {
+  static std::atomic<int> attr_set[64];  // per device: the buffers allowed for both tile counts
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return set_error(NT_ERR_CUDA, "device index out of range");
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(sizeof(uint2) * 2 * 1 * kChunkBlocks * 32)));
-    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(sizeof(uint2) * 2 * 2 * kChunkBlocks * 32)));
+    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_mma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem_bytes(1)));
+    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_mma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem_bytes(2)));
     attr_set[dev].store(1, std::memory_order_release);
   }
-  NT_CUDA_TRY(launch_kernel(kern, dim3((unsigned)total_ctas), dim3(kMmaThreads), smem, st, pdl, d_mats, n_mats, d_cta_mat));
+  return NT_OK;
+}
+
+nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,
+                          cudaStream_t st, bool pdl) {
+  if (max_B < 1 || max_B > kMmaMaxBatch) return set_error(NT_ERR_INVALID_ARG, "batched tensor-core path: 1 <= B <= 16");
+  const int nt = max_B <= 8 ? 1 : 2;
+  NT_TRY(gemv_mma_attrs());
+  auto kern = nt == 1 ? gemv_mma_kernel<1> : gemv_mma_kernel<2>;
+  NT_CUDA_TRY(launch_kernel(kern, dim3((unsigned)total_ctas), dim3(kMmaThreads), gemv_smem_bytes(nt), st, pdl, d_mats,
+                            n_mats, d_cta_mat, MmaMat{}));
+  return check_launch("gemv_mma_kernel");
+}
+
+// One matrix per call (nt_ternary_gemm): the descriptor goes by value; K is split until the
+// call has 8 waves of CTAs (or one chunk per part), the parts meeting in the caller's workspace.
+size_t mma_single_ws_bytes(int N, int K, int B) {
+  MmaMat m{};
+  m.N = N;
+  m.K = K;
+  mma_geometry(m, 1);
+  return (mma_ws_bytes(N, m.ugroups, B) + 15) & ~(size_t)15;
+}
+nt_status launch_gemv_mma_single(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
+                                 int B, float* y, int32_t* acc, void* ws, cudaStream_t st) {
+  if (B < kMmaMinBatch || B > kMmaMaxBatch) return set_error(NT_ERR_INVALID_ARG, "batched tensor-core path: 2 <= B <= 16");
+  MmaMat m{};
+  m.w = w;
+  m.s_w = s_w;
+  m.q = q;
+  m.s_x = s_x;
+  m.y = y;
+  m.acc = acc;
+  m.N = N;
+  m.K = K;
+  m.B = B;
+  mma_geometry(m, 1);
+  for (int parts = 2; mma_ctas(m) < 8LL * device_sm_count() && parts <= 2 * m.kchunks; parts *= 2) mma_geometry(m, parts);
+  m.acc_ws = static_cast<int32_t*>(ws);
+  m.cnt = reinterpret_cast<unsigned int*>(static_cast<int32_t*>(ws) + (size_t)B * N);
+  m.cta_begin = 0;
+  const int nt = B <= 8 ? 1 : 2;
+  NT_TRY(gemv_mma_attrs());
+  auto kern = nt == 1 ? gemv_mma_kernel<1> : gemv_mma_kernel<2>;
+  NT_CUDA_TRY(launch_kernel(kern, dim3((unsigned)mma_ctas(m)), dim3(kMmaThreads), gemv_smem_bytes(nt), st, false,
+                            (const MmaMat*)nullptr, 0, (const uint16_t*)nullptr, m));
   return check_launch("gemv_mma_kernel");
 }
 

@@ -106,6 +106,11 @@ int64_t mma_ctas(const MmaMat& m);
 size_t mma_ws_bytes(int64_t rows, int64_t groups, int B);
 nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_cta_mat, int64_t total_ctas, int max_B,
                           cudaStream_t st, bool pdl = false);
+// One tiled matrix per call on the same path (nt_ternary_gemm with a workspace of
+// mma_single_ws_bytes, zero before its first use and left zero).
+size_t mma_single_ws_bytes(int N, int K, int B);
+nt_status launch_gemv_mma_single(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
+                                 int B, float* y, int32_t* acc, void* ws, cudaStream_t st);
 // Output projection on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, one pass over T.
 nt_status launch_head_mma(const int8_t* T, const float* s_T, int V, int K, const int8_t* q, const float* s_x,
                           int B, float* logits, int32_t* argmax, HeadWs* ws, cudaStream_t st);

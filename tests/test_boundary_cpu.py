@@ -66,7 +66,13 @@ def test_argument_errors_without_gpu(lib):
     # the tensor-core path (tiled, B >= 64) needs a workspace: refused before any device call
     assert _gemv(lib, 0x10000, 1, 256, 512, 0x20000, 0x30000, B=64) == nt.NT_ERR_WORKSPACE
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == 64 * 512 * 2 + 256 * 512 * 2
-    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == 0
+    # 2..16 vectors: an optional workspace of int32 partial sums [B][N] and one counter per
+    # group of 256 rows, rounded up to 16 bytes; none for one vector or above 16
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == (16 * 256 * 4 + 4 + 15) // 16 * 16
+    assert nt.nt_ternary_gemm_workspace_size(1000, 512, 3, nt.NT_LAYOUT_TILED) == (3 * 1000 * 4 + 4 * 4 + 15) // 16 * 16
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 1, nt.NT_LAYOUT_TILED) == 0
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 17, nt.NT_LAYOUT_TILED) == 0
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_PLAIN) == 0
     assert b"multiple of 16" in lib.nt_last_error_string() or True
     vp = ctypes.c_void_p
     assert lib.nt_quantize_act(None, 1, 16, vp(0x100), vp(0x200), None) == nt.NT_ERR_INVALID_ARG
