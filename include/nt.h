@@ -153,10 +153,11 @@ nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, in
  * workspace returns NT_ERR_WORKSPACE.
  * With NT_LAYOUT_TILED and 2 <= B <= 16 the workspace is optional: given one of at least
  * nt_ternary_gemm_workspace_size bytes (16-byte aligned, zero-filled before its first use;
- * every call leaves it zero; calls sharing it must not overlap) the call runs on the tensor
- * cores (f16 MMA of exactly decoded trits, int32 partial sums of K parts meeting in the
- * workspace); with ws NULL or short it runs the dp4a kernel. Otherwise the size is 0 and ws
- * may be NULL.
+ * calls sharing it must not overlap) the call runs on the tensor cores: from N >= 128 on
+ * tcgen05 with the decoded trits in tensor memory (e4m3) and the activations split exactly
+ * into two e4m3 digits kept in the workspace, below that f16 mma.sync; int32 partial sums of
+ * K parts meet in the workspace, which every call leaves zero apart from the digit rows.
+ * With ws NULL or short it runs the dp4a kernel. Otherwise the size is 0 and ws may be NULL.
  */
 nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes);
 nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,

@@ -152,7 +152,8 @@ nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t
     return set_error(NT_ERR_INVALID_ARG, "layout must be NT_LAYOUT_PLAIN or NT_LAYOUT_TILED");
   *bytes = 0;
   if (layout == NT_LAYOUT_TILED && tc_gemm_supported(B, K)) *bytes = tc_gemm_workspace_bytes(B, N, K);
-  else if (layout == NT_LAYOUT_TILED && B >= kMmaMinBatch && B <= kMmaMaxBatch) *bytes = mma_single_ws_bytes(N, K, B);
+  else if (layout == NT_LAYOUT_TILED && B >= kMmaMinBatch && B <= kMmaMaxBatch)
+    *bytes = tc8_supported(N, K, B) ? tc8_ws_bytes(N, K, B) : mma_single_ws_bytes(N, K, B);
   return NT_OK;
 }
 
@@ -172,6 +173,9 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
                              as_stream(stream));
   if (tc)  // prefill-shaped batch: tensor cores
     return launch_gemm_tc(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws, as_stream(stream));
+  if (tc8_supported(N, K, B) && ws && aligned(ws, 16) && ws_bytes >= tc8_ws_bytes(N, K, B))
+    return launch_gemv_tc8(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws,
+                           as_stream(stream));  // a few vectors with a workspace: tcgen05
   if (B >= kMmaMinBatch && B <= kMmaMaxBatch && ws && aligned(ws, 16) && ws_bytes >= mma_single_ws_bytes(N, K, B))
     return launch_gemv_mma_single(static_cast<const uint8_t*>(w), s_w, N, K, q, s_x, B, y, acc_opt, ws,
                                   as_stream(stream));  // a few vectors with a workspace: tensor cores

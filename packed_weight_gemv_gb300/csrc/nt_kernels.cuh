@@ -111,6 +111,13 @@ nt_status launch_gemv_mma(const MmaMat* d_mats, int n_mats, const uint16_t* d_ct
 size_t mma_single_ws_bytes(int N, int K, int B);
 nt_status launch_gemv_mma_single(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
                                  int B, float* y, int32_t* acc, void* ws, cudaStream_t st);
+// One tiled matrix per call on tcgen05 (nt_gemv_tc8.cu): decoded weights in tensor memory,
+// e4m3 digits of the activations; 2..16 vectors and at least 128 rows; workspace of
+// tc8_ws_bytes (zero before its first use and left zero except for the digit rows).
+bool tc8_supported(int N, int K, int B);
+size_t tc8_ws_bytes(int N, int K, int B);
+nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x, int B,
+                          float* y, int32_t* acc, void* ws, cudaStream_t st);
 // Output projection on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, one pass over T.
 nt_status launch_head_mma(const int8_t* T, const float* s_T, int V, int K, const int8_t* q, const float* s_x,
                           int B, float* logits, int32_t* argmax, HeadWs* ws, cudaStream_t st);

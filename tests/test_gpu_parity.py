@@ -130,24 +130,27 @@ def test_gemm(layout, B):
 
 
 @pytest.mark.parametrize("B,N,K", [(2, 260, 1024), (3, 33, 1040), (8, 4096, 4096), (9, 1024, 12288),
-                                   (16, 70001, 512), (5, 4, 16)])
+                                   (16, 70001, 512), (5, 4, 16), (4, 128, 16), (7, 131, 208), (12, 300, 131072)])
 def test_gemm_small_batch_tensor_cores(B, N, K):
-    # Tiled weights, 2..16 vectors and a workspace: one pass on the tensor cores; K parts meet
-    # in the workspace (left zero), a wide matrix runs K unsplit. Bit-exact sums.
+    # Tiled weights, 2..16 vectors and a workspace: one pass on the tensor cores (tcgen05 with
+    # the decoded weights in tensor memory from 128 rows on, mma.sync below); K parts meet in
+    # the workspace, a wide matrix runs K unsplit; K of 16 / 208 (partial K-blocks) and
+    # 131,072. Bit-exact sums.
     p = wl.projection(8, 2, B, N, K, B, seed=21)
-    q, s = oracle.quantize(p.x)
-    acc, y, _ = oracle.gemm(p.w_plain, p.s_w, N, K, q, s)
     nbytes = nt.nt_ternary_gemm_workspace_size(N, K, B, nt.NT_LAYOUT_TILED)
     assert nbytes > 0
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     w = tiled(p.w_plain, N, K)
-    for _ in range(2):  # the second call reuses the workspace as the first left it
+    for x in (p.x, -0.5 * p.x[::-1].copy()):  # the second call reuses the workspace as the first left it
+        q, s = oracle.quantize(x)
+        q[0, :min(K, 64)] = 127  # extreme codes: digits (7, 15)
+        q[-1, :min(K, 64)] = -127  # digits (-8, 1)
+        acc, y, _ = oracle.gemm(p.w_plain, p.s_w, N, K, q, s)
         gy = torch.full((B, N), float("nan"), device=DEV)
         gacc = torch.empty((B, N), dtype=torch.int32, device=DEV)
         nt.nt_ternary_gemm(w, nt.NT_LAYOUT_TILED, dev(p.s_w), N, K, dev(q), dev(s), B, gy, gacc, ws)
         assert np.array_equal(host(gacc), acc)
         assert_close(host(gy), y, f"gemm B={B}")
-        assert not host(ws).any()
 
 
 # ---- int8 output projection ------------------------------------------------------------
