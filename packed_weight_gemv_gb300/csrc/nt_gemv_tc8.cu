@@ -19,7 +19,7 @@
 //                     (N x 128 bytes) into a ring of kStages stages (full / empty mbarriers);
 //   warps 0-3      -- decoders, one thread per weight row (tensor-memory lane = row): 8
 //                     shared loads of its row's words per K-block (conflict-free thanks to the
-//                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into one of two A buffers;
+//                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into one of three A buffers;
 //   warp 5 lane 0  -- MMA issuer: 4 x tcgen05.mma (M 128, N 16/32, K 32) per K-block, commits
 //                     release the stage and the A buffer;
 //   epilogue       -- the decoders read the accumulator (tcgen05.ld), then y = fl(fl(acc) s_w) s_x
@@ -46,7 +46,8 @@ constexpr int kTc8Stages = 8;
 constexpr int kTc8WBytes = kTc8Tiles * kTc8KB;  // weight box: 4 KB
 constexpr int kTc8Threads = 192;
 constexpr int kTc8Decoders = 128;
-constexpr int kTc8TmemCols = 128;              // D at column 0 (<= 32), A buffers at 32 and 64
+constexpr int kTc8TmemCols = 128;              // D at column 0 (<= 32), A buffers at 32, 64, 96
+constexpr int kTc8ABufs = 3;
 constexpr uint64_t kTc8TimeoutNs = 2000000000ull;
 constexpr int64_t kTc8MaxPartK = 131072;       // |D| <= 15 K < 2^24
 
@@ -77,13 +78,23 @@ __device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test, the thread suspended (up to 0.1 ms) until the phase completes.
+__device__ __forceinline__ bool bar_try_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(100000u)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait; false after the timeout or once another role of the CTA has given up.
 __device__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
   if (bar_try(bar, parity)) return true;
   const uint64_t deadline = globaltimer_ns() + kTc8TimeoutNs;
-  for (uint32_t it = 1;; ++it) {
-    if (bar_try(bar, parity)) return true;
-    if ((it & 255u) == 0u && (*fail || globaltimer_ns() > deadline)) {
+  for (;;) {
+    if (bar_try_sleep(bar, parity)) return true;
+    if (*fail || globaltimer_ns() > deadline) {
       *fail = 1;
       return false;
     }
@@ -130,8 +141,8 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTc8Stages * kStageBytes);
   const uint32_t full0 = s_u32(bars), empty0 = full0 + 8 * kTc8Stages;
-  const uint32_t afull0 = empty0 + 8 * kTc8Stages, aempty0 = afull0 + 16, dfull = aempty0 + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kTc8Stages + 5);
+  const uint32_t afull0 = empty0 + 8 * kTc8Stages, aempty0 = afull0 + 8 * kTc8ABufs, dfull = aempty0 + 8 * kTc8ABufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kTc8Stages + 2 * kTc8ABufs + 1);
   volatile int* fail = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -146,7 +157,7 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
       bar_init(full0 + 8 * s, 1);
       bar_init(empty0 + 8 * s, kTc8Decoders + 1);  // the decoders' reads and the MMAs' commit
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kTc8ABufs; ++b) {
       bar_init(afull0 + 8 * b, kTc8Decoders);
       bar_init(aempty0 + 8 * b, 1);
     }
@@ -183,9 +194,9 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3(NN);
       for (int i = 0; i < nkb; ++i) {
-        const int s = i % kTc8Stages, b = i & 1;
+        const int s = i % kTc8Stages, b = i % kTc8ABufs;
         if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail)) break;
-        if (!bar_wait(afull0 + 8 * b, (i >> 1) & 1u, fail)) break;
+        if (!bar_wait(afull0 + 8 * b, (i / kTc8ABufs) & 1u, fail)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t bsm = s_u32(smem + s * kStageBytes + kTc8WBytes);
 #pragma unroll
@@ -211,7 +222,7 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
     const int T = row >> 2, j = row & 3;  // tile within the CTA's 32, row within the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
     for (int i = 0; i < nkb; ++i) {
-      const int s = i % kTc8Stages, b = i & 1;
+      const int s = i % kTc8Stages, b = i % kTc8ABufs;
       if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail)) break;
       // the row's 8 words of the K-block: 16-byte chunk g of box row T sits at chunk g ^ (T % 8)
       const uint8_t* ws = smem + s * kStageBytes + T * kTc8KB + 4 * j;
@@ -219,25 +230,20 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
 #pragma unroll
       for (int g = 0; g < 8; ++g) w[g] = *reinterpret_cast<const uint32_t*>(ws + ((g ^ (T & 7)) << 4));
       bar_arrive(empty0 + 8 * s);  // release: the reads above are ordered before it
-      uint32_t r[32];              // e4m3 bytes of trits 0..127 of the block, in order
+      if (i >= kTc8ABufs && !bar_wait(aempty0 + 8 * b, ((i / kTc8ABufs) - 1) & 1u, fail)) break;
+      // e4m3 bytes of the block's trits 16 g .. 16 g + 15 into columns 4 g .. 4 g + 3 of the A buffer
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         const uint32_t hi = w[g] >> 16;
-        r[4 * g + 0] = prmt(kE4PoolA_lo, kE4PoolA_hi, w[g]);
-        r[4 * g + 1] = prmt(kE4PoolB_lo, kE4PoolB_hi, w[g]) & 0xB8B8B8B8u;
-        r[4 * g + 2] = prmt(kE4PoolA_lo, kE4PoolA_hi, hi);
-        r[4 * g + 3] = prmt(kE4PoolB_lo, kE4PoolB_hi, hi) & 0xB8B8B8B8u;
+        const uint32_t r0 = prmt(kE4PoolA_lo, kE4PoolA_hi, w[g]);
+        const uint32_t r1 = prmt(kE4PoolB_lo, kE4PoolB_hi, w[g]) & 0xB8B8B8B8u;
+        const uint32_t r2 = prmt(kE4PoolA_lo, kE4PoolA_hi, hi);
+        const uint32_t r3 = prmt(kE4PoolB_lo, kE4PoolB_hi, hi) & 0xB8B8B8B8u;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         tl + 32u + 32u * (uint32_t)b + 4u * (uint32_t)g),
+                     "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                     : "memory");
       }
-      if (i >= 2 && !bar_wait(aempty0 + 8 * b, ((i >> 1) - 1) & 1u, fail)) break;
-      asm volatile(
-          "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-          "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
-              tl + 32u + 32u * (uint32_t)b),
-          "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-          "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-          "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-          "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-          : "memory");
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       bar_arrive(afull0 + 8 * b);
