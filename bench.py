@@ -440,7 +440,7 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         g_us[label] = e0.elapsed_time(e1) * 1e3 / 10
     g_bytes = bN * bK // 4 + 4 * bN + gB * bK + 4 * gB * bN + 4 * gB
-    comp["gemm_per_call_large_b8"] = dict(frac(g_bytes, g_us["tc"]), kernel="gemv_mma_kernel",
+    comp["gemm_per_call_large_b8"] = dict(frac(g_bytes, g_us["tc"]), kernel="gemv_tc8_kernel",
                                           dp4a_us=round(g_us["dp4a"], 2),
                                           what=f"one nt_ternary_gemm call, {bN}x{bK} trits, batch {gB}, with a "
                                                "workspace (tensor cores); dp4a_us: the same call without one")
