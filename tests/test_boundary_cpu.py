@@ -66,10 +66,15 @@ def test_argument_errors_without_gpu(lib):
     # the tensor-core path (tiled, B >= 64) needs a workspace: refused before any device call
     assert _gemv(lib, 0x10000, 1, 256, 512, 0x20000, 0x30000, B=64) == nt.NT_ERR_WORKSPACE
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == 64 * 512 * 2 + 256 * 512 * 2
-    # 2..16 vectors: an optional workspace of int32 partial sums [B][N] and one counter per
-    # group of 256 rows, rounded up to 16 bytes; none for one vector or above 16
-    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == (16 * 256 * 4 + 4 + 15) // 16 * 16
-    assert nt.nt_ternary_gemm_workspace_size(1000, 512, 3, nt.NT_LAYOUT_TILED) == (3 * 1000 * 4 + 4 * 4 + 15) // 16 * 16
+    # 2..16 vectors, from 128 rows: an optional workspace of e4m3 digit rows (16 for B <= 8,
+    # else 32, K rounded up to 128), int32 partial sums [B][N] and one counter per 128-row
+    # tile, rounded up to 16 bytes; below 128 rows sums and one counter per 256 rows; none for
+    # one vector or above 16
+    r16 = lambda b: (b + 15) // 16 * 16  # noqa: E731
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == r16(32 * 512 + 16 * 256 * 4 + 2 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(1000, 512, 3, nt.NT_LAYOUT_TILED) == r16(16 * 512 + 3 * 1000 * 4 + 8 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(1000, 208, 3, nt.NT_LAYOUT_TILED) == r16(16 * 256 + 3 * 1000 * 4 + 8 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(100, 512, 3, nt.NT_LAYOUT_TILED) == (3 * 100 * 4 + 4 + 15) // 16 * 16
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 1, nt.NT_LAYOUT_TILED) == 0
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 17, nt.NT_LAYOUT_TILED) == 0
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_PLAIN) == 0
