@@ -32,7 +32,9 @@
 
 #include <algorithm>
 
+#include <climits>
 #include <mutex>
+#include <vector>
 #include <string>
 
 #include "nt_kernels.cuh"
@@ -132,10 +134,20 @@ struct Tc8Params {
   int kblocks;       // 128-trit blocks of padded K
   int kb_per_part, nparts;
 };
+struct Tc8Mat {
+  CUtensorMap tmW;   // the tiles, box 128 bytes x 32 tiles
+  CUtensorMap tmD;   // the digit rows, box 128 bytes x NN rows
+  Tc8Params p;
+  int64_t cta_begin;  // first CTA of this matrix in its launch
+};
 
+// One CTA's work: 128-row tile `cta % mtiles` over K part `cta / mtiles` of the matrix whose
+// maps and parameters are given (kernel parameters for one call, global memory for a plan).
 template <int NN>
-__global__ void __launch_bounds__(kTc8Threads, 1)
-    gemv_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmD, const Tc8Params p) {
+__device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorMap* tmD_, const Tc8Params& p, int cta,
+                                        bool global_maps) {
+  const CUtensorMap& tmW = *tmW_;
+  const CUtensorMap& tmD = *tmD_;
   constexpr int kStageBytes = kTc8WBytes + NN * kTc8KB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
   int* s_last = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const int mtile = blockIdx.x % p.mtiles, part = blockIdx.x / p.mtiles;
+  const int mtile = cta % p.mtiles, part = cta / p.mtiles;
   const int kb0 = part * p.kb_per_part;
   const int nkb = (p.kblocks - kb0 < p.kb_per_part) ? p.kblocks - kb0 : p.kb_per_part;
 
@@ -179,6 +191,10 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
   if (warp == 4) {
     // ---- TMA producer: weight box and digit box of every K-block of the part ----
     if (lane == 0) {
+      if (global_maps) {  // maps written to global memory before the launch: make them visible to the TMA
+        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmW_) : "memory");
+        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmD_) : "memory");
+      }
       for (int i = 0; i < nkb; ++i) {
         const int s = i % kTc8Stages;
         if (i >= kTc8Stages && !bar_wait(empty0 + 8 * s, ((i / kTc8Stages) - 1) & 1u, fail)) break;
@@ -326,17 +342,32 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
   if (t == 0) p.cnt[mtile] = 0u;
 }
 
+template <int NN>
+__global__ void __launch_bounds__(kTc8Threads, 1)
+    gemv_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmD, const Tc8Params p) {
+  tc8_cta<NN>(&tmW, &tmD, p, (int)blockIdx.x, false);
+}
+
+// Several matrices in one launch (a decode plan's stage): CTA -> matrix from the table; the
+// matrices' tensor maps live in global memory (written before the plan's first launch).
+template <int NN>
+__global__ void __launch_bounds__(kTc8Threads, 1)
+    gemv_tc8_multi_kernel(const Tc8Mat* __restrict__ mats, const uint16_t* __restrict__ cta_mat) {
+  const Tc8Mat* m = mats + __ldg(cta_mat + blockIdx.x);
+  const Tc8Params p = m->p;
+  tc8_cta<NN>(&m->tmW, &m->tmD, p, (int)(blockIdx.x - m->cta_begin), true);
+}
+
 // e4m3 codes of the integers 0..15 (2^(e-7) (1 + m/8)); a negative digit sets bit 7
 __constant__ uint8_t kE4Int[16] = {0x00, 0x38, 0x40, 0x44, 0x48, 0x4A, 0x4C, 0x4E,
                                    0x50, 0x51, 0x52, 0x53, 0x54, 0x55, 0x56, 0x57};
 
 // Digit rows of the activations: row 2 v is h = q >> 4, row 2 v + 1 is l = q & 15 of vector v,
 // as e4m3 bytes, K padded with zeros to Kd; rows of vectors >= B are zero.
-__global__ void __launch_bounds__(256) tc8_digits_kernel(const int8_t* __restrict__ q, int B, int K, int Kd, int NN,
-                                                         uint8_t* __restrict__ out) {
-  dependent_launch_wait();
+__device__ __forceinline__ void tc8_digits_range(const int8_t* __restrict__ q, int B, int K, int Kd, int NN,
+                                                 uint8_t* __restrict__ out, int64_t first, int64_t stride) {
   const int64_t n4 = (int64_t)NN * Kd / 4;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t i = first; i < n4; i += stride) {
     const int64_t e = 4 * i;
     const int n = (int)(e / Kd), k = (int)(e - (int64_t)n * Kd);
     const int v = n >> 1, hi = (n & 1) == 0;
@@ -353,6 +384,24 @@ __global__ void __launch_bounds__(256) tc8_digits_kernel(const int8_t* __restric
     }
     *reinterpret_cast<uint32_t*>(out + e) = o;
   }
+}
+__global__ void __launch_bounds__(256) tc8_digits_kernel(const int8_t* __restrict__ q, int B, int K, int Kd, int NN,
+                                                         uint8_t* __restrict__ out) {
+  dependent_launch_wait();
+  tc8_digits_range(q, B, K, Kd, NN, out, blockIdx.x * (int64_t)blockDim.x + threadIdx.x,
+                   (int64_t)gridDim.x * blockDim.x);
+}
+// one job per matrix of a plan (blockIdx.y)
+struct Tc8DigitJob {
+  const int8_t* q;
+  uint8_t* out;
+  int B, K, Kd, NN;
+};
+__global__ void __launch_bounds__(256) tc8_digits_multi_kernel(const Tc8DigitJob* __restrict__ jobs) {
+  dependent_launch_wait();
+  const Tc8DigitJob j = jobs[blockIdx.y];
+  tc8_digits_range(j.q, j.B, j.K, j.Kd, j.NN, j.out, blockIdx.x * (int64_t)blockDim.x + threadIdx.x,
+                   (int64_t)gridDim.x * blockDim.x);
 }
 
 // ---- host ----------------------------------------------------------------------------
@@ -377,6 +426,10 @@ nt_status tc8_setup(int dev) {
   if (dev >= 0 && dev < 64 && !g_tc8_attr[dev]) {
     NT_CUDA_TRY(cudaFuncSetAttribute(gemv_tc8_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc8_smem(16)));
     NT_CUDA_TRY(cudaFuncSetAttribute(gemv_tc8_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc8_smem(32)));
+    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_tc8_multi_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)tc8_smem(16)));
+    NT_CUDA_TRY(cudaFuncSetAttribute(gemv_tc8_multi_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)tc8_smem(32)));
     g_tc8_attr[dev] = true;
   }
   return NT_OK;
@@ -407,26 +460,18 @@ size_t tc8_ws_bytes(int N, int K, int B) {
   return (digits + sizeof(int32_t) * (size_t)B * N + sizeof(unsigned int) * (size_t)tc8_mtiles(N) + 15) & ~(size_t)15;
 }
 
-nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x, int B,
-                          float* y, int32_t* acc, void* ws, cudaStream_t st) {
-  if (!tc8_supported(N, K, B)) return set_error(NT_ERR_INVALID_ARG, "tcgen05 batched path: 2 <= B <= 16, N >= 128");
-  int dev = 0;
-  NT_CUDA_TRY(cudaGetDevice(&dev));
-  NT_TRY(tc8_setup(dev));
+// Maps and parameters of one matrix: K in `parts` parts (at least enough for exact fp32
+// sums, at most one per K-block); digits: its digit rows [nn][Kd]; acc_ws / cnt: partial sums
+// [B][N] and one counter per 128-row tile (used when K is split).
+static nt_status tc8_matrix(const uint8_t* w, const float* s_w, int N, int K, const float* s_x, int B, float* y,
+                            int32_t* acc, uint8_t* digits, int32_t* acc_ws, unsigned int* cnt, int64_t parts,
+                            Tc8Mat* m) {
   const int nn = tc8_nn(B);
-  const int64_t Kd = tc8_kd(K), Kp = padded_k(K), mtiles = tc8_mtiles(N);
-  uint8_t* digits = static_cast<uint8_t*>(ws);
-  int32_t* acc_ws = reinterpret_cast<int32_t*>(digits + (size_t)nn * Kd);
-  unsigned int* cnt = reinterpret_cast<unsigned int*>(acc_ws + (size_t)B * N);
-  {
-    const int64_t n4 = nn * Kd / 4;
-    const int grid = (int)std::min<int64_t>((n4 + 255) / 256, 4LL * device_sm_count());
-    NT_CUDA_TRY(launch_kernel(tc8_digits_kernel, dim3(grid), dim3(256), 0, st, false, q, B, K, (int)Kd, nn, digits));
-  }
-  CUtensorMap mw, md;
-  NT_TRY(tc8_map(&mw, w, padded_rows(N) / 4, Kp, kTc8Tiles));
-  NT_TRY(tc8_map(&md, digits, nn, Kd, nn));
-  Tc8Params p{};
+  const int64_t Kd = tc8_kd(K), Kp = padded_k(K);
+  NT_TRY(tc8_map(&m->tmW, w, padded_rows(N) / 4, Kp, kTc8Tiles));
+  NT_TRY(tc8_map(&m->tmD, digits, nn, Kd, nn));
+  Tc8Params& p = m->p;
+  p = Tc8Params{};
   p.s_w = s_w;
   p.s_x = s_x;
   p.y = y;
@@ -435,17 +480,129 @@ nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, cons
   p.cnt = cnt;
   p.N = N;
   p.B = B;
-  p.mtiles = (int)mtiles;
+  p.mtiles = (int)tc8_mtiles(N);
   p.kblocks = (int)(Kp / kTc8KB);
-  // K parts: enough CTAs for every SM (four resident per SM), each part at most kTc8MaxPartK
-  int64_t parts = (Kp + kTc8MaxPartK - 1) / kTc8MaxPartK;
-  while (mtiles * parts < 4LL * device_sm_count() && parts * 8 <= p.kblocks) parts *= 2;
+  parts = std::max<int64_t>(parts, (Kp + kTc8MaxPartK - 1) / kTc8MaxPartK);
+  parts = std::min<int64_t>(parts, p.kblocks);
   p.kb_per_part = (int)((p.kblocks + parts - 1) / parts);
   p.nparts = (p.kblocks + p.kb_per_part - 1) / p.kb_per_part;
-  const dim3 grid((unsigned)(mtiles * p.nparts));
-  if (nn == 16) NT_CUDA_TRY(launch_kernel(gemv_tc8_kernel<16>, grid, dim3(kTc8Threads), tc8_smem(16), st, true, mw, md, p));
-  else NT_CUDA_TRY(launch_kernel(gemv_tc8_kernel<32>, grid, dim3(kTc8Threads), tc8_smem(32), st, true, mw, md, p));
+  return NT_OK;
+}
+// K parts for a launch of `mtiles` row tiles: doubled while there are fewer than four CTAs per
+// SM and every part keeps at least 8 K-blocks.
+static int64_t tc8_parts(int64_t mtiles, int64_t min_kblocks) {
+  int64_t parts = 1;
+  while (mtiles * parts < 4LL * device_sm_count() && parts * 2 * 8 <= min_kblocks) parts *= 2;
+  return parts;
+}
+
+nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x, int B,
+                          float* y, int32_t* acc, void* ws, cudaStream_t st) {
+  if (!tc8_supported(N, K, B)) return set_error(NT_ERR_INVALID_ARG, "tcgen05 batched path: 2 <= B <= 16, N >= 128");
+  int dev = 0;
+  NT_CUDA_TRY(cudaGetDevice(&dev));
+  NT_TRY(tc8_setup(dev));
+  const int nn = tc8_nn(B);
+  const int64_t Kd = tc8_kd(K), mtiles = tc8_mtiles(N);
+  uint8_t* digits = static_cast<uint8_t*>(ws);
+  int32_t* acc_ws = reinterpret_cast<int32_t*>(digits + (size_t)nn * Kd);
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(acc_ws + (size_t)B * N);
+  {
+    const int64_t n4 = nn * Kd / 4;
+    const int grid = (int)std::min<int64_t>((n4 + 255) / 256, 4LL * device_sm_count());
+    NT_CUDA_TRY(launch_kernel(tc8_digits_kernel, dim3(grid), dim3(256), 0, st, false, q, B, K, (int)Kd, nn, digits));
+  }
+  Tc8Mat m;
+  NT_TRY(tc8_matrix(w, s_w, N, K, s_x, B, y, acc, digits, acc_ws, cnt, tc8_parts(mtiles, padded_k(K) / kTc8KB), &m));
+  const dim3 grid((unsigned)(mtiles * m.p.nparts));
+  if (nn == 16)
+    NT_CUDA_TRY(launch_kernel(gemv_tc8_kernel<16>, grid, dim3(kTc8Threads), tc8_smem(16), st, true, m.tmW, m.tmD, m.p));
+  else
+    NT_CUDA_TRY(launch_kernel(gemv_tc8_kernel<32>, grid, dim3(kTc8Threads), tc8_smem(32), st, true, m.tmW, m.tmD, m.p));
   return check_launch("gemv_tc8_kernel");
+}
+
+// ---- decode plans: all matrices of one stage in one launch ----------------------------
+bool tc8_plan_supported(const MatDesc* mats, int n, int B) {
+  if (n < 1 || n > 65535) return false;
+  for (int i = 0; i < n; ++i)
+    if (!tc8_supported(mats[i].N, mats[i].K, B) || mats[i].B != B) return false;
+  return true;
+}
+
+nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t) {
+  *t = Tc8Plan{};
+  int dev = 0;
+  NT_CUDA_TRY(cudaGetDevice(&dev));
+  NT_TRY(tc8_setup(dev));
+  const int nn = tc8_nn(B);
+  size_t digit_bytes = 0, ws_bytes = 0;
+  int64_t mtiles = 0, min_kb = INT64_MAX, max_n4 = 0;
+  for (int i = 0; i < n; ++i) {
+    digit_bytes += (size_t)nn * tc8_kd(mats[i].K);
+    ws_bytes += sizeof(int32_t) * (size_t)B * mats[i].N + sizeof(unsigned int) * (size_t)tc8_mtiles(mats[i].N);
+    mtiles += tc8_mtiles(mats[i].N);
+    min_kb = std::min<int64_t>(min_kb, padded_k(mats[i].K) / kTc8KB);
+    max_n4 = std::max<int64_t>(max_n4, nn * tc8_kd(mats[i].K) / 4);
+  }
+  const size_t total = ((digit_bytes + 15) & ~(size_t)15) + ws_bytes;
+  cudaError_t e;
+  if ((e = cudaMalloc(&t->d_buf, total)) != cudaSuccess) return set_error(NT_ERR_CUDA, std::string("cudaMalloc: ") + cudaGetErrorString(e));
+  if ((e = cudaMemset(t->d_buf, 0, total)) != cudaSuccess) return set_error(NT_ERR_CUDA, std::string("cudaMemset: ") + cudaGetErrorString(e));
+  uint8_t* digits = static_cast<uint8_t*>(t->d_buf);
+  uint8_t* ws = digits + ((digit_bytes + 15) & ~(size_t)15);
+  const int64_t parts = tc8_parts(mtiles, min_kb);
+  std::vector<Tc8Mat> mm(n);
+  std::vector<Tc8DigitJob> jobs(n);
+  std::vector<uint16_t> tab;
+  int64_t ctas = 0;
+  for (int i = 0; i < n; ++i) {
+    const MatDesc& d = mats[i];
+    int32_t* acc_ws = reinterpret_cast<int32_t*>(ws);
+    unsigned int* cnt = reinterpret_cast<unsigned int*>(acc_ws + (size_t)B * d.N);
+    ws = reinterpret_cast<uint8_t*>(cnt + tc8_mtiles(d.N));
+    NT_TRY(tc8_matrix(d.w, d.s_w, d.N, d.K, d.s_x, B, d.y, d.acc, digits, acc_ws, cnt, parts, &mm[i]));
+    mm[i].cta_begin = ctas;
+    const int64_t c = (int64_t)mm[i].p.mtiles * mm[i].p.nparts;
+    ctas += c;
+    tab.insert(tab.end(), (size_t)c, (uint16_t)i);
+    jobs[i] = Tc8DigitJob{d.q, digits, B, d.K, (int)tc8_kd(d.K), nn};
+    digits += (size_t)nn * tc8_kd(d.K);
+  }
+  if (ctas > INT32_MAX) return set_error(NT_ERR_INVALID_ARG, "tcgen05 batched path: too many row tiles in one stage");
+  if ((e = cudaMalloc(&t->d_mats, sizeof(Tc8Mat) * n)) != cudaSuccess ||
+      (e = cudaMemcpy(t->d_mats, mm.data(), sizeof(Tc8Mat) * n, cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMalloc(&t->d_tab, sizeof(uint16_t) * tab.size())) != cudaSuccess ||
+      (e = cudaMemcpy(t->d_tab, tab.data(), sizeof(uint16_t) * tab.size(), cudaMemcpyHostToDevice)) != cudaSuccess ||
+      (e = cudaMalloc(&t->d_jobs, sizeof(Tc8DigitJob) * n)) != cudaSuccess ||
+      (e = cudaMemcpy(t->d_jobs, jobs.data(), sizeof(Tc8DigitJob) * n, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return set_error(NT_ERR_CUDA, std::string("tcgen05 plan setup: ") + cudaGetErrorString(e));
+  t->n = n;
+  t->nn = nn;
+  t->ctas = ctas;
+  t->digit_grid = (int)std::min<int64_t>((max_n4 + 255) / 256, 64);
+  return NT_OK;
+}
+
+nt_status tc8_plan_launch(const Tc8Plan& t, cudaStream_t st, bool pdl) {
+  NT_CUDA_TRY(launch_kernel(tc8_digits_multi_kernel, dim3(t.digit_grid, t.n), dim3(256), 0, st, pdl,
+                            static_cast<const Tc8DigitJob*>(t.d_jobs)));
+  const Tc8Mat* mats = static_cast<const Tc8Mat*>(t.d_mats);
+  if (t.nn == 16)
+    NT_CUDA_TRY(launch_kernel(gemv_tc8_multi_kernel<16>, dim3((unsigned)t.ctas), dim3(kTc8Threads), tc8_smem(16), st,
+                              true, mats, (const uint16_t*)t.d_tab));
+  else
+    NT_CUDA_TRY(launch_kernel(gemv_tc8_multi_kernel<32>, dim3((unsigned)t.ctas), dim3(kTc8Threads), tc8_smem(32), st,
+                              true, mats, (const uint16_t*)t.d_tab));
+  return check_launch("gemv_tc8_multi_kernel");
+}
+
+void tc8_plan_destroy(Tc8Plan* t) {
+  cudaFree(t->d_mats);
+  cudaFree(t->d_tab);
+  cudaFree(t->d_jobs);
+  cudaFree(t->d_buf);
+  *t = Tc8Plan{};
 }
 
 }  // namespace nt

@@ -118,6 +118,20 @@ bool tc8_supported(int N, int K, int B);
 size_t tc8_ws_bytes(int N, int K, int B);
 nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x, int B,
                           float* y, int32_t* acc, void* ws, cudaStream_t st);
+// All matrices of one decode-plan stage on the same tcgen05 path (2..16 vectors, every
+// matrix >= 128 rows): a digit-row launch, then one launch over every matrix's row tiles.
+struct Tc8Plan {
+  void* d_mats = nullptr;    // per matrix: tensor maps and parameters (device)
+  uint16_t* d_tab = nullptr; // CTA -> matrix
+  void* d_jobs = nullptr;    // per matrix: its digit-row job
+  void* d_buf = nullptr;     // digit rows, then each matrix's partial sums and tile counters
+  int n = 0, nn = 16, digit_grid = 1;
+  int64_t ctas = 0;
+};
+bool tc8_plan_supported(const MatDesc* mats, int n, int B);
+nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t);
+nt_status tc8_plan_launch(const Tc8Plan& t, cudaStream_t st, bool pdl);
+void tc8_plan_destroy(Tc8Plan* t);
 // Output projection on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, one pass over T.
 nt_status launch_head_mma(const int8_t* T, const float* s_T, int V, int K, const int8_t* q, const float* s_x,
                           int B, float* logits, int32_t* argmax, HeadWs* ws, cudaStream_t st);

@@ -137,7 +137,9 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
                               p->d_attn_out, p->d_attn_ws, st, p->d_pos + 1, pdl));
     }
     if (chained) NT_TRY(launch_chain_quant(p->d_cjobs + i, p->B, st, pdl));
-    if (p->d_mma)
+    if (p->tc8.n)
+      NT_TRY(tc8_plan_launch(p->tc8, st, pdl));
+    else if (p->d_mma)
       NT_TRY(launch_gemv_mma(p->d_mma + s.first_mat, s.n_mats, p->d_mma_tab + s.mma_tab_off, s.mma_ctas, p->B, st,
                              pdl));
     else
@@ -162,6 +164,7 @@ void free_plan(nt_decode_plan* p) {
   cudaFree(p->d_mma);
   cudaFree(p->d_mma_ws);
   cudaFree(p->d_mma_tab);
+  tc8_plan_destroy(&p->tc8);
   cudaFree(p->d_qjobs);
   cudaFree(p->d_head_ws);
   cudaFree(p->d_ctrl);
@@ -388,7 +391,13 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
   if ((e = cudaMalloc(&p->d_prefix, sizeof(int64_t) * prefix.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
   if ((e = cudaMemcpy(p->d_prefix, prefix.data(), sizeof(int64_t) * prefix.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy");
-  if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch) {
+  if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch &&
+      p->mode == NT_STEP_INDEPENDENT && p->stages.size() == 1 &&
+      tc8_plan_supported(mats.data(), (int)mats.size(), p->B)) {
+    // one stage of matrices of >= 128 rows: tcgen05 with the decoded trits in tensor memory
+    const nt_status s = tc8_plan_create(mats.data(), (int)mats.size(), p->B, &p->tc8);
+    if (s != NT_OK) return fail(s);
+  } else if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch) {
     // batched plans on the stream / graph launchers: the tensor-core path. Every stage's
     // matrices take disjoint parts of one workspace ([B][N] int32 sums of each matrix, then
     // the unit groups' counters); stages run one after another and leave it zero.

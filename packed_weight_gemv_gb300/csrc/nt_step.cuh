@@ -54,6 +54,8 @@ struct nt_decode_plan {
   nt::MmaMat* d_mma = nullptr;
   void* d_mma_ws = nullptr;
   uint16_t* d_mma_tab = nullptr;
+  // independent batched plans (one stage, every matrix >= 128 rows): the tcgen05 path instead
+  nt::Tc8Plan tc8;
   nt::QuantJob* d_qjobs = nullptr;
   int n_qjobs = 0;
   bool has_head = false;
