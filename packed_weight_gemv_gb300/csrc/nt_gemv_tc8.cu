@@ -13,10 +13,14 @@
 // into that row's tensor-memory lane with tcgen05.st, so the weights never pass through the
 // shared-memory port a second time.
 //
+// Used by nt_ternary_gemm with a workspace (one matrix, gemv_tc8_kernel) and by independent
+// decode plans on the graph / stream launchers (every matrix of the step in one launch,
+// gemv_tc8_multi_kernel, after one launch that writes every matrix's digit rows).
+//
 // CTA (192 threads), one 128-row tile of the weights over a range of K ("part"):
 //   warp 4 lane 0  -- TMA producer: per 128-trit K-block one 2-D box of the tiled weights
 //                     (32 tiles x 128 bytes, 128-byte swizzle) and one box of the digit rows
-//                     (N x 128 bytes) into a ring of kStages stages (full / empty mbarriers);
+//                     (N x 128 bytes) into a ring of kTc8Stages stages (full / empty mbarriers);
 //   warps 0-3      -- decoders, one thread per weight row (tensor-memory lane = row): 8
 //                     shared loads of its row's words per K-block (conflict-free thanks to the
 //                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into one of three A buffers;
@@ -31,7 +35,6 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
-
 #include <climits>
 #include <mutex>
 #include <vector>
