@@ -20,7 +20,7 @@
 // CTA (192 threads), one 128-row tile of the weights over a range of K ("part"):
 //   warp 4 lane 0  -- TMA producer: per 128-trit K-block one 2-D box of the tiled weights
 //                     (32 tiles x 128 bytes, 128-byte swizzle) and one box of the digit rows
-//                     (N x 128 bytes) into a ring of kTc8Stages stages (full / empty mbarriers);
+//                     (N x 128 bytes) into a ring of 8 or 4 stages (full / empty mbarriers);
 //   warps 0-3      -- decoders, one thread per weight row (tensor-memory lane = row): 8
 //                     shared loads of its row's words per K-block (conflict-free thanks to the
 //                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into one of three A buffers;
@@ -47,7 +47,9 @@ namespace {
 
 constexpr int kTc8Tiles = 32;                  // tiles (4 rows) per CTA: 128 weight rows (MMA M)
 constexpr int kTc8KB = 128;                    // trits per K-block = bytes of one tile's block
-constexpr int kTc8Stages = 8;
+// ring stages: as many as keep four CTAs per SM (the tensor-memory limit: 4 x 128 columns);
+// with 32 digit rows a stage is 8 KB and 8 stages would leave room for three
+constexpr int tc8_stages(int nn) { return nn <= 16 ? 8 : 4; }
 constexpr int kTc8WBytes = kTc8Tiles * kTc8KB;  // weight box: 4 KB
 constexpr int kTc8Threads = 192;
 constexpr int kTc8Decoders = 128;
@@ -151,6 +153,7 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
                                         bool global_maps) {
   const CUtensorMap& tmW = *tmW_;
   const CUtensorMap& tmD = *tmD_;
+  constexpr int kTc8Stages = tc8_stages(NN);
   constexpr int kStageBytes = kTc8WBytes + NN * kTc8KB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -413,7 +416,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_tc8_encode = nullptr;
 bool g_tc8_attr[64] = {};
 
 constexpr int tc8_nn(int B) { return B <= 8 ? 16 : 32; }
-constexpr size_t tc8_smem(int nn) { return (size_t)kTc8Stages * (kTc8WBytes + nn * kTc8KB) + 1024 + 256; }
+constexpr size_t tc8_smem(int nn) { return (size_t)tc8_stages(nn) * (kTc8WBytes + nn * kTc8KB) + 1024 + 256; }
 int64_t tc8_kd(int K) { return ((int64_t)K + kTc8KB - 1) / kTc8KB * kTc8KB; }
 int64_t tc8_mtiles(int N) { return (padded_rows(N) / 4 + kTc8Tiles - 1) / kTc8Tiles; }
 
