@@ -20,10 +20,11 @@
 // CTA (192 threads), one 128-row tile of the weights over a range of K ("part"):
 //   warp 4 lane 0  -- TMA producer: per 128-trit K-block one 2-D box of the tiled weights
 //                     (32 tiles x 128 bytes, 128-byte swizzle) and one box of the digit rows
-//                     (N x 128 bytes) into a ring of 8 or 4 stages (full / empty mbarriers);
+//                     (N x 128 bytes) into a ring of 4 stages (full / empty mbarriers);
 //   warps 0-3      -- decoders, one thread per weight row (tensor-memory lane = row): 8
 //                     shared loads of its row's words per K-block (conflict-free thanks to the
-//                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into one of three A buffers;
+//                     swizzle), decode to 32 e4m3 bytes, tcgen05.st into the A buffer once the
+//                     previous block's MMAs have read it;
 //   warp 5 lane 0  -- MMA issuer: 4 x tcgen05.mma (M 128, N 16/32, K 32) per K-block, commits
 //                     release the stage and the A buffer;
 //   epilogue       -- the decoders read the accumulator (tcgen05.ld), then y = fl(fl(acc) s_w) s_x
@@ -47,14 +48,15 @@ namespace {
 
 constexpr int kTc8Tiles = 32;                  // tiles (4 rows) per CTA: 128 weight rows (MMA M)
 constexpr int kTc8KB = 128;                    // trits per K-block = bytes of one tile's block
-// ring stages: as many as keep four CTAs per SM (the tensor-memory limit: 4 x 128 columns);
-// with 32 digit rows a stage is 8 KB and 8 stages would leave room for three
-constexpr int tc8_stages(int nn) { return nn <= 16 ? 8 : 4; }
+// ring stages: few, so that more CTAs share an SM (measured: 4 stages, 64 tensor-memory columns
+// and 56 registers per thread run six CTAs per SM and beat 8 stages with four)
+constexpr int tc8_stages(int nn) { return nn <= 16 ? 4 : 4; }
 constexpr int kTc8WBytes = kTc8Tiles * kTc8KB;  // weight box: 4 KB
 constexpr int kTc8Threads = 192;
+constexpr int kTc8MinBlocks = 6;               // CTAs per SM: registers capped at 56 (no spills)
 constexpr int kTc8Decoders = 128;
-constexpr int kTc8TmemCols = 128;              // D at column 0 (<= 32), A buffers at 32, 64, 96
-constexpr int kTc8ABufs = 3;
+constexpr int kTc8TmemCols = 64;               // D at column 0 (<= 32), the A buffer at 32
+constexpr int kTc8ABufs = 1;                   // the decode of the next block overlaps the MMA
 constexpr uint64_t kTc8TimeoutNs = 2000000000ull;
 constexpr int64_t kTc8MaxPartK = 131072;       // |D| <= 15 K < 2^24
 
@@ -349,7 +351,7 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
 }
 
 template <int NN>
-__global__ void __launch_bounds__(kTc8Threads, 1)
+__global__ void __launch_bounds__(kTc8Threads, kTc8MinBlocks)
     gemv_tc8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmD, const Tc8Params p) {
   tc8_cta<NN>(&tmW, &tmD, p, (int)blockIdx.x, false);
 }
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kTc8Threads, 1)
 // Several matrices in one launch (a decode plan's stage): CTA -> matrix from the table; the
 // matrices' tensor maps live in global memory (written before the plan's first launch).
 template <int NN>
-__global__ void __launch_bounds__(kTc8Threads, 1)
+__global__ void __launch_bounds__(kTc8Threads, kTc8MinBlocks)
     gemv_tc8_multi_kernel(const Tc8Mat* __restrict__ mats, const uint16_t* __restrict__ cta_mat) {
   const Tc8Mat* m = mats + __ldg(cta_mat + blockIdx.x);
   const Tc8Params p = m->p;
