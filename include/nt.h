@@ -348,12 +348,15 @@ typedef struct nt_decode_desc {
   int32_t* head_argmax;  /* [B] int32 */
   int mode;              /* enum nt_step_mode */
   int launcher;          /* enum nt_launcher */
-  double timeout_ms;     /* bound on every device-side wait of the persistent kernel;
-                            <= 0 selects 250 ms */
+  double timeout_ms;     /* bound on every device-side wait of the persistent kernel and of
+                            the tcgen05 batched kernel; <= 0 selects 250 ms */
   int test_fault;        /* 0 in normal use. 1 makes the first grid barrier of the
                             persistent kernel wait for one arrival more than the grid makes,
                             so that wait runs out after timeout_ms and the step reports
-                            NT_ERR_TIMEOUT: the hook the tests of the timeout path use. */
+                            NT_ERR_TIMEOUT: the hook the tests of the timeout path use. 2
+                            does the same for the tcgen05 batched kernel (independent plans,
+                            2..16 vectors, graph / stream launchers): its producers issue no
+                            copies, so the consumers' waits run out. */
   /* Input-table gather at the start of the step (nt_embed_rows); embed_T == NULL leaves it
      out. Projection inputs (x) may point into embed_x: the gather finishes before any
      input is quantized. Tokens outside [0, embed_V) give zero rows. */
@@ -406,8 +409,10 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** plan);
 nt_status nt_decode_step(nt_decode_plan* plan, void* stream);
 
 /* After the caller has synchronized with the last step: NT_OK, or NT_ERR_TIMEOUT when a
- * bounded wait inside the persistent kernel ran out (the step's outputs are then invalid
- * and the plan must be reset before reuse). Reads 4 bytes from the device (synchronous). */
+ * bounded wait inside the persistent kernel or the tcgen05 batched kernel (independent plans
+ * with 2..16 vectors on the graph / stream launchers) ran out (the step's outputs are then
+ * invalid and the plan must be reset before reuse). Reads the device status word
+ * (synchronous). */
 nt_status nt_decode_step_status(nt_decode_plan* plan, nt_status* device_status);
 
 /* Chained plans with attention: the position of the next step's first vector, set in stream

@@ -59,6 +59,7 @@ constexpr int kTc8TmemCols = 64;               // D at column 0 (<= 32), the A b
 constexpr int kTc8ABufs = 1;                   // the decode of the next block overlaps the MMA
 constexpr uint64_t kTc8TimeoutNs = 2000000000ull;
 constexpr int64_t kTc8MaxPartK = 131072;       // |D| <= 15 K < 2^24
+constexpr unsigned int kTc8ErrWait = 16;        // status code of a wait that ran out
 
 // e4m3 pools of the pair codes: the same pools as the dp4a decode with +1 -> 0x38, -1 -> 0xB8.
 // Code 14 (the pair (0, -1)) reads byte 6 in sign-replicate mode: 0x38 -> 0x00 in pool A,
@@ -98,9 +99,9 @@ __device__ __forceinline__ bool bar_try_sleep(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait; false after the timeout or once another role of the CTA has given up.
-__device__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
+__device__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* fail, uint64_t timeout_ns) {
   if (bar_try(bar, parity)) return true;
-  const uint64_t deadline = globaltimer_ns() + kTc8TimeoutNs;
+  const uint64_t deadline = globaltimer_ns() + timeout_ns;
   for (;;) {
     if (bar_try_sleep(bar, parity)) return true;
     if (*fail || globaltimer_ns() > deadline) {
@@ -140,6 +141,9 @@ struct Tc8Params {
   int mtiles;        // 128-row tiles
   int kblocks;       // 128-trit blocks of padded K
   int kb_per_part, nparts;
+  unsigned int* err;  // status word [code, CTA] of a decode plan, or null
+  uint64_t timeout_ns;  // bound on every wait
+  int fault;           // tests of the timeout path: the producer issues no copies
 };
 struct Tc8Mat {
   CUtensorMap tmW;   // the tiles, box 128 bytes x 32 tiles
@@ -198,14 +202,14 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
 
   if (warp == 4) {
     // ---- TMA producer: weight box and digit box of every K-block of the part ----
-    if (lane == 0) {
+    if (lane == 0 && !p.fault) {
       if (global_maps) {  // maps written to global memory before the launch: make them visible to the TMA
         asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmW_) : "memory");
         asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(tmD_) : "memory");
       }
       for (int i = 0; i < nkb; ++i) {
         const int s = i % kTc8Stages;
-        if (i >= kTc8Stages && !bar_wait(empty0 + 8 * s, ((i / kTc8Stages) - 1) & 1u, fail)) break;
+        if (i >= kTc8Stages && !bar_wait(empty0 + 8 * s, ((i / kTc8Stages) - 1) & 1u, fail, p.timeout_ns)) break;
         uint8_t* st = smem + s * kStageBytes;
         bar_expect_tx(full0 + 8 * s, kStageBytes);
         const int x = (kb0 + i) * kTc8KB;  // byte (= trit) offset within a tile, a multiple of 128
@@ -219,8 +223,8 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
       constexpr uint32_t idesc = idesc_e4m3(NN);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % kTc8Stages, b = i % kTc8ABufs;
-        if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail)) break;
-        if (!bar_wait(afull0 + 8 * b, (i / kTc8ABufs) & 1u, fail)) break;
+        if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail, p.timeout_ns)) break;
+        if (!bar_wait(afull0 + 8 * b, (i / kTc8ABufs) & 1u, fail, p.timeout_ns)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t bsm = s_u32(smem + s * kStageBytes + kTc8WBytes);
 #pragma unroll
@@ -247,14 +251,14 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % kTc8Stages, b = i % kTc8ABufs;
-      if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail)) break;
+      if (!bar_wait(full0 + 8 * s, (i / kTc8Stages) & 1u, fail, p.timeout_ns)) break;
       // the row's 8 words of the K-block: 16-byte chunk g of box row T sits at chunk g ^ (T % 8)
       const uint8_t* ws = smem + s * kStageBytes + T * kTc8KB + 4 * j;
       uint32_t w[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) w[g] = *reinterpret_cast<const uint32_t*>(ws + ((g ^ (T & 7)) << 4));
       bar_arrive(empty0 + 8 * s);  // release: the reads above are ordered before it
-      if (i >= kTc8ABufs && !bar_wait(aempty0 + 8 * b, ((i / kTc8ABufs) - 1) & 1u, fail)) break;
+      if (i >= kTc8ABufs && !bar_wait(aempty0 + 8 * b, ((i / kTc8ABufs) - 1) & 1u, fail, p.timeout_ns)) break;
       // e4m3 bytes of the block's trits 16 g .. 16 g + 15 into columns 4 g .. 4 g + 3 of the A buffer
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
@@ -328,6 +332,7 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
   __syncthreads();
   if (warp == 4)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTc8TmemCols) : "memory");
+  if (t == 0 && *fail && p.err && atomicCAS(p.err, 0u, kTc8ErrWait) == 0u) p.err[1] = blockIdx.x;
   if (p.nparts == 1 || *fail) return;
   // K split: the CTA that completes a tile's last part applies the epilogue and clears
   if (t == 0) *s_last = atomicAdd(p.cnt + mtile, 1u) == (unsigned)(p.nparts - 1);
@@ -490,6 +495,7 @@ static nt_status tc8_matrix(const uint8_t* w, const float* s_w, int N, int K, co
   p.B = B;
   p.mtiles = (int)tc8_mtiles(N);
   p.kblocks = (int)(Kp / kTc8KB);
+  p.timeout_ns = kTc8TimeoutNs;
   parts = std::max<int64_t>(parts, (Kp + kTc8MaxPartK - 1) / kTc8MaxPartK);
   parts = std::min<int64_t>(parts, p.kblocks);
   p.kb_per_part = (int)((p.kblocks + parts - 1) / parts);
@@ -538,7 +544,8 @@ bool tc8_plan_supported(const MatDesc* mats, int n, int B) {
   return true;
 }
 
-nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t) {
+nt_status tc8_plan_create(const MatDesc* mats, int n, int B, unsigned int* err, uint64_t timeout_ns, int fault,
+                          Tc8Plan* t) {
   *t = Tc8Plan{};
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
@@ -570,6 +577,9 @@ nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t) {
     unsigned int* cnt = reinterpret_cast<unsigned int*>(acc_ws + (size_t)B * d.N);
     ws = reinterpret_cast<uint8_t*>(cnt + tc8_mtiles(d.N));
     NT_TRY(tc8_matrix(d.w, d.s_w, d.N, d.K, d.s_x, B, d.y, d.acc, digits, acc_ws, cnt, parts, &mm[i]));
+    mm[i].p.err = err;
+    mm[i].p.timeout_ns = timeout_ns;
+    mm[i].p.fault = fault;
     mm[i].cta_begin = ctas;
     const int64_t c = (int64_t)mm[i].p.mtiles * mm[i].p.nparts;
     ctas += c;
@@ -588,6 +598,7 @@ nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t) {
   t->n = n;
   t->nn = nn;
   t->ctas = ctas;
+  t->buf_bytes = total;
   t->digit_grid = (int)std::min<int64_t>((max_n4 + 255) / 256, 64);
   return NT_OK;
 }

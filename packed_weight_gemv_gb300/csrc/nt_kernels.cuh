@@ -127,9 +127,13 @@ struct Tc8Plan {
   void* d_buf = nullptr;     // digit rows, then each matrix's partial sums and tile counters
   int n = 0, nn = 16, digit_grid = 1;
   int64_t ctas = 0;
+  size_t buf_bytes = 0;      // d_buf (zeroed again by a plan reset)
 };
 bool tc8_plan_supported(const MatDesc* mats, int n, int B);
-nt_status tc8_plan_create(const MatDesc* mats, int n, int B, Tc8Plan* t);
+// err: the plan's status word (error code, then the CTA); a wait that runs out (after
+// timeout_ns) records code 16; fault != 0 makes every CTA's producer issue no copies (tests)
+nt_status tc8_plan_create(const MatDesc* mats, int n, int B, unsigned int* err, uint64_t timeout_ns, int fault,
+                          Tc8Plan* t);
 nt_status tc8_plan_launch(const Tc8Plan& t, cudaStream_t st, bool pdl);
 void tc8_plan_destroy(Tc8Plan* t);
 // Output projection on the tensor cores (nt_gemv_mma.cu): 2..16 vectors, one pass over T.

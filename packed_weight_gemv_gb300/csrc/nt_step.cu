@@ -391,11 +391,14 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
   if ((e = cudaMalloc(&p->d_prefix, sizeof(int64_t) * prefix.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
   if ((e = cudaMemcpy(p->d_prefix, prefix.data(), sizeof(int64_t) * prefix.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy");
+  if ((e = cudaMalloc(&p->d_ctrl, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+  if ((e = cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
   if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch &&
       p->mode == NT_STEP_INDEPENDENT && p->stages.size() == 1 &&
       tc8_plan_supported(mats.data(), (int)mats.size(), p->B)) {
     // one stage of matrices of >= 128 rows: tcgen05 with the decoded trits in tensor memory
-    const nt_status s = tc8_plan_create(mats.data(), (int)mats.size(), p->B, &p->tc8);
+    const nt_status s = tc8_plan_create(mats.data(), (int)mats.size(), p->B, &p->d_ctrl->error, p->timeout_ns,
+                                        p->test_fault == 2, &p->tc8);
     if (s != NT_OK) return fail(s);
   } else if (p->launcher != NT_LAUNCH_PERSISTENT && p->B >= kMmaMinBatch && p->B <= kMmaMaxBatch) {
     // batched plans on the stream / graph launchers: the tensor-core path. Every stage's
@@ -487,8 +490,6 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     if ((e = cudaMalloc(&p->d_head_ws, ws)) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemset(p->d_head_ws, 0, ws)) != cudaSuccess) return cuda_fail(e, "cudaMemset");
   }
-  if ((e = cudaMalloc(&p->d_ctrl, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
-  if ((e = cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl))) != cudaSuccess) return cuda_fail(e, "cudaMemset");
 
   if (p->launcher == NT_LAUNCH_PERSISTENT) {
     const nt_status s = persist_prepare(p);
@@ -544,8 +545,7 @@ nt_status nt_decode_step_status(nt_decode_plan* p, nt_status* device_status) {
   *device_status = c.error ? NT_ERR_TIMEOUT : NT_OK;
   if (c.error) {
     char buf[160];
-    snprintf(buf, sizeof buf, "persistent step: a bounded wait ran out (code %u, CTA %u)", c.error,
-             c.error_cta);
+    snprintf(buf, sizeof buf, "decode step: a bounded wait ran out (code %u, CTA %u)", c.error, c.error_cta);
     set_error(NT_ERR_TIMEOUT, buf);
   }
   return NT_OK;
@@ -557,6 +557,7 @@ nt_status nt_decode_plan_reset(nt_decode_plan* p) {
   NT_CUDA_TRY(cudaDeviceSynchronize());
   NT_CUDA_TRY(cudaMemset(p->d_ctrl, 0, sizeof(StepCtrl)));
   if (p->d_head_ws) NT_CUDA_TRY(cudaMemset(p->d_head_ws, 0, head_ws_bytes(p->B)));
+  if (p->tc8.d_buf) NT_CUDA_TRY(cudaMemset(p->tc8.d_buf, 0, p->tc8.buf_bytes));  // partial sums a timeout left
   p->launches = 0;
   p->barrier_count = 0;
   NT_CUDA_TRY(cudaDeviceSynchronize());

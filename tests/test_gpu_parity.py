@@ -350,6 +350,27 @@ def test_persistent_timeout_is_reported_and_recoverable():
     good.close()
 
 
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_GRAPH, nt.NT_LAUNCH_STREAM])
+def test_tcgen05_batched_timeout_is_reported_and_recoverable(launcher):
+    # The tcgen05 batched kernel with producers that issue no copies: every consumer's wait runs
+    # out after timeout_ms, the CTAs free their tensor memory and report NT_ERR_TIMEOUT; the
+    # context stays usable and a plan without the fault is correct.
+    B = 3
+    projs = wl.decoder_projections(1, SMALL, B=B, seed=17, workload=18)
+    dp, _ = plan_inputs(projs, None, B=B)
+    plan = nt.DecodePlan(1, B, dp, None, nt.NT_STEP_INDEPENDENT, launcher, timeout_ms=20.0, test_fault=2)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_ERR_TIMEOUT
+    plan.close()
+    good = nt.DecodePlan(1, B, dp, None, nt.NT_STEP_INDEPENDENT, launcher)
+    good.nt_decode_step()
+    torch.cuda.synchronize()
+    assert good.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, None, dp, None, B=B)
+    good.close()
+
+
 # ---- prefill-shaped batches on the tensor cores -----------------------------------------
 
 TC_SHAPES = [(128, 256, 512), (200, 260, 1024), (64, 20, 528), (256, 3072, 1024),
