@@ -502,11 +502,11 @@ static nt_status tc8_matrix(const uint8_t* w, const float* s_w, int N, int K, co
   p.nparts = (p.kblocks + p.kb_per_part - 1) / p.kb_per_part;
   return NT_OK;
 }
-// K parts for a launch of `mtiles` row tiles: doubled while there are fewer than four CTAs per
-// SM and every part keeps at least 8 K-blocks.
+// K parts for a launch of `mtiles` row tiles: doubled while there are fewer than eight CTAs per
+// SM (six are resident) and every part keeps at least 8 K-blocks.
 static int64_t tc8_parts(int64_t mtiles, int64_t min_kblocks) {
   int64_t parts = 1;
-  while (mtiles * parts < 4LL * device_sm_count() && parts * 2 * 8 <= min_kblocks) parts *= 2;
+  while (mtiles * parts < 8LL * device_sm_count() && parts * 2 * 8 <= min_kblocks) parts *= 2;
   return parts;
 }
 
