@@ -304,6 +304,7 @@ __device__ __forceinline__ void tiled_tile(const MatDesc& m, int64_t tile, int l
 
 template <int NB>
 __global__ void __launch_bounds__(kThreads) gemv_tiled_kernel(const MatDesc m) {
+  dependent_launch_wait();
   const int lane = threadIdx.x & 31;
   const int64_t tiles = padded_rows(m.N) / 4;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < tiles;
@@ -468,13 +469,14 @@ nt_status launch_gemv_plain(const uint32_t* w, const float* s_w, int N, int K, c
   return check_launch("gemv_plain_kernel");
 }
 
+// One call: a programmatic dependent launch, so back-to-back calls overlap one call's launch
+// and ramp with the previous call's drain (the kernel waits for its predecessor before it
+// reads anything; after a kernel that does not signal early it simply starts after it).
 nt_status launch_gemv_tiled(const MatDesc& m, cudaStream_t st) {
   const int g = grid_for(padded_rows(m.N) / 4, 8);
-  if (m.B == 1) gemv_tiled_kernel<1><<<g, kThreads, 0, st>>>(m);
-  else if (m.B == 2) gemv_tiled_kernel<2><<<g, kThreads, 0, st>>>(m);
-  else if (m.B <= 4) gemv_tiled_kernel<4><<<g, kThreads, 0, st>>>(m);
-  else if (m.B <= 8) gemv_tiled_kernel<8><<<g, kThreads, 0, st>>>(m);
-  else gemv_tiled_kernel<16><<<g, kThreads, 0, st>>>(m);
+  auto kern = m.B == 1 ? gemv_tiled_kernel<1> : m.B == 2 ? gemv_tiled_kernel<2>
+            : m.B <= 4 ? gemv_tiled_kernel<4> : m.B <= 8 ? gemv_tiled_kernel<8> : gemv_tiled_kernel<16>;
+  NT_CUDA_TRY(launch_kernel(kern, dim3(g), dim3(kThreads), 0, st, true, m));
   return check_launch("gemv_tiled_kernel");
 }
 
