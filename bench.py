@@ -236,6 +236,130 @@ def cpu_baseline(oracle, budget_s=12.0):
                        f"151936 output-table rows, {n} repetition(s), scaled to one token")}
 
 
+class OracleRounds:
+    """The oracle timed per workload at one thread and at every core, one round at a time, so
+    that its rounds can interleave with the GPU's: the single 1536 x 512 GEMV (config 1), one
+    decoder layer of the 8B-shaped step (scaled to the 36-layer token, config 2) and 8,192 rows of
+    the output table (scaled to 151,936, config 3); throughput in GB/s of packed weight bytes."""
+
+    def __init__(self, oracle):
+        self.o = oracle
+        self.cores = os.cpu_count() or 1
+        self.single = wl.single_gemv()
+        self.layer = [wl.projection(wl.WL_DECODE, 0, i, *wl.DECODER_8B[n]) for i, n in enumerate(wl.PROJ_NAMES)]
+        self.hv = 8192
+        self.head = wl.head(V=self.hv)
+        self.rows = {}
+
+    def _time(self, fn, min_s):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_s:
+                return dt / n
+
+    def round(self):
+        o, p1, h = self.o, self.single, self.head
+        q1, s1 = o.quantize(p1.x)
+        ql = [o.quantize(p.x) for p in self.layer]
+        qh, sh = o.quantize(h.x)
+        res = {}
+        for th in (1, self.cores):
+            o.set_threads(th)
+            t1 = self._time(lambda: o.gemv(p1.w_plain, p1.s_w, p1.N, p1.K, q1[0], s1), 0.2)
+            tl = self._time(lambda: [o.gemv(p.w_plain, p.s_w, p.N, p.K, q[0], s)
+                                     for p, (q, s) in zip(self.layer, ql)], 0.5)
+            th_ = self._time(lambda: o.logits_argmax(h.T, h.s_T, self.hv, h.K, qh, sh), 0.3)
+            res[th] = (t1, tl, th_)
+        o.set_threads(0)
+        for th, v in res.items():
+            self.rows.setdefault(th, []).append(v)
+
+    def summary(self):
+        p1 = self.single
+        b1 = p1.N * p1.K // 4
+        bl = wl.packed_bytes_per_token(n_layers=1)
+        bh = self.hv * self.head.K
+        out = {}
+        for th, rows in self.rows.items():
+            t1, tl, th_ = (statistics.median(c) for c in zip(*rows))
+            out[f"threads_{th}"] = {
+                "config1_single_gemv": {"us_per_call": round(t1 * 1e6, 2), "GBps_packed": round(b1 / t1 / 1e9, 3)},
+                "config2_decode_projections": {"us_per_token": round(tl * wl.DECODER_8B_LAYERS * 1e6, 1),
+                                               "GBps_packed": round(bl / tl / 1e9, 3)},
+                "config3_lm_head": {"us_per_token": round(th_ * wl.HEAD_V / self.hv * 1e6, 1),
+                                    "GBps_packed": round(bh / th_ / 1e9, 3)},
+            }
+        return out
+
+
+def time_single_gemv(torch, nt, oracle, dev, stream, peak):
+    """The single 1536 x 512 GEMV of the first workload, per call: with its weights resident in L2
+    (the same matrix every call) and cold (a rotating pool of copies larger than 4 x L2, one
+    copy per call). The calls are captured in a CUDA graph and replayed, so the host's per-call
+    cost is not timed; parity against the oracle first."""
+    p = wl.single_gemv()
+    q, s = oracle.quantize(p.x)
+    acc, y, _ = oracle.gemv(p.w_plain, p.s_w, p.N, p.K, q[0], s)
+    w = torch.empty(nt.nt_repack_size(p.N, p.K), dtype=torch.uint8, device=dev)
+    nt.nt_repack_ternary(torch.from_numpy(p.w_plain.view(np.int32)).to(dev), p.N, p.K, w)
+    sw = torch.from_numpy(p.s_w).to(dev)
+    qd, sd = torch.from_numpy(q[0]).to(dev), torch.from_numpy(s).to(dev)
+    yd = torch.empty(p.N, dtype=torch.float32, device=dev)
+    ad = torch.empty(p.N, dtype=torch.int32, device=dev)
+    nt.nt_ternary_gemv(w, nt.NT_LAYOUT_TILED, sw, p.N, p.K, qd, sd, yd, ad, stream=stream)
+    torch.cuda.synchronize()
+    ok = np.array_equal(ad.cpu().numpy(), acc) and np.all(
+        np.abs(yd.cpu().numpy().astype(np.float64) - y) <= 1e-6 * np.abs(y.astype(np.float64)))
+    nbytes = p.N * p.K // 4 + 4 * p.N + p.K + 4 * p.N + 4
+    l2 = 129 * 2 ** 20
+    pool_n = -(-4 * l2 // (w.numel() + 4 * p.N))
+    ws = w.unsqueeze(0).repeat(pool_n, 1)
+    sws = sw.unsqueeze(0).repeat(pool_n, 1)
+
+    def graph_of(calls):
+        for _ in range(2):
+            calls()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            calls()
+        return g
+
+    def hot():
+        st = torch.cuda.current_stream()
+        for _ in range(pool_n):
+            nt.nt_ternary_gemv(w, nt.NT_LAYOUT_TILED, sw, p.N, p.K, qd, sd, yd, stream=st)
+
+    def cold():
+        st = torch.cuda.current_stream()
+        for i in range(pool_n):
+            nt.nt_ternary_gemv(ws[i], nt.NT_LAYOUT_TILED, sws[i], p.N, p.K, qd, sd, yd, stream=st)
+
+    res = {}
+    for name, calls in (("l2_resident", hot), ("cold_rotating_pool", cold)):
+        g = graph_of(calls)
+        g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(3):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (3 * pool_n)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": round(us, 3), "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4)}
+        del g
+    del ws, sws
+    torch.cuda.empty_cache()
+    return dict(res, bytes_per_call=nbytes, calls_per_replay=pool_n, kernel="gemv_tiled_kernel",
+                pool_bytes=int(pool_n * (w.numel() + 4 * p.N)), parity="pass" if ok else "differs",
+                what="1536x512 trits (seed 0), batch 1, nt_ternary_gemv calls replayed as a CUDA graph")
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -280,13 +404,35 @@ def run_ours(args, rank, world):
     per_step_us = us / args.steps
     value = us / (args.steps * world)
 
-    # End to end through the same public call, with pinned host buffers: every step copies its
-    # fp32 inputs host->device, runs the step and reads the emitted token back. Inputs and
-    # token are double-buffered: step i+1's copy (on its own stream) overlaps step i's compute
-    # and waits until step i-1 has finished with the buffers it overwrites; the token is read
-    # back on a third stream.
+    # Serial end to end through the same public call: every step copies its fp32 inputs from
+    # pinned host memory, runs, and reads its token back to the host before the next step
+    # starts, as a dependent single-stream decode must.
     x_host = torch.empty(x_all.numel(), dtype=torch.float32, pin_memory=True)
     x_host.copy_(x_all.cpu())
+    am_host = torch.empty(2, dtype=torch.int32, pin_memory=True)
+
+    def serial_step():
+        x_all.copy_(x_host, non_blocking=True)
+        plan.nt_decode_step(stream)
+        am_host[0:1].copy_(hd["argmax"], non_blocking=True)
+        stream.synchronize()
+
+    serial_steps = max(1, min(args.steps, 2000))
+    for _ in range(3):
+        serial_step()
+    t0 = time.perf_counter()
+    for _ in range(serial_steps):
+        serial_step()
+    e2e_serial_us = (time.perf_counter() - t0) * 1e6 / serial_steps
+    if int(am_host[0]) != int(hd["argmax"].item()):
+        raise RuntimeError("serial end-to-end: the token read back differs from the device's")
+
+    # Pipelined end to end through the same public call, with pinned host buffers: every step
+    # copies its fp32 inputs host->device, runs the step and reads the emitted token back.
+    # Inputs and token are double-buffered: step i+1's copy (on its own stream) overlaps step
+    # i's compute and waits until step i-1 has finished with the buffers it overwrites; the
+    # token is read back on a third stream. Possible only because the workload supplies every
+    # step's inputs (a dependent decode cannot do this: the serial figure above is its cost).
     x_alt = torch.empty_like(x_all)
     dp_alt, off = [], 0
     for d in dp:
@@ -295,7 +441,6 @@ def run_ours(args, rank, world):
     hd_alt = dict(hd, x=x_alt[off:off + head.K], argmax=torch.empty_like(hd["argmax"]))
     plans = [plan, nt.DecodePlan(L, 1, dp_alt, hd_alt, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)]
     bufs, am_dev = [x_all, x_alt], [hd["argmax"], hd_alt["argmax"]]
-    am_host = torch.empty(2, dtype=torch.int32, pin_memory=True)
     copy_stream, read_stream = torch.cuda.Stream(), torch.cuda.Stream()
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
@@ -333,6 +478,19 @@ def run_ours(args, rank, world):
     if plans[1].nt_decode_step_status() != nt.NT_OK:
         raise RuntimeError("end-to-end steps reported a timeout")
     plans[1].close()
+
+    # The oracle's protocol: GPU steps and the oracle's samples in interleaved rounds (the
+    # oracle at one thread and at every core, per workload), medians reported.
+    rounds = None
+    if rank == 0 and world == 1:
+        orc = OracleRounds(oracle)
+        gpu_rounds = []
+        for _ in range(3):
+            n_r = max(3, min(args.steps, 300))
+            gpu_rounds.append(time_steps(torch, plan, n_r, stream) / n_r)
+            orc.round()
+        rounds = dict(orc.summary(), rounds=3, gpu_us_per_token_by_round=[round(u, 2) for u in gpu_rounds],
+                      cores_available=orc.cores)
 
     # Breakdown (not the headline): the other launchers and modes over the same inputs.
     extra = {}
@@ -445,7 +603,8 @@ def run_ours(args, rank, world):
                                           what=f"one nt_ternary_gemm call, {bN}x{bK} trits, batch {gB}, with a "
                                                "workspace (tensor cores); dp4a_us: the same call without one")
     del big_w, big_q, big_sw, big_sx, big_y, g_q, g_sx, g_y, g_ws
-    hws = torch.empty(nt.nt_int8_logits_workspace_size(head.V, head.K, 1), dtype=torch.uint8, device=dev)
+    hws = torch.zeros(nt.nt_int8_logits_workspace_size(head.V, head.K, 1), dtype=torch.uint8, device=dev)
+    am_step = int(hd["argmax"].item())  # the step's arg-max (checked against the oracle above)
     nt.nt_quantize_act(hd["x"], hd["q"], hd["sx"], stream)
 
     def head_call():
@@ -460,9 +619,12 @@ def run_ours(args, rank, world):
         head_call()
     e1.record(stream)
     torch.cuda.synchronize()
+    if nt.nt_workspace_status(hws) != nt.NT_OK or int(hd["argmax"].item()) != am_step:
+        raise RuntimeError("standalone output projection: timeout reported or arg-max differs from the step's")
     comp["lm_head"] = dict(frac(wl.head_bytes(B=1), e0.elapsed_time(e1) * 1e3 / n_extra),
-                           kernel="persist_kernel (implicit schedule)",
+                           kernel="persist_kernel (implicit schedule, programmatic dependent launch)",
                            what=f"int8 table {head.V}x{head.K}, fp32 logits, greedy arg-max")
+    comp["single_gemv_config1"] = time_single_gemv(torch, nt, oracle, dev, stream, peak)
     rN, rK = wl.DECODER_8B["gate"]
     r1 = torch.randint(-2 ** 31, 2 ** 31 - 1, (rN * rK // 16,), dtype=torch.int32, device=dev)
     r2 = torch.randint(-2 ** 31, 2 ** 31 - 1, (rN * rK // 16,), dtype=torch.int32, device=dev)
@@ -489,6 +651,8 @@ def run_ours(args, rank, world):
     nbytes = step_bytes(n_layers=L)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     cpu = cpu_baseline(oracle) if (rank == 0 and world == 1) else None
+    if cpu is not None and rounds is not None:
+        cpu["per_config_interleaved"] = rounds
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -513,8 +677,11 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                      "kernel": "persist_kernel", "frac_of_8TBps_spec": round(achieved / 8000.0, 4)},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_us, 2), "unit": "us/token",
+        "e2e": {"value": round(e2e_serial_us, 2), "unit": "us/token", "mode": "serial",
                 "h2d_bytes_per_step": int(x_all.numel() * 4), "d2h_bytes_per_step": 4},
+        "e2e_pipelined": {"value": round(e2e_us, 2), "unit": "us/token",
+                          "h2d_bytes_per_step": int(x_all.numel() * 4), "d2h_bytes_per_step": 4,
+                          "what": "step i+1's input copy overlaps step i (inputs supplied, not produced)"},
         "gpu_launches": args.steps,
         "clocks": clk,
         "parity": parity if parity_after == "pass" else f"after timing: {parity_after}",

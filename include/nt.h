@@ -83,7 +83,7 @@ typedef enum nt_status {
   NT_ERR_ALIGNMENT = 2,   /* a pointer is not aligned as the call requires */
   NT_ERR_UNSUPPORTED = 3, /* the current device is not compute capability 10.3 (GB300) */
   NT_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed (detail string has it) */
-  NT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (decode plan status) */
+  NT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (decode plan or workspace status) */
   NT_ERR_WORKSPACE = 6    /* the workspace is NULL or smaller than the size call reported */
 } nt_status;
 
@@ -98,6 +98,31 @@ const char* nt_status_string(nt_status s);
 /* Detail of the last error returned to the calling host thread ("" if none). The pointer
  * stays valid until the next nt_* call on the same thread. */
 const char* nt_last_error_string(void);
+
+/* Status of a workspace after the calls that used it ("A 104 microsecond floor ...": the
+ * kernels that stream the weights wait on copies in flight, and every such wait here has a time
+ * limit). Every workspace the library takes (nt_ternary_gemm, nt_ternary_gemm_multi,
+ * nt_int8_logits_argmax) begins with a 16-byte status header. When a bounded device-side wait
+ * of a call runs out (the streaming output projection: 250 ms; the tensor-core GEMMs: 2 s), the
+ * kernel records an error code and its CTA there instead of hanging; that call's outputs are
+ * invalid (the output projection writes -1 as every vector's arg-max). The code stays until the
+ * caller zero-fills the whole workspace again, and until then the results of every call that
+ * uses the workspace are invalid (the streaming output projection does no work and writes -1).
+ *   ws             the workspace (device pointer, as passed to the calls); it must have been
+ *                  zero-filled before its first use for its header to mean anything
+ *   device_status  host: NT_OK, or NT_ERR_TIMEOUT (the detail string names the code and CTA)
+ * Synchronous (reads 16 bytes); call it after synchronizing with the calls that used ws. */
+nt_status nt_workspace_status(const void* ws, nt_status* device_status);
+
+/* Test hook of the per-call timeout paths, for tests only: with `fault` set, the next launches
+ * of one kernel issue no weight copies, so their consumers' bounded waits run out after
+ * timeout_ms (<= 0 keeps the normal limits) and the call's workspace reports NT_ERR_TIMEOUT.
+ *   fault 1: the streaming output projection (nt_int8_logits_argmax and its allocation-free
+ *            variant at B = 1); 2: the tcgen05 path of nt_ternary_gemm (2..16 vectors with a
+ *            workspace, N >= 128); 3: the prefill GEMM (64 or more vectors); 0: none.
+ * Process-wide; set it only while no other thread launches library calls. No GPU fault is
+ * involved: every wait gives up cleanly and the context stays usable. */
+nt_status nt_set_test_fault(int fault, double timeout_ms);
 
 /* Checks that the current CUDA device is a GB300 (compute capability 10.3) and reports its
  * SM count (host int*, may be NULL). Every other call performs the same check once per
@@ -159,6 +184,9 @@ nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, in
  * K parts meet in the workspace, which every call leaves zero apart from the digit rows.
  * With ws NULL or short it runs the dp4a kernel. Otherwise the size is 0 and ws may be NULL.
  */
+/* Every workspace of this call starts with the 16-byte status header nt_workspace_status
+ * reads (the tensor-core kernels' waits are bounded at 2 s); after NT_ERR_TIMEOUT the whole
+ * workspace must be zero-filled again before its next use. */
 nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes);
 nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, int B, float* y,
@@ -173,11 +201,18 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
  *   q [B][K] int8 (16-byte aligned)                s_x [B] fp32
  *   logits_opt [B][V] fp32 (output) or NULL        argmax [B] int32 (output)
  *   ws: nt_int8_logits_workspace_size(V, K, B) bytes of device memory that is zero-filled
- *       before its first use; every call returns it to that state. Calls that share one
- *       workspace must not overlap on the device.
+ *       before its first use; every call returns it to that state (unless a wait ran out:
+ *       see nt_workspace_status). Calls that share one workspace must not overlap on the
+ *       device.
  * B = 1 streams T through the persistent dp4a kernel; 2 <= B <= 16 reads T once on the
  * tensor cores (f16 MMA of exactly converted int8 with exact int32 sums); larger B takes
  * several passes of 16. Logits and arg-max are the same in every case.
+ * At B = 1 the call is a programmatic dependent launch: it starts streaming T while the
+ * previous kernel on the stream finishes, and reads q, s_x and s_T and writes its outputs
+ * only after that kernel has completed. T is treated as a constant: do not write it with the
+ * kernel launched immediately before this call on the same stream. A bounded wait of the
+ * streaming kernel that runs out (250 ms) makes argmax -1 for every vector and leaves
+ * NT_ERR_TIMEOUT in the workspace's status header (nt_workspace_status).
  */
 nt_status nt_int8_logits_workspace_size(int V, int K, int B, size_t* bytes);
 nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
@@ -193,11 +228,13 @@ nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
  * scratch is a fixed ~128 KiB array in the library's device globals, present on every device
  * that loads the library until the process exits.
  *   B must be <= 16 (the scratch's size); larger B returns NT_ERR_INVALID_ARG.
- *   The first call on a device looks up that device's scratch address (once, with the
- *   device current); make that first call before any stream capture.
+ *   Every call looks up the current device's scratch address (the first call on a device
+ *   may load the library's device code); make that first call before any stream capture.
  *   Every call on a device shares the one scratch array, so calls that overlap on that
  *   device (e.g. from two streams) race and give wrong results; serialize them. Each call
- *   clears the part of the scratch that must start at zero.
+ *   clears the part of the scratch that must start at zero (an asynchronous 16-byte memset
+ *   on `stream` before the kernel), so a wait that ran out in one call does not carry over:
+ *   the only sign of it is -1 as that call's arg-max (B = 1, the streaming kernel).
  */
 nt_status nt_int8_logits_argmax_noalloc(const int8_t* T, const float* s_T, int V, int K,
                                         const int8_t* q, const float* s_x, int B,
@@ -435,6 +472,19 @@ nt_status nt_decode_plan_reset(nt_decode_plan* plan);
  * of the plan overwrites it. Other launchers and stream/graph plans record nothing. */
 nt_status nt_decode_plan_trace_layout(const nt_decode_plan* plan, int* grid, int* barriers);
 nt_status nt_decode_plan_set_trace(nt_decode_plan* plan, unsigned long long* trace);
+
+/* Stage inputs of a chained plan, as the step quantized them: the fp32 vector each stage
+ * turned into int8 codes after every operation before it (residual additions, RMS
+ * normalisation, attention, the SiLU-gated product), for checking each stage on its own
+ * inputs ("A 104 microsecond floor ...": each layer applies its matrices to the current
+ * activations). nt_decode_plan_capture_size reports the buffer's length in floats (host
+ * size_t): per stage in step order -- per layer {q,k,v}, {o}, {gate,up}, {down}, then the
+ * output projection if the plan has one -- B x K values, K the stage's reduction length,
+ * vector-major. nt_decode_plan_set_capture installs a 16-byte aligned device buffer of that
+ * length (or, with NULL, removes it; synchronous); every later step of the plan overwrites
+ * it. Only NT_STEP_CHAINED plans (NT_ERR_INVALID_ARG otherwise). */
+nt_status nt_decode_plan_capture_size(const nt_decode_plan* plan, size_t* floats);
+nt_status nt_decode_plan_set_capture(nt_decode_plan* plan, float* buf);
 
 /* Releases the plan and everything it allocated. NULL is ignored. */
 void nt_decode_plan_destroy(nt_decode_plan* plan);

@@ -75,6 +75,8 @@ class Oracle:
         lib = ctypes.CDLL(path)
         i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
         lib.orc_threads.restype = i32
+        lib.orc_set_threads.argtypes = [i32]
+        lib.orc_set_threads.restype = None
         lib.orc_count_invalid.argtypes = [vp, i64]
         lib.orc_count_invalid.restype = i64
         lib.orc_unpack_plain.argtypes = [vp, i32, i32, vp]
@@ -100,6 +102,10 @@ class Oracle:
     def threads(self) -> int:
         """OpenMP threads the oracle's parallel loops use."""
         return int(self.lib.orc_threads())
+
+    def set_threads(self, n: int) -> None:
+        """Threads for the parallel loops from now on (timing only); n <= 0: every core."""
+        self.lib.orc_set_threads(int(n))
 
     def count_invalid(self, w_plain: np.ndarray) -> int:
         w = _c(w_plain, np.uint32)
@@ -218,6 +224,10 @@ def default() -> Oracle:
 
 def threads() -> int:
     return default().threads()
+
+
+def set_threads(n: int) -> None:
+    default().set_threads(n)
 
 
 def count_invalid(w_plain):

@@ -48,6 +48,16 @@ int orc_threads(void) {
 #endif
 }
 
+/* Threads the parallel loops use from now on (for timing the oracle at one thread and at all
+ * of them; no result depends on it). n <= 0 selects every core. */
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+  (void)n;
+#endif
+}
+
 /* Value of one plain field code; 2 (the invalid code) is reported through *bad. */
 static int plain_trit(uint32_t code, int* bad) {
   switch (code & 3u) {

@@ -15,7 +15,16 @@ thread_local std::string g_last_error;
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 GB300, 2 other
 std::atomic<int> g_dev_sms[kMaxDevices];
+std::atomic<int> g_fault{0};
+std::atomic<uint64_t> g_fault_timeout_ns{0};
 }  // namespace
+
+int test_fault() { return g_fault.load(std::memory_order_relaxed); }
+
+uint64_t test_fault_timeout_ns(uint64_t dflt) {
+  const uint64_t t = g_fault_timeout_ns.load(std::memory_order_relaxed);
+  return (g_fault.load(std::memory_order_relaxed) != kFaultNone && t > 0) ? t : dflt;
+}
 
 nt_status set_error(nt_status s, const std::string& detail) {
   g_last_error = detail;
@@ -105,6 +114,28 @@ const char* nt_status_string(nt_status s) {
 }
 
 const char* nt_last_error_string(void) { return g_last_error.c_str(); }
+
+nt_status nt_set_test_fault(int fault, double timeout_ms) {
+  clear_error();
+  if (fault < kFaultNone || fault > kFaultPrefill) return set_error(NT_ERR_INVALID_ARG, "fault must be 0..3");
+  g_fault_timeout_ns.store(timeout_ms > 0 ? (uint64_t)(timeout_ms * 1e6) : 0, std::memory_order_relaxed);
+  g_fault.store(fault, std::memory_order_relaxed);
+  return NT_OK;
+}
+
+nt_status nt_workspace_status(const void* ws, nt_status* device_status) {
+  clear_error();
+  if (!ws || !device_status) return set_error(NT_ERR_INVALID_ARG, "NULL argument");
+  WsHeader h;
+  NT_CUDA_TRY(cudaMemcpy(&h, ws, sizeof h, cudaMemcpyDeviceToHost));
+  *device_status = h.error ? NT_ERR_TIMEOUT : NT_OK;
+  if (h.error) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "workspace: a bounded wait ran out (code %u, CTA %u)", h.error, h.error_cta);
+    set_error(NT_ERR_TIMEOUT, buf);
+  }
+  return NT_OK;
+}
 
 nt_status nt_device_check(int* sm_count_opt) {
   clear_error();
@@ -266,7 +297,7 @@ nt_status nt_int8_logits_argmax(const int8_t* T, const float* s_T, int V, int K,
     return set_error(NT_ERR_WORKSPACE, "workspace NULL, misaligned or smaller than nt_int8_logits_workspace_size");
   NT_TRY(check_device());
   return launch_head(T, s_T, V, K, q, s_x, B, logits_opt, argmax, static_cast<HeadWs*>(ws),
-                     as_stream(stream));
+                     as_stream(stream), /*pdl=*/true);
 }
 
 }  // extern "C"

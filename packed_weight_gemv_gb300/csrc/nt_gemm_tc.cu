@@ -27,8 +27,8 @@
 //        warps 0-7: epilogue -- tcgen05.ld of a finished accumulator (lane = weight row,
 //          column = token), scales, fp32 stores that are 128-byte coalesced per warp --
 //          overlapping the next tile's MMAs in the other accumulator.
-// Every wait is bounded (2 s); a CTA that gives up still drains its own copies and MMAs and
-// frees its tensor memory.
+// Every wait is bounded (2 s); a CTA that gives up still drains its own copies and MMAs, frees
+// its tensor memory and records the code 17 in the workspace's status header.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -54,6 +54,7 @@ constexpr int kTcMaxMats = 8;            // matrices per call sharing the activa
 constexpr int kThreadsTc = kEpiThreads + 64;
 constexpr int kTmemCols = 2 * kBN;       // two accumulators
 constexpr uint64_t kTcTimeoutNs = 2000000000ull;
+constexpr unsigned int kTcErrWait = 17;  // status code of a wait that ran out
 constexpr int kSmemTc = kStages * kStageBytes + 1024 /* alignment */ + 2 * kBN * 4 /* token scales */ +
                         256 /* barriers */;
 
@@ -80,9 +81,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait; false after the timeout or once another role of the CTA has given up.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail) {
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* fail, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
+  const uint64_t deadline = globaltimer_ns() + timeout_ns;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u && (*fail || globaltimer_ns() > deadline)) {
@@ -211,6 +212,9 @@ struct TcParams {
   const float* s_w[kTcMaxMats];  // [N_i]
   float* y[kTcMaxMats];          // [M][N_i]
   int32_t* acc[kTcMaxMats];      // [M][N_i] or null
+  unsigned int* err;             // the workspace's status header [code, CTA]
+  uint64_t timeout_ns;           // bound on every wait
+  int fault;                     // tests of the timeout path: the producer issues no copies
 };
 
 __device__ __forceinline__ void epi_sync() {
@@ -261,11 +265,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   if (warp == kProducerWarp && lane == 0) {
     // ---- TMA producer ----
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles && !*fail; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < n_tiles && !*fail && !p.fault; tile += gridDim.x) {
       const int tn = tile % p.tiles_n, tm = tile / p.tiles_n;
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
         const uint32_t s = it % kStages;
-        if (it >= kStages && !mbar_wait(empty0 + 8 * s, ((it / kStages) - 1) & 1u, fail)) break;
+        if (it >= kStages && !mbar_wait(empty0 + 8 * s, ((it / kStages) - 1) & 1u, fail, p.timeout_ns)) break;
         const uint32_t a = smem_u32(smem + s * kStageBytes);
         mbar_expect_tx(full0 + 8 * s, kABytes + TN * kBK * 2);
         tma_load_2d(a, &tmW, ks * kBK, tn * kBM, full0 + 8 * s);
@@ -275,7 +279,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     // Drain: the last copy issued into each stage must land before the CTA may exit.
     for (uint32_t s = 0; s < kStages && s < it; ++s) {
       const uint32_t last = (it - 1 - s) / kStages * kStages + s;
-      const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
+      const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
       while (!mbar_try_wait(full0 + 8 * s, (last / kStages) & 1u))
         if (globaltimer_ns() > deadline) break;
     }
@@ -285,13 +289,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t idesc = idesc_for(TN);
     for (int tile = blockIdx.x; tile < n_tiles && !*fail; tile += gridDim.x, ++j) {
       const uint32_t buf = j & 1u;
-      if (j >= 2 && !mbar_wait(tempty0 + 8 * buf, ((j >> 1) - 1) & 1u, fail)) break;
+      if (j >= 2 && !mbar_wait(tempty0 + 8 * buf, ((j >> 1) - 1) & 1u, fail, p.timeout_ns)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t d = tmem + buf * kBN;
       bool ok = true;
       for (int ks = 0; ks < ksteps; ++ks, ++it) {
         const uint32_t s = it % kStages;
-        if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1u, fail)) { ok = false; break; }
+        if (!mbar_wait(full0 + 8 * s, (it / kStages) & 1u, fail, p.timeout_ns)) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t a = smem_u32(smem + s * kStageBytes), b = a + kABytes;
 #pragma unroll
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mma_commit(tfull0 + 8 * buf);  // accumulator buf complete
     }
     mma_commit(drain);  // every MMA of this CTA done (waited below before the memory is freed)
-    const uint64_t deadline = globaltimer_ns() + kTcTimeoutNs;
+    const uint64_t deadline = globaltimer_ns() + p.timeout_ns;
     while (!mbar_try_wait(drain, 0))
       if (globaltimer_ns() > deadline) break;
   } else if (warp < kProducerWarp) {
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       epi_sync();  // token scales of this tile visible to every epilogue thread
       // After a failed wait the thread keeps walking the tiles (the named barrier above needs
       // every epilogue thread) and only skips the stores.
-      const bool ok = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1u, fail);
+      const bool ok = mbar_wait(tfull0 + 8 * buf, (j >> 1) & 1u, fail, p.timeout_ns);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const uint32_t base = tmem + buf * kBN + half * (TN / 2) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
@@ -360,6 +364,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   __syncthreads();
   if (warp == kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  if (t == 0 && *fail && atomicCAS(p.err, 0u, kTcErrWait) == 0u) p.err[1] = blockIdx.x;
 }
 
 // ---- host ----------------------------------------------------------------------------
@@ -429,8 +434,9 @@ int64_t tc_weight_rows(int n, const int* N) {
 
 size_t tc_gemm_workspace_bytes(int M, int N, int K) { return tc_gemm_multi_workspace_bytes(M, 1, &N, K); }
 
+// workspace: the status header (kWsHeaderBytes), bf16 activations, bf16 weight rows
 size_t tc_gemm_multi_workspace_bytes(int M, int n, const int* N, int K) {
-  return align256((size_t)M * K * 2) + align256((size_t)tc_weight_rows(n, N) * K * 2);
+  return kWsHeaderBytes + align256((size_t)M * K * 2) + align256((size_t)tc_weight_rows(n, N) * K * 2);
 }
 
 nt_status launch_gemm_tc(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
@@ -445,7 +451,7 @@ nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* cons
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
   NT_TRY(tc_setup(dev));
-  uint8_t* a_bf16 = static_cast<uint8_t*>(ws);
+  uint8_t* a_bf16 = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
   uint8_t* b_bf16 = a_bf16 + align256((size_t)M * K * 2);
   const int sms = device_sm_count();
   PrepArgs pa{};
@@ -455,6 +461,9 @@ nt_status launch_gemm_tc_multi(int n, const uint8_t* const* w, const float* cons
   pa.n = n;
   pa.K = K;
   TcParams p{};
+  p.err = static_cast<unsigned int*>(ws);
+  p.timeout_ns = test_fault_timeout_ns(kTcTimeoutNs);
+  p.fault = test_fault() == kFaultPrefill;
   p.s_x = s_x;
   p.M = M;
   p.K = K;

@@ -546,7 +546,7 @@ size_t mma_single_ws_bytes(int N, int K, int B) {
   m.N = N;
   m.K = K;
   mma_geometry(m, 1);
-  return (mma_ws_bytes(N, m.ugroups, B) + 15) & ~(size_t)15;
+  return kWsHeaderBytes + ((mma_ws_bytes(N, m.ugroups, B) + 15) & ~(size_t)15);  // status header first
 }
 nt_status launch_gemv_mma_single(const uint8_t* w, const float* s_w, int N, int K, const int8_t* q, const float* s_x,
                                  int B, float* y, int32_t* acc, void* ws, cudaStream_t st) {
@@ -563,8 +563,8 @@ nt_status launch_gemv_mma_single(const uint8_t* w, const float* s_w, int N, int 
   m.B = B;
   mma_geometry(m, 1);
   for (int parts = 2; mma_ctas(m) < 8LL * device_sm_count() && parts <= 2 * m.kchunks; parts *= 2) mma_geometry(m, parts);
-  m.acc_ws = static_cast<int32_t*>(ws);
-  m.cnt = reinterpret_cast<unsigned int*>(static_cast<int32_t*>(ws) + (size_t)B * N);
+  m.acc_ws = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kWsHeaderBytes);  // after the status header
+  m.cnt = reinterpret_cast<unsigned int*>(m.acc_ws + (size_t)B * N);
   m.cta_begin = 0;
   const int nt = B <= 8 ? 1 : 2;
   NT_TRY(gemv_mma_attrs());

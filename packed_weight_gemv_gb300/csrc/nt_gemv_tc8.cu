@@ -141,7 +141,7 @@ struct Tc8Params {
   int mtiles;        // 128-row tiles
   int kblocks;       // 128-trit blocks of padded K
   int kb_per_part, nparts;
-  unsigned int* err;  // status word [code, CTA] of a decode plan, or null
+  unsigned int* err;  // status word [code, CTA]: a decode plan's, or the call's workspace header
   uint64_t timeout_ns;  // bound on every wait
   int fault;           // tests of the timeout path: the producer issues no copies
 };
@@ -467,10 +467,12 @@ bool tc8_supported(int N, int K, int B) {
   return B >= kMmaMinBatch && B <= kMmaMaxBatch && padded_rows(N) / 4 >= kTc8Tiles && K >= 16 && K % 16 == 0;
 }
 
-// workspace: digit rows [NN][Kd], then int32 partial sums [B][N], then one counter per 128-row tile
+// workspace: the status header (kWsHeaderBytes), digit rows [NN][Kd], then int32 partial sums
+// [B][N], then one counter per 128-row tile
 size_t tc8_ws_bytes(int N, int K, int B) {
   const size_t digits = (size_t)tc8_nn(B) * (size_t)tc8_kd(K);
-  return (digits + sizeof(int32_t) * (size_t)B * N + sizeof(unsigned int) * (size_t)tc8_mtiles(N) + 15) & ~(size_t)15;
+  return kWsHeaderBytes +
+         ((digits + sizeof(int32_t) * (size_t)B * N + sizeof(unsigned int) * (size_t)tc8_mtiles(N) + 15) & ~(size_t)15);
 }
 
 // Maps and parameters of one matrix: K in `parts` parts (at least enough for exact fp32
@@ -518,7 +520,7 @@ nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, cons
   NT_TRY(tc8_setup(dev));
   const int nn = tc8_nn(B);
   const int64_t Kd = tc8_kd(K), mtiles = tc8_mtiles(N);
-  uint8_t* digits = static_cast<uint8_t*>(ws);
+  uint8_t* digits = static_cast<uint8_t*>(ws) + kWsHeaderBytes;
   int32_t* acc_ws = reinterpret_cast<int32_t*>(digits + (size_t)nn * Kd);
   unsigned int* cnt = reinterpret_cast<unsigned int*>(acc_ws + (size_t)B * N);
   {
@@ -528,6 +530,9 @@ nt_status launch_gemv_tc8(const uint8_t* w, const float* s_w, int N, int K, cons
   }
   Tc8Mat m;
   NT_TRY(tc8_matrix(w, s_w, N, K, s_x, B, y, acc, digits, acc_ws, cnt, tc8_parts(mtiles, padded_k(K) / kTc8KB), &m));
+  m.p.err = static_cast<unsigned int*>(ws);  // the workspace's status header
+  m.p.timeout_ns = test_fault_timeout_ns(kTc8TimeoutNs);
+  m.p.fault = test_fault() == kFaultTc8;
   const dim3 grid((unsigned)(mtiles * m.p.nparts));
   if (nn == 16)
     NT_CUDA_TRY(launch_kernel(gemv_tc8_kernel<16>, grid, dim3(kTc8Threads), tc8_smem(16), st, true, m.tmW, m.tmD, m.p));

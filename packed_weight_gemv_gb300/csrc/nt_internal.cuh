@@ -21,6 +21,12 @@ int device_sm_count();
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Test hook of the per-call timeout paths (nt_set_test_fault): the fault that is set (0 =
+// none) and the bound on the per-call kernels' waits while it is set (`dflt` otherwise).
+enum : int { kFaultNone = 0, kFaultHeadStream = 1, kFaultTc8 = 2, kFaultPrefill = 3 };
+int test_fault();
+uint64_t test_fault_timeout_ns(uint64_t dflt);
+
 #define NT_TRY(expr)                         \
   do {                                       \
     nt_status _s = (expr);                   \

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kChainThreads) chain_quant_kernel(const ChainJ
                       __fmul_rn(__fmul_rn(v.z, r), g.z), __fmul_rn(__fmul_rn(v.w, r), g.w));
     }
     const uint32_t c = quant4(v, s, nz);
+    if (j.src.cap) *reinterpret_cast<float4*>(j.src.cap + (int64_t)b * K + k) = v;
     for (int rr = 0; rr < j.n_rec; ++rr) *reinterpret_cast<uint32_t*>(j.q[rr] + (int64_t)b * K + k) = c;
   }
 }
@@ -492,11 +493,11 @@ nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_prefix
 
 nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool pdl) {
   if (B >= kMmaMinBatch && B <= kMmaMaxBatch)  // one pass over T on the tensor cores
     return launch_head_mma(T, s_T, V, K, q, s_x, B, logits, argmax, ws, st);
   if (persist_head_fits(K, B))  // the streaming kernel (bulk copies into per-warp rings)
-    return persist_launch_head(T, s_T, V, K, q, s_x, B, logits, argmax, ws, st);
+    return persist_launch_head(T, s_T, V, K, q, s_x, B, logits, argmax, ws, st, pdl);
   int g = grid_for(V, 4);
   if (g > kHeadMaxCtas) g = kHeadMaxCtas;
   if (B == 1) head_kernel<1><<<g, kThreads, 0, st>>>(T, s_T, V, K, q, s_x, B, logits, argmax, ws);

@@ -22,7 +22,8 @@ struct QuantJob {
 //   kChainSiluProduct fl(silu(in0[b][k]) * in1[b][k]), silu(x) = x / (1 + exp(-x)) in fp32
 // With gamma set, the quantized vector is the RMS-normalised fl(fl(v * r) * gamma[k]),
 // r = fl32(1 / sqrt(mean(v^2) + eps)): the squares summed in fp32 within each warp, the warps'
-// sums added and r formed in double by one thread.
+// sums added and r formed in double by one thread. With cap set, the kernel that quantizes the
+// stage also stores the fp32 values it quantized there ([B][K]; nt_decode_plan_set_capture).
 enum : int { kChainNone = 0, kChainDirect = 1, kChainHeads = 2, kChainProduct = 3, kChainSum = 4,
              kChainSiluProduct = 5 };
 struct ChainSrc {
@@ -32,6 +33,7 @@ struct ChainSrc {
   const float* gamma;
   float eps;
   int pad_;
+  float* cap;
 };
 
 // One ternary projection in the tiled layout, B activation vectors.
@@ -69,11 +71,23 @@ struct HeadPartial {
   float val;
   int idx;
 };
+// The first 16 bytes of every workspace are its status header (nt_workspace_status): the
+// error code and CTA of a bounded wait that ran out, then, for the output projection, the
+// counter of CTAs done with the arg-max at the offset the decode plan's StepCtrl keeps it.
+struct WsHeader {
+  unsigned int error;      // 0 = fine; otherwise the code of the wait that ran out
+  unsigned int error_cta;
+  unsigned int pad_;
+  unsigned int done;       // output projection: CTAs finished; the last one resets it to 0
+};
 struct HeadWs {
-  unsigned int done;       // CTAs finished; the last one resets it to 0
-  unsigned int pad_[3];
+  unsigned int error, error_cta, pad_;
+  unsigned int done;
   HeadPartial part[1];     // [kHeadMaxCtas][B]
 };
+// Bytes in front of the data of the GEMM workspaces (the status header, padded so the data
+// keeps the alignment its tensor maps need).
+constexpr size_t kWsHeaderBytes = 256;
 inline size_t head_ws_bytes(int B) { return 16 + sizeof(HeadPartial) * (size_t)kHeadMaxCtas * B; }
 
 // Launchers (asynchronous on `st`; they return launch-configuration errors only).
@@ -143,7 +157,7 @@ nt_status launch_gemv_tiled_group(const MatDesc* d_mats, const int64_t* d_tile_p
                                   int64_t total_tiles, int max_B, cudaStream_t st, bool pdl = false);
 nt_status launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                       const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
-                      cudaStream_t st);
+                      cudaStream_t st, bool pdl = false);
 
 // Quantizes one chained stage input per vector (one CTA per vector).
 nt_status launch_chain_quant(const ChainJob* d_job, int B, cudaStream_t st, bool pdl = false);

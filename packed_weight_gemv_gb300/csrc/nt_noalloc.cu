@@ -7,7 +7,6 @@
 // not call cudaMalloc (it can synchronize the device and stall unrelated streams), or code
 // running under a fixed memory budget where a late allocation may fail. This entry point
 // needs only the inputs and outputs the caller already has.
-#include <mutex>
 #include <string>
 
 #include "nt_kernels.cuh"
@@ -23,26 +22,16 @@ constexpr size_t kNoAllocScratchBytes = 16 + sizeof(HeadPartial) * (size_t)kHead
 // One copy per device that loads the library, held until the process exits (~128 KiB).
 static __device__ __align__(256) unsigned char g_head_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of this device's scratch, looked up once per device (with it current). In
-// host code g_head_scratch names a host-side stand-in, not device memory, so only the
-// address from cudaGetSymbolAddress may be handed to a kernel.
+// Device address of the current device's scratch. In host code g_head_scratch names a
+// host-side stand-in, not device memory, so only the address from cudaGetSymbolAddress may be
+// handed to a kernel. It is looked up on every call (a cheap lookup once the module is loaded),
+// so a device reset that reloads the module and moves the array is harmless.
 nt_status scratch_for_current_device(void** out) {
-  int dev = 0;
-  NT_CUDA_TRY(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return set_error(NT_ERR_UNSUPPORTED, "device index out of range");
-  std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_head_scratch);
-    if (e != cudaSuccess || !p)
-      return set_error(NT_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_head_scratch);
+  if (e != cudaSuccess || !p)
+    return set_error(NT_ERR_CUDA, std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
+  *out = p;
   return NT_OK;
 }
 

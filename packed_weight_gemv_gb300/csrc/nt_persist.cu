@@ -86,6 +86,7 @@ struct PersistParams {
   int act_k;     // bytes per activation vector in shared memory
   uint32_t barrier_base;    // grid-barrier arrivals of all earlier launches on this plan (mod 2^32)
   uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
+  int no_copies;           // timeout-path tests: the producer issues nothing, so consumers time out
   uint64_t timeout_ns;
   unsigned long long* trace;  // optional timeline: [grid][n_barriers + 1][4]
   // input-table gather before quantization (embed_T == NULL: none)
@@ -280,7 +281,7 @@ __device__ void producer(const PersistParams& P, int n_items, uint8_t* ring, uin
   const uint32_t ring_w = smem_addr(ring) + (uint32_t)(w * P.nslots * kSlotBytes);
   const uint32_t full_w = full0 + 8u * w * kMaxSlots, empty_w = empty0 + 8u * w * kMaxSlots;
   uint32_t slot = 0, phase = 0, issued = 0, seq = 0;
-  bool ok = true;
+  bool ok = !P.no_copies;
   for (int i = 0; i < n_items && ok; ++i) {
     const WorkItem it = get_item(P, i);
     const uint8_t* base;
@@ -473,6 +474,7 @@ __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, ui
           *reinterpret_cast<uint32_t*>(abuf + b * act_k + k) = c;
           if (record) {
             const int64_t o = (int64_t)(b0 + b) * cs.K + k;
+            if (cs.cap) *reinterpret_cast<float4*>(cs.cap + o) = v[i];
             if (hq) *reinterpret_cast<uint32_t*>(hq + o) = c;
             for (int rr = 0; rr < n_rec; ++rr) *reinterpret_cast<uint32_t*>(const_cast<int8_t*>(rec[rr].q) + o) = c;
           }
@@ -524,10 +526,12 @@ __device__ void chain_prologue(const ChainSrc& cs, int b0, int nb, int act_k, ui
     const bool nz = m != 0.0f;
     const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
     for (int k = 4 * t; k < cs.K; k += 4 * C::CT) {
-      const uint32_t c = quant4(value4(b0 + b, k, r), s, nz);
+      const float4 v = value4(b0 + b, k, r);
+      const uint32_t c = quant4(v, s, nz);
       *reinterpret_cast<uint32_t*>(abuf + b * act_k + k) = c;
       if (record) {
         const int64_t o = (int64_t)(b0 + b) * cs.K + k;
+        if (cs.cap) *reinterpret_cast<float4*>(cs.cap + o) = v;
         if (hq) *reinterpret_cast<uint32_t*>(hq + o) = c;
         for (int r = 0; r < n_rec; ++r) *reinterpret_cast<uint32_t*>(const_cast<int8_t*>(rec[r].q) + o) = c;
       }
@@ -762,6 +766,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   // ---- consumers ----
   // Every consumer warp walks the same sequence of named and grid barriers whatever
   // happens; after an abort (s_abort) they only skip the work, so no barrier is left short.
+  // Launched as a programmatic dependent (the standalone output projection), the producer
+  // streams weights at once while the consumers wait here for the previous kernel: nothing
+  // below reads an input or writes an output before this point.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the standalone call lets the next kernel's CTAs take each SM as this kernel's CTA leaves it
+  if (!P.items) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0 && *reinterpret_cast<volatile unsigned int*>(&P.ctrl->error))
+    *s_abort = 1;  // an earlier wait that ran out poisons the control word until it is cleared
+  consumer_sync<C>();
   const int cw = warp;
   Ring rg{ring + cw * P.nslots * kSlotBytes, full0 + 8u * cw * kMaxSlots, empty0 + 8u * cw * kMaxSlots,
           0u, 0u, P.nslots};
@@ -860,6 +873,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
 
   if (P.has_head) {  // CTA best per vector, then the last CTA to finish reduces all CTAs
     volatile int& s_last = *reinterpret_cast<volatile int*>(smem + L.abort_flag + 4);
+    volatile int& s_fail = *reinterpret_cast<volatile int*>(smem + L.abort_flag + 8);
     consumer_sync<C>();
     if (threadIdx.x < P.B && !*s_abort) {
       HeadPartial b = hbest[threadIdx.x];
@@ -868,26 +882,41 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
         if (better(c.val, c.idx, b.val, b.idx)) b = c;
       }
       P.head_ws->part[(int64_t)blockIdx.x * P.B + threadIdx.x] = b;
-      __threadfence();
     }
     consumer_sync<C>();
-    if (threadIdx.x == 0) s_last = !*s_abort && atomicAdd(&P.ctrl->head_done, 1u) == gridDim.x - 1;
+    if (threadIdx.x == 0) {
+      // Every CTA counts itself, also one that gave up, so the counter always returns to zero.
+      // The fence orders this CTA's partials and any error it recorded before its arrival.
+      __threadfence();
+      const bool last = atomicAdd(&P.ctrl->head_done, 1u) == gridDim.x - 1;
+      if (last) __threadfence();
+      s_fail = last && (*s_abort || *reinterpret_cast<volatile unsigned int*>(&P.ctrl->error) != 0u);
+      s_last = last;
+    }
     consumer_sync<C>();
     if (s_last) {
-      __threadfence();
-      if (threadIdx.x < P.B) {
+      // warp w picks the winner of vector w (w + CW, ...): its lanes walk the CTAs' partials,
+      // then a shuffle reduction; a step in which some wait ran out reports -1 instead
+      const bool failed = s_fail;
+      for (int b = warp; b < P.B; b += C::CW) {
         float bv = -INFINITY;
         int bi = INT_MAX;
-        for (int c = 0; c < (int)gridDim.x; ++c) {
-          const HeadPartial* pp = &P.head_ws->part[(int64_t)c * P.B + threadIdx.x];
+        for (int c = lane; c < (int)gridDim.x && !failed; c += 32) {
+          const HeadPartial* pp = &P.head_ws->part[(int64_t)c * P.B + b];
           const float pv = __ldcg(&pp->val);
           const int pi = __ldcg(&pp->idx);
           if (better(pv, pi, bv, bi)) { bv = pv; bi = pi; }
         }
-        P.head_argmax[threadIdx.x] = bi == INT_MAX ? 0 : bi;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+          if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) P.head_argmax[b] = failed ? -1 : (bi == INT_MAX ? 0 : bi);
       }
       if (threadIdx.x == 0) P.ctrl->head_done = 0u;
-      if (P.verify_emit) {  // accept the longest agreeing draft prefix on the device
+      if (P.verify_emit && !failed) {  // accept the longest agreeing draft prefix on the device
         consumer_sync<C>();
         if (threadIdx.x == 0) *P.verify_n = verify_accept_device(P.verify_draft, P.head_argmax, P.B, P.verify_emit);
       }
@@ -1184,7 +1213,7 @@ bool persist_head_fits(int K, int B) {
 
 nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                               const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool pdl) {
   int dev = 0;
   NT_CUDA_TRY(cudaGetDevice(&dev));
   PersistParams P{};
@@ -1193,8 +1222,9 @@ nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, c
   if (!pick_config(B, P.act_k, &P.nslots, &P.chunk_b, &smem))
     return set_error(NT_ERR_INVALID_ARG, "output projection: K too large for the streaming kernel");
   NT_TRY(configure_kernel(dev));
-  // The workspace's 16-byte header serves as the control word (error, counter); it is zero
-  // before the first call and every successful call leaves it zero.
+  // The workspace's 16-byte status header serves as the control word (error, counter): zero
+  // before the first call, and every call leaves the counter zero; an error code stays until
+  // the caller clears the workspace.
   P.ctrl = reinterpret_cast<StepCtrl*>(ws);
   P.head_ws = ws;
   P.head_T = T;
@@ -1207,10 +1237,11 @@ nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, c
   P.head_K = K;
   P.has_head = 1;
   P.B = B;
-  P.timeout_ns = 250000000ull;
+  P.timeout_ns = test_fault_timeout_ns(250000000ull);
+  P.no_copies = test_fault() == kFaultHeadStream;
   const int grid = (int)std::min<int64_t>(device_sm_count(), V);
-  if (B == 1) persist_kernel<Cfg1><<<grid, Cfg1::THREADS, smem, st>>>(P);
-  else persist_kernel<CfgB><<<grid, CfgB::THREADS, smem, st>>>(P);
+  if (B == 1) NT_CUDA_TRY(launch_kernel(persist_kernel<Cfg1>, dim3(grid), dim3(Cfg1::THREADS), smem, st, pdl, P));
+  else NT_CUDA_TRY(launch_kernel(persist_kernel<CfgB>, dim3(grid), dim3(CfgB::THREADS), smem, st, pdl, P));
   return check_launch("persist_kernel (output projection)");
 }
 

@@ -381,6 +381,7 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     }
     p->mats = mats;
     p->n_cjobs = (int)cjobs.size();
+    p->cjobs = cjobs;
     if ((e = cudaMalloc(&p->d_cjobs, sizeof(ChainJob) * cjobs.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemcpy(p->d_cjobs, cjobs.data(), sizeof(ChainJob) * cjobs.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e, "cudaMemcpy");
@@ -577,6 +578,40 @@ nt_status nt_decode_plan_set_trace(nt_decode_plan* p, unsigned long long* trace)
   if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
   if (trace && !aligned(trace, 8)) return set_error(NT_ERR_ALIGNMENT, "trace must be 8-byte aligned");
   p->trace = trace;
+  return NT_OK;
+}
+
+nt_status nt_decode_plan_capture_size(const nt_decode_plan* p, size_t* floats) {
+  clear_error();
+  if (!p || !floats) return set_error(NT_ERR_INVALID_ARG, "NULL argument");
+  if (p->mode != NT_STEP_CHAINED) return set_error(NT_ERR_INVALID_ARG, "capture needs a chained plan");
+  size_t n = 0;
+  for (const PlanStage& s : p->stages) n += (size_t)p->B * p->mats[s.first_mat].K;
+  if (p->has_head) n += (size_t)p->B * p->head_K;
+  *floats = n;
+  return NT_OK;
+}
+
+nt_status nt_decode_plan_set_capture(nt_decode_plan* p, float* buf) {
+  clear_error();
+  if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
+  if (p->mode != NT_STEP_CHAINED) return set_error(NT_ERR_INVALID_ARG, "capture needs a chained plan");
+  if (buf && !aligned(buf, 16)) return set_error(NT_ERR_ALIGNMENT, "capture buffer must be 16-byte aligned");
+  // every stage's slice starts at B times the K of the stages before it (K % 16 == 0, so each
+  // slice stays 16-byte aligned)
+  size_t off = 0;
+  for (size_t i = 0; i < p->stages.size(); ++i) {
+    const PlanStage& s = p->stages[i];
+    float* cap = buf ? buf + off : nullptr;
+    for (int m = s.first_mat; m < s.first_mat + s.n_mats; ++m) p->mats[m].src.cap = cap;
+    p->cjobs[i].src.cap = cap;
+    off += (size_t)p->B * p->mats[s.first_mat].K;
+  }
+  p->head_src.cap = buf && p->has_head ? buf + off : nullptr;
+  if (p->has_head) p->cjobs[p->stages.size()].src.cap = p->head_src.cap;
+  NT_CUDA_TRY(cudaDeviceSynchronize());  // no step of this plan may be reading the descriptors
+  NT_CUDA_TRY(cudaMemcpy(p->d_mats, p->mats.data(), sizeof(MatDesc) * p->mats.size(), cudaMemcpyHostToDevice));
+  NT_CUDA_TRY(cudaMemcpy(p->d_cjobs, p->cjobs.data(), sizeof(ChainJob) * p->cjobs.size(), cudaMemcpyHostToDevice));
   return NT_OK;
 }
 

@@ -102,6 +102,7 @@ struct nt_decode_plan {
   float* d_chain_tmp = nullptr;     // [B][max K] stage inputs of the stream / graph launchers
   nt::ChainJob* d_cjobs = nullptr;  // one per stage, then one for the output projection
   int n_cjobs = 0;
+  std::vector<nt::ChainJob> cjobs;  // host copy of d_cjobs (nt_decode_plan_set_capture edits it)
   // chained steps with the attention side
   bool attn = false;
   int Hq = 0, Hkv = 0, t_stride = 0;
@@ -120,7 +121,9 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st);
 // Standalone output projection on the streaming kernel (no plan): B <= 16 and K small
 // enough for its shared-memory activation buffers.
 bool persist_head_fits(int K, int B);
+// With pdl the launch is a programmatic dependent one: the weight stream starts while the
+// previous kernel in the stream finishes.
 nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, const int8_t* q,
                               const float* s_x, int B, float* logits, int32_t* argmax, HeadWs* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, bool pdl);
 }  // namespace nt

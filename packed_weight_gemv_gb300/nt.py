@@ -36,7 +36,8 @@ NT_LAUNCH_STREAM = 2
 
 # Every symbol include/nt.h declares.
 EXPORTS = (
-    "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_device_check",
+    "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_workspace_status",
+    "nt_set_test_fault", "nt_device_check",
     "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
     "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_ternary_gemm_multi_workspace_size",
     "nt_ternary_gemm_multi", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
@@ -44,7 +45,8 @@ EXPORTS = (
     "nt_attention_workspace_size", "nt_attention_decode", "nt_rope_append", "nt_rmsnorm",
     "nt_decode_plan_create", "nt_decode_step", "nt_decode_step_status", "nt_decode_plan_reset",
     "nt_decode_plan_set_position",
-    "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_destroy",
+    "nt_decode_plan_trace_layout", "nt_decode_plan_set_trace", "nt_decode_plan_capture_size",
+    "nt_decode_plan_set_capture", "nt_decode_plan_destroy",
 )
 
 
@@ -102,6 +104,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_status_string": ([i], ctypes.c_char_p),
             "nt_last_error_string": ([], ctypes.c_char_p),
             "nt_device_check": ([ctypes.POINTER(i)], i),
+            "nt_workspace_status": ([vp, ctypes.POINTER(i)], i),
+            "nt_set_test_fault": ([i, ctypes.c_double], i),
             "nt_quantize_act": ([vp, i, i, vp, vp, vp], i),
             "nt_repack_size": ([i, i, ctypes.POINTER(sz)], i),
             "nt_repack_ternary": ([vp, i, i, vp, vp, vp], i),
@@ -127,6 +131,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_decode_plan_set_position": ([vp, i, vp], i),
             "nt_decode_plan_trace_layout": ([vp, ctypes.POINTER(i), ctypes.POINTER(i)], i),
             "nt_decode_plan_set_trace": ([vp, vp], i),
+            "nt_decode_plan_capture_size": ([vp, ctypes.POINTER(sz)], i),
+            "nt_decode_plan_set_capture": ([vp, vp], i),
             "nt_decode_plan_destroy": ([vp], None),
         }
         for name, (args, res) in sig.items():
@@ -156,6 +162,18 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def nt_abi_version() -> int:
     return load_library().nt_abi_version()
+
+
+def nt_workspace_status(ws: torch.Tensor) -> int:
+    """NT_OK or NT_ERR_TIMEOUT from a workspace's status header (synchronous)."""
+    st = ctypes.c_int(0)
+    _check(load_library().nt_workspace_status(_ptr(ws), ctypes.byref(st)), "nt_workspace_status")
+    return st.value
+
+
+def nt_set_test_fault(fault: int, timeout_ms: float = 0.0):
+    """Test hook of the per-call timeout paths (0 = off)."""
+    _check(load_library().nt_set_test_fault(fault, timeout_ms), "nt_set_test_fault")
 
 
 def nt_device_check() -> int:
@@ -387,6 +405,17 @@ class DecodePlan:
         """Installs a device int64 tensor of grid * (barriers + 1) * 4 values (or None)."""
         self._trace = trace
         _check(load_library().nt_decode_plan_set_trace(self._h, _ptr(trace)), "nt_decode_plan_set_trace")
+
+    def nt_decode_plan_capture_size(self) -> int:
+        """Floats of the stage-input capture buffer of a chained plan."""
+        n = ctypes.c_size_t(0)
+        _check(load_library().nt_decode_plan_capture_size(self._h, ctypes.byref(n)), "nt_decode_plan_capture_size")
+        return n.value
+
+    def nt_decode_plan_set_capture(self, buf: Optional[torch.Tensor]):
+        """Installs a device fp32 tensor of nt_decode_plan_capture_size() values (or None)."""
+        self._capture = buf
+        _check(load_library().nt_decode_plan_set_capture(self._h, _ptr(buf)), "nt_decode_plan_set_capture")
 
     def close(self):
         if getattr(self, "_h", None) and self._h.value:

@@ -65,16 +65,19 @@ def test_argument_errors_without_gpu(lib):
     assert _gemv(lib, 0, 1, 16, 16, 0x20000, 0x30000) == nt.NT_ERR_INVALID_ARG
     # the tensor-core path (tiled, B >= 64) needs a workspace: refused before any device call
     assert _gemv(lib, 0x10000, 1, 256, 512, 0x20000, 0x30000, B=64) == nt.NT_ERR_WORKSPACE
-    assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == 64 * 512 * 2 + 256 * 512 * 2
+    # every workspace starts with the 256-byte status header (16 bytes used, the rest keeps the
+    # data's alignment)
+    H = 256
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == H + 64 * 512 * 2 + 256 * 512 * 2
     # 2..16 vectors, from 128 rows: an optional workspace of e4m3 digit rows (16 for B <= 8,
     # else 32, K rounded up to 128), int32 partial sums [B][N] and one counter per 128-row
     # tile, rounded up to 16 bytes; below 128 rows sums and one counter per 256 rows; none for
     # one vector or above 16
     r16 = lambda b: (b + 15) // 16 * 16  # noqa: E731
-    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == r16(32 * 512 + 16 * 256 * 4 + 2 * 4)
-    assert nt.nt_ternary_gemm_workspace_size(1000, 512, 3, nt.NT_LAYOUT_TILED) == r16(16 * 512 + 3 * 1000 * 4 + 8 * 4)
-    assert nt.nt_ternary_gemm_workspace_size(1000, 208, 3, nt.NT_LAYOUT_TILED) == r16(16 * 256 + 3 * 1000 * 4 + 8 * 4)
-    assert nt.nt_ternary_gemm_workspace_size(100, 512, 3, nt.NT_LAYOUT_TILED) == (3 * 100 * 4 + 4 + 15) // 16 * 16
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_TILED) == H + r16(32 * 512 + 16 * 256 * 4 + 2 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(1000, 512, 3, nt.NT_LAYOUT_TILED) == H + r16(16 * 512 + 3 * 1000 * 4 + 8 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(1000, 208, 3, nt.NT_LAYOUT_TILED) == H + r16(16 * 256 + 3 * 1000 * 4 + 8 * 4)
+    assert nt.nt_ternary_gemm_workspace_size(100, 512, 3, nt.NT_LAYOUT_TILED) == H + (3 * 100 * 4 + 4 + 15) // 16 * 16
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 1, nt.NT_LAYOUT_TILED) == 0
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 17, nt.NT_LAYOUT_TILED) == 0
     assert nt.nt_ternary_gemm_workspace_size(256, 512, 16, nt.NT_LAYOUT_PLAIN) == 0
@@ -88,6 +91,17 @@ def test_argument_errors_without_gpu(lib):
     r = lib.nt_int8_logits_argmax(vp(0x1008), vp(0x2000), 10, 16, vp(0x3000), vp(0x4000), 1,
                                   None, vp(0x5000), vp(0x6000), 1 << 20, None)
     assert r == nt.NT_ERR_ALIGNMENT
+
+
+def test_status_and_fault_hook_without_gpu(lib):
+    st = ctypes.c_int(-1)
+    assert lib.nt_workspace_status(None, ctypes.byref(st)) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_workspace_status(ctypes.c_void_p(0x1000), None) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_set_test_fault(4, 1.0) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_set_test_fault(-1, 1.0) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_set_test_fault(0, 0.0) == nt.NT_OK
+    assert lib.nt_decode_plan_capture_size(None, ctypes.byref(ctypes.c_size_t(0))) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_decode_plan_set_capture(None, None) == nt.NT_ERR_INVALID_ARG
 
 
 def test_plan_descriptor_errors_without_gpu(lib):

@@ -43,6 +43,61 @@ def test_decode_step_8b_full_every_output():
     plan.close()
 
 
+def test_decode_step_8b_full_ordered_every_output():
+    # the same 36-layer step with a grid barrier before every stage (the ordered mode the
+    # benchmark's breakdown times): every projection and the full table against the oracle
+    projs = wl.decoder_projections()
+    head = wl.head()
+    dp, hd = plan_inputs(projs, head)
+    plan = nt.DecodePlan(36, 1, dp, hd, nt.NT_STEP_ORDERED, nt.NT_LAUNCH_PERSISTENT)
+    for _ in range(2):
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    for p, d in zip(projs, dp):
+        q, s = oracle.quantize(p.x)
+        assert np.array_equal(host(d["q"])[0], q[0]) and host(d["s_x"])[0] == s[0], p.name
+        _, y, _ = oracle.gemv(p.w_plain, p.s_w, p.N, p.K, q[0], s)
+        assert_close(host(d["y"])[0], y, p.name)
+    q, s = oracle.quantize(head.x)
+    logits, am, _ = oracle.logits_argmax(head.T, head.s_T, head.V, head.K, q, s)
+    assert_close(host(hd["logits"]), logits, "head")
+    assert int(host(hd["argmax"])[0]) == int(am[0])
+    plan.close()
+
+
+def test_decode_step_8b_full_chained_every_output():
+    # 36 chained layers of the 8B shape and the full table: every stage quantizes what the
+    # previous stages produced, so the whole trajectory is compared with the oracle's chained
+    # step -- every stage's codes and scale bit for bit, every output within 1e-6
+    L = wl.DECODER_8B_LAYERS
+    projs = wl.decoder_projections()
+    head = wl.head()
+    # Without normalisation the gated product squares the hidden state's size every layer; an
+    # input of about 1e-4 grows by ~1.3x per layer and stays finite through all 36 (the
+    # quantizer is scale-free, so the codes still use the full int8 range at every stage)
+    projs[0].x *= np.float32(1e-4)
+    dp, hd = plan_inputs(projs, head)
+    plan = nt.DecodePlan(L, 1, dp, hd, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_PERSISTENT)
+    for _ in range(2):  # the residual stream starts from the supplied input every step
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    layers = [[(p.w_plain, p.s_w, p.N, p.K) for p in projs[7 * l:7 * l + 7]] for l in range(L)]
+    want = oracle.decode_chained(layers, projs[0].x[:1], (head.T, head.s_T, head.V, head.K))
+    assert all(np.isfinite(h).all() and np.abs(h).max() < 1e6 for h in want["h"])
+    assert all(np.abs(q).max() == 127 for q in want["q"])  # every stage uses the full code range
+    for i, (p, d) in enumerate(zip(projs, dp)):
+        assert np.array_equal(host(d["q"]), want["q"][i]), p.name
+        assert np.array_equal(host(d["s_x"]), want["s"][i]), p.name
+        assert_close(host(d["y"]), want["y"][i], p.name)
+    assert np.array_equal(host(hd["q"]), want["head_q"])
+    assert np.array_equal(host(hd["sx"]), want["head_s"])
+    assert_close(host(hd["logits"]), want["logits"], "head")
+    assert np.array_equal(host(hd["argmax"]), want["argmax"])
+    plan.close()
+
+
 def test_zero_inputs_give_positive_zero_and_argmax_zero():
     shapes = {"q": (64, 512), "k": (16, 512), "v": (16, 512), "o": (64, 512),
               "gate": (128, 512), "up": (128, 512), "down": (64, 1024)}

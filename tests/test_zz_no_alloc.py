@@ -1,29 +1,24 @@
-"""The allocation-free output projection (nt_int8_logits_argmax_noalloc) against the regular
-call with a caller workspace, through the C ABI, on two calls in a row.
+"""The allocation-free output projection (nt_int8_logits_argmax_noalloc) through the C ABI,
+against the oracle and against the regular call with a caller workspace, over several calls in
+a row.
 
 That entry point is for callers that cannot allocate device memory (their host owns every
 allocation, or they must not risk cudaMalloc's device synchronization); it keeps its scratch
-in a fixed array of the library's device globals. Two consecutive calls on different inputs
-check that the scratch left by the first call does not leak into the second. This file is
-named to be collected last.
+in a fixed array of the library's device globals, sized for 16 vectors. The calls run the
+largest batch the array serves twice, then one vector twice (the streaming kernel), then a
+small batch, each on new inputs, so every kernel that uses the array runs on what the previous
+call of the same kernel left there. This file is named to be collected last.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from packed_weight_gemv_gb300 import nt
 from synth import workloads as wl
 from tests._gpu import DEV, assert_close, dev, host
 
 pytestmark = pytest.mark.gpu
-
-
-def _inputs(seed, V, K, B):
-    h = wl.head(V=V, K=K, B=B, seed=seed, workload=14)
-    q = torch.empty((B, K), dtype=torch.int8, device=DEV)
-    s = torch.empty(B, dtype=torch.float32, device=DEV)
-    nt.nt_quantize_act(dev(h.x), q, s)
-    return dev(h.T), dev(h.s_T), q, s
 
 
 def _with_workspace(T, s_T, V, K, q, s, B):
@@ -34,18 +29,23 @@ def _with_workspace(T, s_T, V, K, q, s, B):
     return host(logits), host(am)
 
 
-def test_noalloc_matches_workspace_call_twice():
+def test_noalloc_matches_oracle_over_calls_in_a_row():
     torch.cuda.set_device(DEV)
     V, K = 20011, 4096
-    for call, (seed, B) in enumerate([(21, 3), (22, 1)]):
-        T, s_T, q, s = _inputs(seed, V, K, B)
-        want_logits, want_am = _with_workspace(T, s_T, V, K, q, s, B)
+    for call, (seed, B) in enumerate([(21, 16), (22, 16), (23, 1), (24, 1), (25, 3)]):
+        h = wl.head(V=V, K=K, B=B, seed=seed, workload=14)
+        q, s = oracle.quantize(h.x)
+        want_logits, want_am, _ = oracle.logits_argmax(h.T, h.s_T, V, K, q, s)
+        T, s_T, qd, sd = dev(h.T), dev(h.s_T), dev(q), dev(s)
         logits = torch.full((B, V), float("nan"), device=DEV)
-        am = torch.full((B,), -1, dtype=torch.int32, device=DEV)
-        nt.nt_int8_logits_argmax_noalloc(T, s_T, V, K, q, s, B, logits, am)
+        am = torch.full((B,), -2, dtype=torch.int32, device=DEV)
+        nt.nt_int8_logits_argmax_noalloc(T, s_T, V, K, qd, sd, B, logits, am)
         torch.cuda.synchronize()
-        assert_close(host(logits), want_logits, f"no-alloc call {call + 1} logits")
-        assert np.array_equal(host(am), want_am), f"no-alloc call {call + 1} arg-max"
+        what = f"no-alloc call {call + 1} (B={B})"
+        assert_close(host(logits), want_logits, what + " logits")
+        assert np.array_equal(host(am), want_am), what + " arg-max"
+        ws_logits, ws_am = _with_workspace(T, s_T, V, K, qd, sd, B)
+        assert np.array_equal(host(logits), ws_logits) and np.array_equal(host(am), ws_am), what
 
 
 def test_noalloc_rejects_batch_beyond_scratch():
