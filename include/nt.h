@@ -84,7 +84,8 @@ typedef enum nt_status {
   NT_ERR_UNSUPPORTED = 3, /* the current device is not compute capability 10.3 (GB300) */
   NT_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed (detail string has it) */
   NT_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (decode plan or workspace status) */
-  NT_ERR_WORKSPACE = 6    /* the workspace is NULL or smaller than the size call reported */
+  NT_ERR_WORKSPACE = 6,   /* the workspace is NULL or smaller than the size call reported */
+  NT_ERR_INVALID_CODE = 7 /* a plain ternary matrix holds the invalid field code 10 */
 } nt_status;
 
 enum nt_layout { NT_LAYOUT_PLAIN = 0, NT_LAYOUT_TILED = 1 };
@@ -149,6 +150,18 @@ nt_status nt_quantize_act(const float* x, int B, int K, int8_t* q, float* s_x, v
  *                  invalid 10 fields it met (each decoded as 0).
  */
 nt_status nt_repack_size(int N, int K, size_t* bytes);
+
+/* Load-time check of a plain ternary matrix for the one field code the format leaves
+ * invalid (binary 10; the pages publish no format, so the 2-bit code is this library's
+ * reading). The kernels decode such a field as 0 and never check it on the hot path; a loader
+ * calls this once per matrix.
+ *   w_plain        [N][K/16] uint32 (device, 4-byte aligned); K % 16 == 0, N >= 1
+ *   n_invalid_opt  host uint64 or NULL: the number of invalid fields
+ * Returns NT_OK when every field is 00, 01 or 11, NT_ERR_INVALID_CODE otherwise. Synchronous:
+ * allocates an 8-byte device counter, runs one counting kernel on `stream`, waits for it and
+ * frees the counter (not a hot call). */
+nt_status nt_validate_ternary(const uint32_t* w_plain, int N, int K, uint64_t* n_invalid_opt,
+                              void* stream);
 nt_status nt_repack_ternary(const uint32_t* w_plain, int N, int K, void* w_tiled,
                             uint32_t* n_invalid_opt, void* stream);
 

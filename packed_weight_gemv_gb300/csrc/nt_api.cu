@@ -109,6 +109,7 @@ const char* nt_status_string(nt_status s) {
     case NT_ERR_CUDA: return "CUDA error";
     case NT_ERR_TIMEOUT: return "device-side wait timed out";
     case NT_ERR_WORKSPACE: return "workspace missing or too small";
+    case NT_ERR_INVALID_CODE: return "invalid ternary field code (binary 10)";
   }
   return "unknown status";
 }
@@ -172,6 +173,34 @@ nt_status nt_repack_ternary(const uint32_t* w_plain, int N, int K, void* w_tiled
   if (n_invalid_opt && !aligned(n_invalid_opt, 4)) return set_error(NT_ERR_ALIGNMENT, "counter must be 4-byte aligned");
   NT_TRY(check_device());
   return launch_repack(w_plain, N, K, static_cast<uint8_t*>(w_tiled), n_invalid_opt, as_stream(stream));
+}
+
+nt_status nt_validate_ternary(const uint32_t* w_plain, int N, int K, uint64_t* n_invalid_opt, void* stream) {
+  clear_error();
+  if (!w_plain) return set_error(NT_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (N < 1 || K < 16 || K % 16 != 0)
+    return set_error(NT_ERR_INVALID_ARG, "need N >= 1 and K a positive multiple of 16");
+  if (!aligned(w_plain, 4)) return set_error(NT_ERR_ALIGNMENT, "w_plain must be 4-byte aligned");
+  NT_TRY(check_device());
+  const cudaStream_t st = as_stream(stream);
+  unsigned long long* d_count = nullptr;
+  NT_CUDA_TRY(cudaMalloc(&d_count, sizeof *d_count));
+  unsigned long long count = 0;
+  cudaError_t e = cudaMemsetAsync(d_count, 0, sizeof *d_count, st);
+  nt_status s = e == cudaSuccess ? launch_validate(w_plain, N, K, d_count, st)
+                                 : set_error(NT_ERR_CUDA, std::string("cudaMemsetAsync: ") + cudaGetErrorString(e));
+  if (s == NT_OK && (e = cudaMemcpyAsync(&count, d_count, sizeof count, cudaMemcpyDeviceToHost, st)) == cudaSuccess)
+    e = cudaStreamSynchronize(st);
+  if (s == NT_OK && e != cudaSuccess) s = set_error(NT_ERR_CUDA, std::string("validate: ") + cudaGetErrorString(e));
+  cudaFree(d_count);
+  if (s != NT_OK) return s;
+  if (n_invalid_opt) *n_invalid_opt = count;
+  if (count) {
+    char buf[96];
+    snprintf(buf, sizeof buf, "%llu invalid 10 field(s)", count);
+    return set_error(NT_ERR_INVALID_CODE, buf);
+  }
+  return NT_OK;
 }
 
 nt_status nt_ternary_gemm_workspace_size(int N, int K, int B, int layout, size_t* bytes) {

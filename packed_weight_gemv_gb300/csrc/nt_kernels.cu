@@ -203,6 +203,19 @@ __global__ void __launch_bounds__(kThreads) repack_kernel(const uint32_t* __rest
   }
 }
 
+// Counts the invalid 10 fields of a plain matrix: a field is 10 when its high bit is set and
+// its low bit clear, so (w >> 1) & ~w & 0x55555555 has one bit per invalid field.
+__global__ void __launch_bounds__(kThreads) validate_kernel(const uint32_t* __restrict__ w, int64_t n_words,
+                                                            unsigned long long* __restrict__ n_invalid) {
+  unsigned int bad = 0;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_words; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t v = __ldg(w + i);
+    bad += __popc((v >> 1) & ~v & 0x55555555u);
+  }
+  bad = __reduce_add_sync(0xffffffffu, bad);
+  if ((threadIdx.x & 31) == 0 && bad) atomicAdd(n_invalid, (unsigned long long)bad);
+}
+
 // ---------------------------------------------------------------------------------------
 // Plain-layout projection: one warp per row, lanes over the row's words. NB activation
 // vectors per pass; larger batches loop over passes.
@@ -458,6 +471,15 @@ nt_status launch_repack(const uint32_t* w, int N, int K, uint8_t* out, uint32_t*
   if (g > cap) g = cap;
   repack_kernel<<<(int)g, kThreads, 0, st>>>(w, N, K, reinterpret_cast<uint32_t*>(out), n_invalid);
   return check_launch("repack_kernel");
+}
+
+nt_status launch_validate(const uint32_t* w, int N, int K, unsigned long long* n_invalid, cudaStream_t st) {
+  const int64_t words = (int64_t)N * (K / 16);
+  int64_t g = (words + kThreads - 1) / kThreads;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (g > cap) g = cap;
+  validate_kernel<<<(int)g, kThreads, 0, st>>>(w, words, n_invalid);
+  return check_launch("validate_kernel");
 }
 
 nt_status launch_gemv_plain(const uint32_t* w, const float* s_w, int N, int K, const int8_t* q,

@@ -95,6 +95,7 @@ nt_status launch_quantize(const float* x, int B, int K, int8_t* q, float* s, cud
 nt_status launch_quantize_jobs(const QuantJob* d_jobs, int n_jobs, int max_B, cudaStream_t st, bool pdl = false);
 nt_status launch_repack(const uint32_t* w, int N, int K, uint8_t* out, uint32_t* n_invalid,
                         cudaStream_t st);
+nt_status launch_validate(const uint32_t* w, int N, int K, unsigned long long* n_invalid, cudaStream_t st);
 nt_status launch_gemv_plain(const uint32_t* w, const float* s_w, int N, int K, const int8_t* q,
                             const float* s_x, int B, float* y, int32_t* acc, cudaStream_t st);
 nt_status launch_gemv_tiled(const MatDesc& m, cudaStream_t st);

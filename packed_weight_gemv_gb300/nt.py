@@ -24,6 +24,7 @@ NT_ERR_UNSUPPORTED = 3
 NT_ERR_CUDA = 4
 NT_ERR_TIMEOUT = 5
 NT_ERR_WORKSPACE = 6
+NT_ERR_INVALID_CODE = 7
 
 NT_LAYOUT_PLAIN = 0
 NT_LAYOUT_TILED = 1
@@ -38,7 +39,7 @@ NT_LAUNCH_STREAM = 2
 EXPORTS = (
     "nt_abi_version", "nt_status_string", "nt_last_error_string", "nt_workspace_status",
     "nt_set_test_fault", "nt_device_check",
-    "nt_quantize_act", "nt_repack_size", "nt_repack_ternary", "nt_ternary_gemv",
+    "nt_quantize_act", "nt_repack_size", "nt_validate_ternary", "nt_repack_ternary", "nt_ternary_gemv",
     "nt_ternary_gemm_workspace_size", "nt_ternary_gemm", "nt_ternary_gemm_multi_workspace_size",
     "nt_ternary_gemm_multi", "nt_int8_logits_workspace_size", "nt_int8_logits_argmax",
     "nt_int8_logits_argmax_noalloc", "nt_embed_rows", "nt_verify_accept",
@@ -109,6 +110,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "nt_quantize_act": ([vp, i, i, vp, vp, vp], i),
             "nt_repack_size": ([i, i, ctypes.POINTER(sz)], i),
             "nt_repack_ternary": ([vp, i, i, vp, vp, vp], i),
+            "nt_validate_ternary": ([vp, i, i, ctypes.POINTER(ctypes.c_uint64), vp], i),
             "nt_ternary_gemv": ([vp, i, vp, i, i, vp, vp, vp, vp, vp], i),
             "nt_ternary_gemm_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], i),
             "nt_ternary_gemm": ([vp, i, vp, i, i, vp, vp, i, vp, vp, vp, sz, vp], i),
@@ -191,6 +193,15 @@ def nt_quantize_act(x: torch.Tensor, q: torch.Tensor, s_x: torch.Tensor, stream=
 def nt_repack_size(N: int, K: int) -> int:
     n = ctypes.c_size_t(0)
     _check(load_library().nt_repack_size(N, K, ctypes.byref(n)), "nt_repack_size")
+    return n.value
+
+
+def nt_validate_ternary(w_plain: torch.Tensor, N: int, K: int, stream=None) -> int:
+    """Number of invalid 10 fields in a plain matrix (0 when valid); synchronous."""
+    n = ctypes.c_uint64(0)
+    st = load_library().nt_validate_ternary(_ptr(w_plain), N, K, ctypes.byref(n), _stream(stream))
+    if st not in (NT_OK, NT_ERR_INVALID_CODE):
+        _check(st, "nt_validate_ternary")
     return n.value
 
 

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.nt_abi_version() == 1
-    for s in range(7):
+    for s in range(8):
         assert lib.nt_status_string(s)
     assert b"unknown" in lib.nt_status_string(99)
 
@@ -91,6 +91,15 @@ def test_argument_errors_without_gpu(lib):
     r = lib.nt_int8_logits_argmax(vp(0x1008), vp(0x2000), 10, 16, vp(0x3000), vp(0x4000), 1,
                                   None, vp(0x5000), vp(0x6000), 1 << 20, None)
     assert r == nt.NT_ERR_ALIGNMENT
+
+
+def test_validate_argument_errors_without_gpu(lib):
+    vp, n = ctypes.c_void_p, ctypes.c_uint64(0)
+    assert lib.nt_validate_ternary(None, 4, 16, ctypes.byref(n), None) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_validate_ternary(vp(0x1000), 4, 15, ctypes.byref(n), None) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_validate_ternary(vp(0x1000), 0, 16, ctypes.byref(n), None) == nt.NT_ERR_INVALID_ARG
+    assert lib.nt_validate_ternary(vp(0x1002), 4, 16, ctypes.byref(n), None) == nt.NT_ERR_ALIGNMENT
+    assert b"10" in lib.nt_status_string(nt.NT_ERR_INVALID_CODE)
 
 
 def test_status_and_fault_hook_without_gpu(lib):

@@ -1,6 +1,8 @@
 """GPU parity: every C ABI call against the CPU oracle, element by element, on the same seeded
 inputs. Integer results (int8 codes, int32 accumulators, arg-max indices, repacked bytes) must
 match bit for bit; fp32 outputs within a relative error of 1e-6."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +63,22 @@ def test_repack_counts_invalid_fields():
     out = torch.empty(nt.nt_repack_size(N, K), dtype=torch.uint8, device=DEV)
     nt.nt_repack_ternary(dev(w), N, K, out, cnt)
     assert int(cnt.item()) == oracle.count_invalid(w) == 2
+
+
+@pytest.mark.parametrize("N,K,n_bad", [(9, 64, 0), (9, 64, 2), (1536, 512, 1), (4096, 4096, 977)])
+def test_validate_ternary(N, K, n_bad):
+    w = synth.ternary_plain(N, K, 6, N + K + n_bad)
+    rng = np.random.default_rng(N + n_bad)
+    flat = w.reshape(-1)
+    for i in rng.choice(flat.size * 16, size=n_bad, replace=False):  # distinct fields -> 10
+        word, f = divmod(int(i), 16)
+        flat[word] = (flat[word] & ~np.uint32(3 << (2 * f))) | np.uint32(2 << (2 * f))
+    assert oracle.count_invalid(w) == n_bad
+    wd = dev(w)
+    assert nt.nt_validate_ternary(wd, N, K) == n_bad
+    n = ctypes.c_uint64(7)
+    st = nt.load_library().nt_validate_ternary(ctypes.c_void_p(wd.data_ptr()), N, K, ctypes.byref(n), None)
+    assert st == (nt.NT_ERR_INVALID_CODE if n_bad else nt.NT_OK) and n.value == n_bad
 
 
 # ---- ternary projection ----------------------------------------------------------------
