@@ -78,6 +78,9 @@ struct PersistParams {
   float* head_logits;
   int32_t* head_argmax;
   HeadWs* head_ws;
+  unsigned int* head_next;  // kItemHeadDyn: counter of handed-out rows after the fixed ones
+  int head_fixed;           // kItemHeadDyn: rows each CTA takes before the counter (its own block)
+  int head_dyn;             // the implicit schedule (standalone call) uses kItemHeadDyn
   int head_V, head_K;
   int has_head;
   int B;         // activation vectors
@@ -110,7 +113,7 @@ __device__ __forceinline__ void stamp(const PersistParams& P, int b, int i) {
 }
 
 struct SmemLayout {
-  int ring, act, bars, hbest, red, abort_flag, chain_s, total;
+  int ring, act, bars, hbest, red, abort_flag, chain_s, slot_row, total;
 };
 
 template <class C>
@@ -123,7 +126,8 @@ __host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int a
   L.red = L.hbest + C::CW * kStepMaxBatch * (int)sizeof(HeadPartial);
   L.abort_flag = L.red + C::CW * 4 + (C::CHAINED ? 16 : 0);  // chained: the norm factor after the warps' values
   L.chain_s = L.abort_flag + 16;
-  L.total = L.chain_s + kStepMaxBatch * 4;
+  L.slot_row = L.chain_s + kStepMaxBatch * 4;   // kItemHeadDyn: the row each ring slot holds
+  L.total = L.slot_row + C::CW * kMaxSlots * 4;
   return L;
 }
 
@@ -244,12 +248,12 @@ __device__ __forceinline__ int item_count(const PersistParams& P) {
 __device__ __forceinline__ WorkItem get_item(const PersistParams& P, int i) {
   if (P.items) return P.items[P.item_off[blockIdx.x] + i];
   WorkItem w;
-  w.kind = kItemHead;
+  w.kind = P.head_dyn ? kItemHeadDyn : kItemHead;
   w.mat = 0;
   w.flags = 0;
   w.b0 = i * P.chunk_b;
-  w.begin = (int64_t)blockIdx.x * P.head_V / gridDim.x;
-  w.end = (int64_t)(blockIdx.x + 1) * P.head_V / gridDim.x;
+  w.begin = P.head_dyn ? 0 : (int64_t)blockIdx.x * P.head_V / gridDim.x;
+  w.end = P.head_dyn ? P.head_V : (int64_t)(blockIdx.x + 1) * P.head_V / gridDim.x;
   return w;
 }
 
@@ -276,32 +280,65 @@ __device__ __forceinline__ int64_t first_unit(const WorkItem& it, uint32_t seq, 
 // Lane w of the producer warp feeds consumer warp w's ring.
 template <class C>
 __device__ void producer(const PersistParams& P, int n_items, uint8_t* ring, uint32_t full0,
-                         uint32_t empty0, volatile int* s_abort, int w) {
+                         uint32_t empty0, volatile int* s_abort, int* slot_row, int w) {
   const uint64_t pol = evict_first_policy();
   const uint32_t ring_w = smem_addr(ring) + (uint32_t)(w * P.nslots * kSlotBytes);
   const uint32_t full_w = full0 + 8u * w * kMaxSlots, empty_w = empty0 + 8u * w * kMaxSlots;
+  int* rows_w = slot_row + w * kMaxSlots;
   uint32_t slot = 0, phase = 0, issued = 0, seq = 0;
   bool ok = !P.no_copies;
+  // Copies unit u (ub bytes at base + u * ub) chunk by chunk into this lane's ring; with a row
+  // index (kItemHeadDyn) the consumer learns which row each slot holds from rows_w.
+  auto issue_unit = [&](const uint8_t* base, int ub, int64_t u, int row) {
+    const uint8_t* src = base + u * (int64_t)ub;
+    for (int off = 0; off < ub && ok; off += kSlotBytes) {
+      const uint32_t bytes = (uint32_t)min(kSlotBytes, ub - off);
+      if (!wait_phase(empty_w + 8 * slot, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
+        if (!*s_abort) record_error(P.ctrl, kErrEmptyWait, s_abort);
+        ok = false;
+        break;
+      }
+      rows_w[slot] = row;  // ordered before the consumer's wait by the arrive's release
+      mbar_expect_tx(full_w + 8 * slot, bytes);
+      bulk_load(ring_w + slot * kSlotBytes, src + off, bytes, full_w + 8 * slot, pol);
+      ++issued;
+      if (++slot == (uint32_t)P.nslots) { slot = 0; phase ^= 1u; }
+    }
+  };
   for (int i = 0; i < n_items && ok; ++i) {
     const WorkItem it = get_item(P, i);
     const uint8_t* base;
     int ub;
     unit_geometry(P, it, base, ub);
-    for (int64_t u = first_unit<C>(it, seq, w); u < it.end && ok; u += C::CW) {
-      const uint8_t* src = base + u * (int64_t)ub;
-      for (int off = 0; off < ub; off += kSlotBytes) {
-        const uint32_t bytes = (uint32_t)min(kSlotBytes, ub - off);
-        if (!wait_phase(empty_w + 8 * slot, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
-          if (!*s_abort) record_error(P.ctrl, kErrEmptyWait, s_abort);
-          ok = false;
-          break;
-        }
-        mbar_expect_tx(full_w + 8 * slot, bytes);
-        bulk_load(ring_w + slot * kSlotBytes, src + off, bytes, full_w + 8 * slot, pol);
-        ++issued;
-        if (++slot == (uint32_t)P.nslots) { slot = 0; phase ^= 1u; }
+    if (it.kind == kItemHeadDyn) {  // always a CTA's last item
+      // this CTA's own block of fixed rows first (issued before the previous kernel has finished,
+      // for the standalone call), then CW rows per grab, one per lane, until the table is done
+      const int64_t f0 = (int64_t)blockIdx.x * P.head_fixed;
+      for (int64_t r = f0 + w; r < f0 + P.head_fixed && ok; r += C::CW) issue_unit(base, ub, r, (int)r);
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the counter is the previous call's until it ends
+      const int64_t dyn0 = (int64_t)gridDim.x * P.head_fixed;
+      constexpr unsigned int kLanes = (1u << C::CW) - 1u;
+      for (;;) {
+        unsigned int g = 0;
+        if (w == 0) g = atomicAdd(P.head_next, (unsigned int)C::CW);
+        g = __shfl_sync(kLanes, g, 0);
+        if (dyn0 + (int64_t)g >= it.end || !__all_sync(kLanes, ok)) break;
+        const int64_t r = dyn0 + (int64_t)g + w;
+        if (r < it.end) issue_unit(base, ub, r, (int)r);
       }
+      // end of the stream: a slot whose row is -1, its phase completed by a plain arrival
+      if (ok && wait_phase(empty_w + 8 * slot, phase ^ 1u, P.timeout_ns, P.ctrl, s_abort)) {
+        rows_w[slot] = -1;
+        mbar_arrive(full_w + 8 * slot);
+        ++issued;  // the drain below treats it as this slot's last use (its phase is complete)
+        if (++slot == (uint32_t)P.nslots) { slot = 0; phase ^= 1u; }
+      } else if (ok) {
+        if (!*s_abort) record_error(P.ctrl, kErrEmptyWait, s_abort);
+        ok = false;
+      }
+      continue;
     }
+    for (int64_t u = first_unit<C>(it, seq, w); u < it.end && ok; u += C::CW) issue_unit(base, ub, u, 0);
     seq += (uint32_t)(it.end - it.begin);
   }
   // Drain: every slot's last copy must have landed before this thread (and so the CTA)
@@ -708,7 +745,7 @@ __device__ __forceinline__ void consume_head_row(const PersistParams& P, const f
 template <class C, int NB>
 __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkItem& it, uint32_t seq, const uint8_t* act,
                              Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort,
-                             const float* s_chain) {
+                             const float* s_chain, const int* slot_row) {
   float sx[NB];
   const float* sxp = it.kind == kItemTernary ? P.mats[it.mat].s_x : P.head_sx;
 #pragma unroll
@@ -723,6 +760,17 @@ __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkI
     for (int64_t u = first; u < it.end; u += C::CW)
       if (!__shfl_sync(0xffffffffu, *s_abort, 0))
         consume_tile<NB, C::CHAINED>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
+  } else if (it.kind == kItemHeadDyn) {
+    // rows in the order the producer lane handed them out; the slot of a row's first chunk
+    // names it, and a slot naming row -1 ends the stream
+    const int* rows = slot_row + cw * kMaxSlots;
+    for (;;) {
+      if (__shfl_sync(0xffffffffu, *s_abort, 0)) break;
+      if (wait_chunk(P, ring, lane, s_abort) == nullptr) break;  // a wait ran out
+      const int r = rows[ring.slot];
+      if (r < 0) break;
+      consume_head_row<NB>(P, sx, it.b0, r, act, ring, wbest, lane, s_abort);  // its first wait returns at once
+    }
   } else {
     for (int64_t u = first; u < it.end; u += C::CW)
       if (!__shfl_sync(0xffffffffu, *s_abort, 0))
@@ -741,6 +789,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   float* red = reinterpret_cast<float*>(smem + L.red);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.abort_flag);
   float* s_chain = reinterpret_cast<float*>(smem + L.chain_s);
+  int* slot_row = reinterpret_cast<int*>(smem + L.slot_row);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + C::BARS);
@@ -759,7 +808,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   const int n_items = item_count(P);
   stamp(P, 0, 0);
   if (warp == C::CW) {
-    if (lane < C::CW) producer<C>(P, n_items, ring, full0, empty0, s_abort, lane);
+    if (lane < C::CW) producer<C>(P, n_items, ring, full0, empty0, s_abort, slot_row, lane);
     return;
   }
 
@@ -855,13 +904,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       abuf = ab;
     }
     if constexpr (C::NBMAX == 1) {
-      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc);
+      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row);
     } else {
       switch (nb) {
-        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
-        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
-        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
-        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc); break;
+        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
+        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
+        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
+        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
       }
     }
     seq += (uint32_t)(it.end - it.begin);
@@ -915,7 +964,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
         }
         if (lane == 0) P.head_argmax[b] = failed ? -1 : (bi == INT_MAX ? 0 : bi);
       }
-      if (threadIdx.x == 0) P.ctrl->head_done = 0u;
+      if (threadIdx.x == 0) {
+        P.ctrl->head_done = 0u;
+        if (P.head_next) *P.head_next = 0u;  // every producer's last grab came before its CTA arrived
+      }
       if (P.verify_emit && !failed) {  // accept the longest agreeing draft prefix on the device
         consumer_sync<C>();
         if (threadIdx.x == 0) *P.verify_n = verify_accept_device(P.verify_draft, P.head_argmax, P.B, P.verify_emit);
@@ -983,6 +1035,15 @@ bool pick_config_for(int B, int act_k, int* nslots, int* chunk_b, size_t* smem) 
   return false;
 }
 
+// Rows of the output table each CTA takes before it starts drawing rows from the counter
+// (kItemHeadDyn): as many as every producer lane's ring holds at once, so the standalone call
+// issues them without waiting for a slot, and never more than the table has for every CTA.
+int head_fixed_rows(int cw, int nslots, int K, int V, int grid) {
+  const int per_row = (int)((K + kSlotBytes - 1) / kSlotBytes);
+  const int fixed = cw * (nslots / per_row);
+  return std::min(fixed, V / std::max(grid, 1));
+}
+
 bool pick_config(int B, int act_k, int* nslots, int* chunk_b, size_t* smem) {
   return B == 1 ? pick_config_for<Cfg1>(B, act_k, nslots, chunk_b, smem)
                 : pick_config_for<CfgB>(B, act_k, nslots, chunk_b, smem);
@@ -1000,6 +1061,12 @@ nt_status configure_kernel(int device) {
   NT_CUDA_TRY(cudaFuncSetAttribute(persist_kernel<CfgBC>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
   if (device >= 0 && device < 64) g_attr_set[device] = true;
   return NT_OK;
+}
+
+// Consumer warps of the kernel instance for a batch and step mode.
+int kernel_cw(int B, bool chained) {
+  if (chained) return B == 1 ? Cfg1C::CW : CfgBC::CW;
+  return B == 1 ? Cfg1::CW : CfgB::CW;
 }
 
 // The kernel instance and block size for a batch and step mode.
@@ -1041,14 +1108,23 @@ nt_status persist_prepare(nt_decode_plan* p) {
   const Unitset head{kItemHead, 0, p->head_V, p->head_K};
   const bool chained = p->mode == NT_STEP_CHAINED;
   int barriers = (p->n_qjobs > 0 ? 1 : 0) + (p->embed_T && (p->n_qjobs > 0 || chained) ? 1 : 0);
+  p->head_fixed = 0;
   if (p->mode == NT_STEP_INDEPENDENT) {
-    // Each CTA gets 1/grid of the ternary bytes and 1/grid of the output table (per pass),
-    // so every CTA has the same mix of decode-heavy and decode-free work.
+    // Each CTA gets 1/grid of the ternary bytes. The output table follows as rows handed out
+    // at run time (one pass: every CTA ends with the same dynamic item, so CTAs that finish
+    // their ternary share early take more rows and all finish together); with several passes
+    // each CTA gets 1/grid of the table per pass.
+    const bool dyn = p->has_head && p->B <= p->chunk_b;
+    if (dyn) p->head_fixed = head_fixed_rows(kernel_cw(p->B, false), p->nslots, p->head_K, p->head_V, grid);
     for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) {
       std::vector<Unitset> all;
       for (int i = 0; i < n_proj; ++i) all.push_back(ternary(i));
       partition_stage(all, grid, b0, false, per_cta);
-      if (p->has_head) partition_stage({head}, grid, b0, false, per_cta);
+      if (dyn) {
+        for (int c = 0; c < grid; ++c) per_cta[c].push_back(WorkItem{kItemHeadDyn, 0, 0, b0, 0, p->head_V});
+      } else if (p->has_head) {
+        partition_stage({head}, grid, b0, false, per_cta);
+      }
     }
   } else if (chained && p->attn) {
     // one launch per segment; the attention side runs between segments
@@ -1140,6 +1216,8 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.head_logits = p->head_logits;
   P.head_argmax = p->head_argmax;
   P.head_ws = p->d_head_ws;
+  P.head_next = &p->d_ctrl->head_next;
+  P.head_fixed = p->head_fixed;
   P.head_V = p->head_V;
   P.head_K = p->head_K;
   P.has_head = p->has_head ? 1 : 0;
@@ -1237,9 +1315,14 @@ nt_status persist_launch_head(const int8_t* T, const float* s_T, int V, int K, c
   P.head_K = K;
   P.has_head = 1;
   P.B = B;
+  const int grid = (int)std::min<int64_t>(device_sm_count(), V);
+  // one pass: rows handed out at run time (the counter is the header's third word, which the
+  // standalone call has no other use for)
+  P.head_dyn = B <= P.chunk_b ? 1 : 0;
+  P.head_next = reinterpret_cast<unsigned int*>(ws) + 2;
+  P.head_fixed = head_fixed_rows(B == 1 ? Cfg1::CW : CfgB::CW, P.nslots, K, V, grid);
   P.timeout_ns = test_fault_timeout_ns(250000000ull);
   P.no_copies = test_fault() == kFaultHeadStream;
-  const int grid = (int)std::min<int64_t>(device_sm_count(), V);
   if (B == 1) NT_CUDA_TRY(launch_kernel(persist_kernel<Cfg1>, dim3(grid), dim3(Cfg1::THREADS), smem, st, pdl, P));
   else NT_CUDA_TRY(launch_kernel(persist_kernel<CfgB>, dim3(grid), dim3(CfgB::THREADS), smem, st, pdl, P));
   return check_launch("persist_kernel (output projection)");

@@ -25,10 +25,14 @@ struct StepCtrl {
   unsigned int error_cta;
   unsigned int arrive;     // grid-barrier arrivals (wraps; compared modulo 2^32)
   unsigned int head_done;  // CTAs finished with the output projection's arg-max
+  unsigned int head_next;  // output-table rows handed out so far (dynamic rows; the last CTA resets it)
+  unsigned int pad_[3];
 };
 
-// One contiguous run of work for one CTA of the persistent kernel.
-enum : int { kItemTernary = 0, kItemHead = 1 };
+// One contiguous run of work for one CTA of the persistent kernel. kItemHeadDyn: the output
+// table's rows handed out at run time (a few fixed rows per CTA first, then CW rows per grab from
+// a global counter), so that CTAs on SMs that stream faster take more rows.
+enum : int { kItemTernary = 0, kItemHead = 1, kItemHeadDyn = 2 };
 enum : int { kFlagStage = 1 };  // a grid-wide barrier precedes this item (ordered mode)
 struct WorkItem {
   int kind;      // kItemTernary (begin/end count tiles of mats[mat]) or kItemHead (rows)
@@ -87,6 +91,7 @@ struct nt_decode_plan {
   size_t smem_bytes = 0;
   int act_stride = 0;               // bytes of one activation vector in shared memory
   int nslots = 0, chunk_b = 0;      // ring slots per consumer warp; vectors per pass
+  int head_fixed = 0;               // output-table rows per CTA before the dynamic ones (independent mode)
   uint64_t launches = 0;
   uint32_t barrier_count = 0;       // grid barriers passed by all launches so far (mod 2^32)
   // chained plans with the attention side: one persistent launch per segment (the stages
