@@ -1167,6 +1167,54 @@ def run_prefill(args):
         torch.cuda.empty_cache()
 
 
+# ---------------------------------------------------------------------------------------
+# One prefill-shaped GEMM (not the headline line): a single nt_ternary_gemm call of M tokens
+# against one N x K ternary matrix on the tensor cores -- the case the prefill kernel's
+# profiles are taken on
+# ---------------------------------------------------------------------------------------
+
+def run_gemm(args):
+    import torch
+
+    import oracle
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    M, N, K = args.gemm
+    w = wl.ternary_plain(N, K, 0, wl.tag(wl.WL_PREFILL, 98, 0, wl.ROLE_TRITS))
+    s_w = wl.scales(N, np.sqrt(K), 0, wl.tag(wl.WL_PREFILL, 98, 0, wl.ROLE_ROW_SCALE))
+    x = wl.normal(M * K, 0, wl.tag(wl.WL_PREFILL, 98, K, wl.ROLE_X)).reshape(M, K)
+    q, s = oracle.quantize(x)
+    wt = torch.empty(nt.nt_repack_size(N, K), dtype=torch.uint8, device=dev)
+    nt.nt_repack_ternary(torch.from_numpy(w.view(np.int32)).to(dev), N, K, wt)
+    swd, qd, sd = torch.from_numpy(s_w).to(dev), torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    ws = torch.zeros(nt.nt_ternary_gemm_workspace_size(N, K, M, nt.NT_LAYOUT_TILED), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        nt.nt_ternary_gemm(wt, nt.NT_LAYOUT_TILED, swd, N, K, qd, sd, M, y, ws=ws, stream=stream)
+    torch.cuda.synchronize()
+    rows = np.linspace(0, M - 1, 16).astype(np.int64)
+    _, yo, _ = oracle.gemm(w, s_w, N, K, q[rows], s[rows])
+    got = y.cpu().numpy()[rows].astype(np.float64)
+    parity = "pass" if np.all(np.abs(got - yo) <= 1e-6 * np.abs(yo.astype(np.float64))) else "differs"
+    steps = max(3, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        nt.nt_ternary_gemm(wt, nt.NT_LAYOUT_TILED, swd, N, K, qd, sd, M, y, ws=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    if nt.nt_workspace_status(ws) != nt.NT_OK:
+        parity = "timeout reported"
+    print(json.dumps({"metric": "prefill ternary GEMM, one call", "M": M, "N": N, "K": K, "calls": steps,
+                      "us_per_call": round(us, 2), "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 1),
+                      "kernels": "act_f16_kernel + gemm_tc_kernel", "parity_16_tokens": parity}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1194,6 +1242,8 @@ def main():
                     help="--layer-attention, --sweep: launchers to time (persistent,graph)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
+    ap.add_argument("--gemm", type=lambda v: [int(x) for x in v.split(",")], default=None,
+                    help="one prefill-shaped GEMM M,N,K (the profiling case of the prefill kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -1217,6 +1267,9 @@ def main():
         return
     if args.prefill:
         run_prefill(args)
+        return
+    if args.gemm:
+        run_gemm(args)
         return
     if world > 1:
         import torch

@@ -186,8 +186,9 @@ nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, in
  * Results equal B independent nt_ternary_gemv calls, bit for bit. Any B >= 1 is accepted.
  * With NT_LAYOUT_TILED, B >= 64 and K <= 131072 the call runs on the tensor cores and needs
  * a workspace of nt_ternary_gemm_workspace_size bytes (16-byte aligned device memory; its
- * contents are scratch: bf16 copies of this call's activations and weights, overwritten by
- * the next call that uses it; calls sharing it must not overlap). A missing or short
+ * contents are scratch: an f16 copy of this call's activations, overwritten by the next call
+ * that uses it -- the weights are read in their packed form and decoded inside the kernel;
+ * calls sharing it must not overlap). A missing or short
  * workspace returns NT_ERR_WORKSPACE.
  * With NT_LAYOUT_TILED and 2 <= B <= 16 the workspace is optional: given one of at least
  * nt_ternary_gemm_workspace_size bytes (16-byte aligned, zero-filled before its first use;

@@ -68,7 +68,8 @@ def test_argument_errors_without_gpu(lib):
     # every workspace starts with the 256-byte status header (16 bytes used, the rest keeps the
     # data's alignment)
     H = 256
-    assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == H + 64 * 512 * 2 + 256 * 512 * 2
+    # prefill: the status header and an f16 copy of the activations (the weights stay packed)
+    assert nt.nt_ternary_gemm_workspace_size(256, 512, 64, nt.NT_LAYOUT_TILED) == H + 64 * 512 * 2
     # 2..16 vectors, from 128 rows: an optional workspace of e4m3 digit rows (16 for B <= 8,
     # else 32, K rounded up to 128), int32 partial sums [B][N] and one counter per 128-row
     # tile, rounded up to 16 bytes; below 128 rows sums and one counter per 256 rows; none for

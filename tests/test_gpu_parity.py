@@ -392,7 +392,7 @@ def test_tcgen05_batched_timeout_is_reported_and_recoverable(launcher):
 # ---- prefill-shaped batches on the tensor cores -----------------------------------------
 
 TC_SHAPES = [(128, 256, 512), (200, 260, 1024), (64, 20, 528), (256, 3072, 1024),
-             (2048, 1024, 3072), (130, 1024, 2048)]
+             (2048, 1024, 3072), (130, 1024, 2048), (8192, 640, 2048), (97, 4100, 1040)]
 
 
 @pytest.mark.parametrize("M,N,K", TC_SHAPES)
