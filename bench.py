@@ -1168,6 +1168,57 @@ def run_prefill(args):
 
 
 # ---------------------------------------------------------------------------------------
+# Step timeline (not the headline line): where the time between stages of the ordered and
+# chained persistent steps goes, from the plan's per-CTA %globaltimer stamps
+# ---------------------------------------------------------------------------------------
+
+def run_timeline(args):
+    import torch
+
+    from packed_weight_gemv_gb300 import nt
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nt.nt_device_check()
+    L = args.layers
+    projs, head, dp, hd, _ = build_inputs(torch, nt, dev, L)
+    stream = torch.cuda.current_stream()
+    kinds = {1: "o", 2: "gate_up", 3: "down", 0: "qkv"}
+    for mode, name in ((nt.NT_STEP_ORDERED, "ordered"), (nt.NT_STEP_CHAINED, "chained")):
+        plan = nt.DecodePlan(L, 1, dp, hd, mode, nt.NT_LAUNCH_PERSISTENT)
+        G, S = plan.nt_decode_plan_trace_layout()
+        n_pre = S - 4 * L  # barriers before the first stage boundary (input quantization)
+        steps = max(3, min(args.steps, 200))
+        us = time_steps(torch, plan, steps, stream) / steps
+        tr = torch.zeros(G * (S + 1) * 4, dtype=torch.int64, device=dev)
+        plan.nt_decode_plan_set_trace(tr)
+        for _ in range(3):
+            plan.nt_decode_step(stream)
+        torch.cuda.synchronize()
+        t = tr.cpu().numpy().reshape(G, S + 1, 4).astype(np.int64)
+        t = (t - t[:, 0, 0].min()) / 1000.0
+        acc = {}
+        for b in range(1, S + 1):
+            done, pas, act = t[:, b, 0], t[:, b, 1], t[:, b, 2]
+            nxt = t[:, b + 1, 0] if b < S else t[:, 0, 1]
+            i = b - n_pre
+            k = "quantize" if i <= 0 else ("head" if i == 4 * L else kinds[i % 4])
+            acc.setdefault(k, []).append((done.max() - np.median(done), pas.min() - done.max(),
+                                          np.median(act - pas), np.median(nxt) - np.median(act)))
+        by = {k: dict(zip(("tail_us", "barrier_release_us", "stage_input_us", "stage_work_us"),
+                          [round(float(x), 2) for x in np.mean(v, axis=0)]), count=len(v)) for k, v in acc.items()}
+        print(json.dumps({"metric": "step timeline", "mode": name, "layers": L, "us_per_token": round(us, 2),
+                          "barriers": S, "trace_span_us": round(float(t[:, 0, 1].max()), 1), "before_stage": by,
+                          "what": ("per boundary, averaged per stage kind: tail = last CTA done - median CTA done; "
+                                   "barrier_release = first CTA past the barrier - last CTA done; stage_input = "
+                                   "median (activations ready - barrier passed; chained: the stage input quantized "
+                                   "from L2); stage_work = median next done - median activations ready")}),
+              flush=True)
+        plan.nt_decode_plan_set_trace(None)
+        plan.close()
+
+
+# ---------------------------------------------------------------------------------------
 # One prefill-shaped GEMM (not the headline line): a single nt_ternary_gemm call of M tokens
 # against one N x K ternary matrix on the tensor cores -- the case the prefill kernel's
 # profiles are taken on
@@ -1242,6 +1293,8 @@ def main():
                     help="--layer-attention, --sweep: launchers to time (persistent,graph)")
     ap.add_argument("--prefill", action="store_true",
                     help="prefill GEMMs of the 28-layer small model at 2048 and 8192 tokens")
+    ap.add_argument("--timeline", action="store_true",
+                    help="per-boundary step timeline of the ordered and chained persistent steps")
     ap.add_argument("--gemm", type=lambda v: [int(x) for x in v.split(",")], default=None,
                     help="one prefill-shaped GEMM M,N,K (the profiling case of the prefill kernel)")
     args = ap.parse_args()
@@ -1270,6 +1323,9 @@ def main():
         return
     if args.gemm:
         run_gemm(args)
+        return
+    if args.timeline:
+        run_timeline(args)
         return
     if world > 1:
         import torch
