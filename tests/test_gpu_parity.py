@@ -45,6 +45,50 @@ def test_quantize(B, K, kind):
     assert np.array_equal(host(s), os_)
 
 
+def half_integer_quotients(m: float) -> np.ndarray:
+    """A vector of absmax m whose quotients x / s (s = fl(m / 127)) sit on and beside every
+    half-integer k + 0.5: the products fl((k + 0.5) s) and their neighbours up to 3 ulps away,
+    padded to a multiple of 16 with m."""
+    m = np.float32(m)
+    s = m / np.float32(127)
+    vals = [m, -m]
+    for k in range(-127, 127):
+        x = np.float32(np.float32(k + 0.5) * s)
+        if abs(x) > m:
+            continue
+        vals.append(x)
+        up, down = x, x
+        for _ in range(3):
+            up, down = np.nextafter(up, np.float32(np.inf)), np.nextafter(down, np.float32(-np.inf))
+            vals += [v for v in (up, down) if abs(v) <= m]
+    vals += [m] * (-len(vals) % 16)
+    return np.array(vals, dtype=np.float32)
+
+
+@pytest.mark.parametrize("m", [100.0, 3.7, 1e-3, 55.55, 127.0, 0.1])
+def test_quantize_half_integer_quotients(m):
+    # The kernels form the quotient as x * fl(1/s) and fall back to the IEEE division near a
+    # half-integer; these inputs sit exactly there. Per call and in a decode step's first phase.
+    x = half_integer_quotients(m)
+    oq, os_ = oracle.quantize(x)
+    q = torch.empty(x.size, dtype=torch.int8, device=DEV)
+    s = torch.empty(1, dtype=torch.float32, device=DEV)
+    nt.nt_quantize_act(dev(x), q, s)
+    assert np.array_equal(host(q), oq.reshape(-1)) and host(s)[0] == os_[0]
+    K = x.size
+    shapes = {n: (64, K) for n in wl.PROJ_NAMES}
+    projs = wl.decoder_projections(1, shapes, seed=8, workload=44)
+    for p in projs:
+        p.x[0] = x
+    dp, _ = plan_inputs(projs, None)
+    plan = nt.DecodePlan(1, 1, dp, None, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    for d in dp:
+        assert np.array_equal(host(d["q"])[0], oq.reshape(-1)) and host(d["s_x"])[0] == os_[0]
+    plan.close()
+
+
 # ---- load-time repack ------------------------------------------------------------------
 
 @pytest.mark.parametrize("N,K", [(1536, 512), (5, 48), (7, 528), (13, 1040), (1024, 4096), (4, 12288)])
