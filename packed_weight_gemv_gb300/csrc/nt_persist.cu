@@ -124,7 +124,7 @@ __host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int a
   L.bars = L.act + 2 * chunk_b * act_k;
   L.hbest = L.bars + 2 * C::BARS * 8;
   L.red = L.hbest + C::CW * kStepMaxBatch * (int)sizeof(HeadPartial);
-  L.abort_flag = L.red + C::CW * 4 + (C::CHAINED ? 16 : 0);  // chained: the norm factor after the warps' values
+  L.abort_flag = L.red + 2 * C::CW * 4 + (C::CHAINED ? 16 : 0);  // chained: the norm factor after the warps' values
   L.chain_s = L.abort_flag + 16;
   L.slot_row = L.chain_s + kStepMaxBatch * 4;   // kItemHeadDyn: the row each ring slot holds
   L.total = L.slot_row + C::CW * kMaxSlots * 4;
@@ -386,12 +386,15 @@ __device__ __forceinline__ void release_chunk(Ring& r, int lane) {
   if (++r.slot == (uint32_t)r.nslots) { r.slot = 0; r.phase ^= 1u; }
 }
 
-// Quantize one fp32 vector with the consumer threads.
+// Quantize one fp32 vector with the consumer threads: s = fl(max|x| / 127), q[k] =
+// clamp(rint(fl(x[k] / s)), -127, 127), in two passes over x (the second from L2). x is read
+// through L2: the input-table rows that other CTAs wrote earlier in the same launch are
+// quantized here.
 template <class C>
 __device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_out, float* red) {
   const int t = threadIdx.x;
   float m = 0.0f;
-  for (int k = t; k < K; k += C::CT) m = fmaxf(m, fabsf(x[k]));
+  for (int k = t; k < K; k += C::CT) m = fmaxf(m, fabsf(__ldcg(x + k)));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if ((t & 31) == 0) red[t >> 5] = m;
@@ -399,17 +402,99 @@ __device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_ou
   m = red[0];
 #pragma unroll
   for (int i = 1; i < C::CW; ++i) m = fmaxf(m, red[i]);
-  const float s = (m == 0.0f) ? 0.0f : __fdiv_rn(m, 127.0f);
+  const bool nz = m != 0.0f;
+  const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
   if (t == 0) *s_out = s;
-  for (int k = t; k < K; k += C::CT) {
-    int v = 0;
-    if (m != 0.0f) {
-      v = __float2int_rn(__fdiv_rn(x[k], s));
-      v = v > 127 ? 127 : (v < -127 ? -127 : v);
-    }
-    q[k] = (int8_t)v;
-  }
+  for (int k = t; k < K; k += C::CT) q[k] = (int8_t)quant_byte(__ldcg(x + k), s, nz);
   consumer_sync<C>();  // red[] reuse
+}
+
+// Register-resident vectors of the first phase: up to 4 * kQPer * CT values (at least 12,288),
+// thread t holding the float4 groups at 4t + 4 CT i.
+template <class C>
+struct QRegs {
+  static constexpr int kPer = (12288 + 4 * C::CT - 1) / (4 * C::CT);
+  float4 v[kPer];
+};
+template <class C>
+__device__ __forceinline__ bool qregs_fit(const QuantJob& j) {
+  return j.B == 1 && j.K <= 4 * QRegs<C>::kPer * C::CT &&
+         ((reinterpret_cast<uintptr_t>(j.x) & 15) | (reinterpret_cast<uintptr_t>(j.q) & 3) | (j.K & 3)) == 0;
+}
+template <class C>
+__device__ __forceinline__ void qregs_load(const QuantJob& j, QRegs<C>& r) {
+#pragma unroll
+  for (int i = 0; i < QRegs<C>::kPer; ++i) {
+    const int k = 4 * threadIdx.x + 4 * C::CT * i;
+    r.v[i] = k < j.K ? __ldcg(reinterpret_cast<const float4*>(j.x + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+// The scale and codes of one register-resident vector; red2 holds CW floats and is reused two
+// vectors later, so one consumer barrier per vector suffices.
+template <class C>
+__device__ __forceinline__ void qregs_quantize(const QuantJob& j, const QRegs<C>& r, float* red2) {
+  const int t = threadIdx.x;
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < QRegs<C>::kPer; ++i)
+    m = fmaxf(fmaxf(m, fmaxf(fabsf(r.v[i].x), fabsf(r.v[i].y))), fmaxf(fabsf(r.v[i].z), fabsf(r.v[i].w)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((t & 31) == 0) red2[t >> 5] = m;
+  consumer_sync<C>();
+  m = red2[0];
+#pragma unroll
+  for (int i = 1; i < C::CW; ++i) m = fmaxf(m, red2[i]);
+  const bool nz = m != 0.0f;
+  const float s = nz ? __fdiv_rn(m, 127.0f) : 0.0f;
+  if (t == 0) *j.s = s;
+#pragma unroll
+  for (int i = 0; i < QRegs<C>::kPer; ++i) {
+    const int k = 4 * t + 4 * C::CT * i;
+    if (k < j.K) *reinterpret_cast<uint32_t*>(j.q + k) = quant4(r.v[i], s, nz);
+  }
+}
+
+// The step's first phase: this CTA's quantization jobs j = blockIdx.x + r * gridDim.x (a job
+// with B = 0 ends the list). Software-pipelined over two register sets: while one vector is
+// reduced and converted, the next one's values are on their way into the other set and the
+// descriptor after it is being read; vectors that do not fit the registers take the two-pass
+// path.
+template <class C>
+__device__ void quantize_phase(const PersistParams& P, float* red) {
+  auto job = [&](int j) {
+    QuantJob q{nullptr, nullptr, nullptr, 0, 0};
+    if (j < P.n_qjobs) q = P.qjobs[j];
+    return q;
+  };
+  const int g = gridDim.x;
+  int j = blockIdx.x, par = 0;
+  QuantJob cur = job(j), nxt = job(j + g);
+  QRegs<C> a, b;
+  if (qregs_fit<C>(cur)) qregs_load<C>(cur, a);
+  // quantizes cur (its values in `mine` when they fit) and starts nxt's loads into `other`
+  auto step = [&](QRegs<C>& mine, QRegs<C>& other) {
+    const QuantJob after = job(j + 2 * g);
+    if (qregs_fit<C>(cur)) {
+      if (qregs_fit<C>(nxt)) qregs_load<C>(nxt, other);
+      qregs_quantize<C>(cur, mine, red + par * C::CW);
+      par ^= 1;
+    } else {
+      consumer_sync<C>();  // red[] may still be read for the previous vector
+      for (int v = 0; v < cur.B; ++v)
+        quantize_consumers<C>(cur.x + (int64_t)v * cur.K, cur.K, cur.q + (int64_t)v * cur.K, cur.s + v, red);
+      if (qregs_fit<C>(nxt)) qregs_load<C>(nxt, other);
+    }
+    cur = nxt;
+    nxt = after;
+    j += g;
+  };
+  while (cur.B > 0) {
+    step(a, b);
+    if (cur.B == 0) break;
+    step(b, a);
+  }
+  consumer_sync<C>();
 }
 
 // Input-table row of token b, dequantized into embed_x[b] by the consumer threads:
@@ -840,12 +925,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     }
   }
 
-  if (P.n_qjobs > 0) {  // quantize the step's fp32 inputs, then wait for every CTA
-    for (int j = blockIdx.x; j < P.n_qjobs; j += gridDim.x) {
-      const QuantJob qj = P.qjobs[j];
-      for (int b = 0; b < qj.B; ++b)
-        quantize_consumers<C>(qj.x + (int64_t)b * qj.K, qj.K, qj.q + (int64_t)b * qj.K, qj.s + b, red);
-    }
+  if (!C::CHAINED && P.n_qjobs > 0) {  // quantize the step's fp32 inputs, then wait for every CTA
+    if constexpr (!C::CHAINED) quantize_phase<C>(P, red);
     ++barriers;
     grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
     stamp(P, (int)barriers, 2);

@@ -155,6 +155,31 @@ nt_status issue_launches(nt_decode_plan* p, cudaStream_t st) {
   return NT_OK;
 }
 
+// Quantization jobs of the persistent launcher: CTA c runs entries c, c + grid, c + 2 grid, ...
+// before the step's first grid barrier, so that phase ends with its most loaded CTA. Each
+// vector becomes a job of its own, the jobs go largest first to the least loaded CTA, and
+// empty jobs (B = 0) fill the rounds a CTA has no work in; no CTA then holds more than one
+// 12,288-wide vector, or two 4,096-wide ones, of the 8B-shaped batch-1 step.
+std::vector<QuantJob> place_quant_jobs(const std::vector<QuantJob>& jobs, int grid) {
+  std::vector<QuantJob> one;
+  for (const QuantJob& j : jobs)
+    for (int b = 0; b < j.B; ++b) one.push_back(QuantJob{j.x + (int64_t)b * j.K, j.q + (int64_t)b * j.K, j.s + b, j.K, 1});
+  std::stable_sort(one.begin(), one.end(), [](const QuantJob& a, const QuantJob& b) { return a.K > b.K; });
+  std::vector<std::vector<QuantJob>> per(grid);
+  std::vector<int64_t> load(grid, 0);
+  for (const QuantJob& j : one) {
+    const int c = (int)(std::min_element(load.begin(), load.end()) - load.begin());
+    per[c].push_back(j);
+    load[c] += j.K + 1024;  // + the two consumer barriers and the scale, as elements
+  }
+  size_t rounds = 0;
+  for (const auto& v : per) rounds = std::max(rounds, v.size());
+  std::vector<QuantJob> out(rounds * grid, QuantJob{nullptr, nullptr, nullptr, 0, 0});
+  for (int c = 0; c < grid; ++c)
+    for (size_t r = 0; r < per[c].size(); ++r) out[r * grid + c] = per[c][r];
+  return out;
+}
+
 void free_plan(nt_decode_plan* p) {
   if (!p) return;
   if (p->exec) cudaGraphExecDestroy(p->exec);
@@ -480,6 +505,10 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** out) {
     if ((e = cudaMalloc(&p->d_mma, sizeof(MmaMat) * mm.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
     if ((e = cudaMemcpy(p->d_mma, mm.data(), sizeof(MmaMat) * mm.size(), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e, "cudaMemcpy");
+  }
+  if (!jobs.empty() && p->launcher == NT_LAUNCH_PERSISTENT) {
+    jobs = place_quant_jobs(jobs, p->sm_count);
+    p->n_qjobs = (int)jobs.size();
   }
   if (!jobs.empty()) {
     if ((e = cudaMalloc(&p->d_qjobs, sizeof(QuantJob) * jobs.size())) != cudaSuccess) return cuda_fail(e, "cudaMalloc");

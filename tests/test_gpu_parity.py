@@ -379,6 +379,37 @@ def test_decode_step_batched_wide_stage(launcher, B):
     plan.close()
 
 
+@pytest.mark.parametrize("B", [1, 3])
+def test_decode_step_persistent_quantize_paths(B):
+    # The persistent step's first phase keeps vectors of up to 12,288 values in registers when
+    # they are 16-byte aligned; wider (14,336) or only 4-byte aligned inputs take the two-pass
+    # path. Every other projection's input (and the table's) is offset by one float here, and
+    # the codes and scales must be the oracle's either way.
+    shapes = dict(SMALL, down=(512, 14336), gate=(14336, 512), up=(14336, 512))
+    projs = wl.decoder_projections(1, shapes, B=B, seed=19, workload=19)
+    head = wl.head(V=1999, K=512, B=B, seed=19, workload=19)
+    dp, hd = plan_inputs(projs, head, B=B)
+
+    def offset(x):
+        buf = torch.empty(x.numel() + 1, dtype=torch.float32, device=DEV)
+        v = buf[1:].view(x.shape)
+        v.copy_(x)
+        assert v.data_ptr() % 16 == 4
+        return v
+
+    for i, d in enumerate(dp):
+        if i % 2 == 0:
+            d["x"] = offset(d["x"])
+    hd["x"] = offset(hd["x"])
+    plan = nt.DecodePlan(1, B, dp, hd, nt.NT_STEP_INDEPENDENT, nt.NT_LAUNCH_PERSISTENT)
+    for _ in range(2):
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, head, dp, hd, B=B)
+    plan.close()
+
+
 def test_decode_step_prequantized_inputs():
     projs = wl.decoder_projections(1, SMALL, seed=6, workload=12)
     dp, _ = plan_inputs(projs, None, quantize_in_step=False)
