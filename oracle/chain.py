@@ -1,9 +1,9 @@
 """Chained decode step of the oracle -- TEST INFRASTRUCTURE ONLY (same rules as the rest of
 ``oracle/``: only tests, the smoke check and the benchmark's CPU legs may use it).
 
-"The Neutrino Engine", § "A 104 microsecond floor inside a 694 microsecond step": every
-decoder layer applies its attention and feed-forward matrices to the current activations,
-and the engine reads no tensor twice for one token. In a chained step each stage therefore
+"The Neutrino Engine", § "A 104 microsecond floor inside a 694 microsecond step": each of
+the decoder's layers multiplies the activations it is handed by its attention and
+feed-forward weights, and no tensor is read twice per token. In a chained step each stage therefore
 quantizes what the previous stage produced instead of an input supplied from outside.
 
 The pages do not spell the layer out; the reading taken here (every step one fp32 operation
