@@ -409,7 +409,7 @@ __device__ void quantize_consumers(const float* x, int K, int8_t* q, float* s_ou
   consumer_sync<C>();  // red[] reuse
 }
 
-// Register-resident vectors of the first phase: up to 4 * kQPer * CT values (at least 12,288),
+// Register-resident vectors of the first phase: up to 4 * kPer * CT values (at least 12,288),
 // thread t holding the float4 groups at 4t + 4 CT i.
 template <class C>
 struct QRegs {
@@ -456,43 +456,26 @@ __device__ __forceinline__ void qregs_quantize(const QuantJob& j, const QRegs<C>
 }
 
 // The step's first phase: this CTA's quantization jobs j = blockIdx.x + r * gridDim.x (a job
-// with B = 0 ends the list). Software-pipelined over two register sets: while one vector is
-// reduced and converted, the next one's values are on their way into the other set and the
-// descriptor after it is being read; vectors that do not fit the registers take the two-pass
-// path.
+// with B = 0 ends the list), one vector each; vectors that do not fit the registers take the
+// two-pass path. (Loading the next vector into a second register set while one is converted
+// shortened this phase by ~1 us but made the rest of the kernel's code slower in ordered
+// steps, ~28 us per token.)
 template <class C>
 __device__ void quantize_phase(const PersistParams& P, float* red) {
-  auto job = [&](int j) {
-    QuantJob q{nullptr, nullptr, nullptr, 0, 0};
-    if (j < P.n_qjobs) q = P.qjobs[j];
-    return q;
-  };
-  const int g = gridDim.x;
-  int j = blockIdx.x, par = 0;
-  QuantJob cur = job(j), nxt = job(j + g);
-  QRegs<C> a, b;
-  if (qregs_fit<C>(cur)) qregs_load<C>(cur, a);
-  // quantizes cur (its values in `mine` when they fit) and starts nxt's loads into `other`
-  auto step = [&](QRegs<C>& mine, QRegs<C>& other) {
-    const QuantJob after = job(j + 2 * g);
+  int par = 0;
+  for (int j = blockIdx.x; j < P.n_qjobs; j += gridDim.x) {
+    const QuantJob cur = P.qjobs[j];
+    if (cur.B == 0) break;
     if (qregs_fit<C>(cur)) {
-      if (qregs_fit<C>(nxt)) qregs_load<C>(nxt, other);
-      qregs_quantize<C>(cur, mine, red + par * C::CW);
+      QRegs<C> a;
+      qregs_load<C>(cur, a);
+      qregs_quantize<C>(cur, a, red + par * C::CW);
       par ^= 1;
     } else {
       consumer_sync<C>();  // red[] may still be read for the previous vector
       for (int v = 0; v < cur.B; ++v)
         quantize_consumers<C>(cur.x + (int64_t)v * cur.K, cur.K, cur.q + (int64_t)v * cur.K, cur.s + v, red);
-      if (qregs_fit<C>(nxt)) qregs_load<C>(nxt, other);
     }
-    cur = nxt;
-    nxt = after;
-    j += g;
-  };
-  while (cur.B > 0) {
-    step(a, b);
-    if (cur.B == 0) break;
-    step(b, a);
   }
   consumer_sync<C>();
 }
