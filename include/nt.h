@@ -372,7 +372,11 @@ enum nt_launcher {
   NT_LAUNCH_STREAM = 2      /* the same launches issued one by one (the launch-gap case) */
 };
 
-/* One projection. All pointers device; the weights in NT_LAYOUT_TILED. */
+/* One projection. All pointers device; the weights in NT_LAYOUT_TILED. The fp32 inputs x
+ * (and head_x) of an NT_STEP_INDEPENDENT or NT_STEP_ORDERED plan may also point into pinned
+ * host memory that the device can address (page-locked, mapped; on this platform every pinned
+ * allocation is): the step's first phase then reads them over the host link each step, with
+ * no separate copy. */
 typedef struct nt_proj {
   int N, K;
   const void* w;     /* nt_repack_ternary output for an N x K matrix */

@@ -410,6 +410,25 @@ def test_decode_step_persistent_quantize_paths(B):
     plan.close()
 
 
+@pytest.mark.parametrize("launcher", [nt.NT_LAUNCH_PERSISTENT, nt.NT_LAUNCH_GRAPH])
+def test_decode_step_inputs_in_pinned_host_memory(launcher):
+    # The step reads its fp32 inputs straight from pinned host memory (no copy call): codes,
+    # scales, outputs and the arg-max are the oracle's, over repeated steps.
+    projs = wl.decoder_projections(1, SMALL, B=2, seed=21, workload=21)
+    head = wl.head(V=2003, K=512, B=2, seed=21, workload=21)
+    dp, hd = plan_inputs(projs, head, B=2)
+    for d in dp:
+        d["x"] = d["x"].cpu().pin_memory()
+    hd["x"] = hd["x"].cpu().pin_memory()
+    plan = nt.DecodePlan(1, 2, dp, hd, nt.NT_STEP_INDEPENDENT, launcher)
+    for _ in range(3):
+        plan.nt_decode_step()
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    _check_step(projs, head, dp, hd, B=2)
+    plan.close()
+
+
 def test_decode_step_prequantized_inputs():
     projs = wl.decoder_projections(1, SMALL, seed=6, workload=12)
     dp, _ = plan_inputs(projs, None, quantize_in_step=False)
