@@ -260,16 +260,22 @@ __device__ __forceinline__ void tc8_cta(const CUtensorMap* tmW_, const CUtensorM
       bar_arrive(empty0 + 8 * s);  // release: the reads above are ordered before it
       if (i >= kTc8ABufs && !bar_wait(aempty0 + 8 * b, ((i / kTc8ABufs) - 1) & 1u, fail, p.timeout_ns)) break;
       // e4m3 bytes of the block's trits 16 g .. 16 g + 15 into columns 4 g .. 4 g + 3 of the A buffer
+      // two words (8 columns) per store: fewer store instructions than one per word, while
+      // wider stores (16 or 32 columns) ran slower (they keep more registers live)
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint32_t hi = w[g] >> 16;
-        const uint32_t r0 = prmt(kE4PoolA_lo, kE4PoolA_hi, w[g]);
-        const uint32_t r1 = prmt(kE4PoolB_lo, kE4PoolB_hi, w[g]) & 0xB8B8B8B8u;
-        const uint32_t r2 = prmt(kE4PoolA_lo, kE4PoolA_hi, hi);
-        const uint32_t r3 = prmt(kE4PoolB_lo, kE4PoolB_hi, hi) & 0xB8B8B8B8u;
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+      for (int g = 0; g < 8; g += 2) {
+        uint32_t r[8];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t ww = w[g + j], hi = ww >> 16;
+          r[4 * j + 0] = prmt(kE4PoolA_lo, kE4PoolA_hi, ww);
+          r[4 * j + 1] = prmt(kE4PoolB_lo, kE4PoolB_hi, ww) & 0xB8B8B8B8u;
+          r[4 * j + 2] = prmt(kE4PoolA_lo, kE4PoolA_hi, hi);
+          r[4 * j + 3] = prmt(kE4PoolB_lo, kE4PoolB_hi, hi) & 0xB8B8B8B8u;
+        }
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
                          tl + 32u + 32u * (uint32_t)b + 4u * (uint32_t)g),
-                     "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                     "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                      : "memory");
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
