@@ -460,7 +460,12 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** plan);
 
 /* Runs one decode step on `stream`. Allocates nothing. Steps of one plan must not overlap
  * on the device (issue them on one stream). NT_LAUNCH_PERSISTENT needs every CTA of its
- * grid resident at once and returns NT_ERR_CUDA if the device cannot provide that. */
+ * grid resident at once and returns NT_ERR_CUDA if the device cannot provide that.
+ * A persistent step that is one launch (every plan but a chained one with attention) takes
+ * the same launch parameters on every call -- its grid-barrier counter is reset on the device
+ * by the CTA that finishes last -- so it can be recorded into a CUDA graph by stream capture
+ * and replayed; inputs written in place between replays are read by the next replay. A
+ * trace or capture buffer set after recording is not seen by the recorded launch. */
 nt_status nt_decode_step(nt_decode_plan* plan, void* stream);
 
 /* After the caller has synchronized with the last step: NT_OK, or NT_ERR_TIMEOUT when a

@@ -88,6 +88,9 @@ struct PersistParams {
   int nslots;    // ring slots per consumer warp (<= kMaxSlots)
   int act_k;     // bytes per activation vector in shared memory
   uint32_t barrier_base;    // grid-barrier arrivals of all earlier launches on this plan (mod 2^32)
+  int reset_barriers;       // single-launch steps: the barrier targets start at 0 and the CTA that
+                            // finishes last zeroes the arrival counter, so every launch of the step
+                            // takes the same parameters (the launch can be captured in a CUDA graph)
   uint32_t barrier_extra;  // added to every grid barrier's target (timeout-path tests)
   int no_copies;           // timeout-path tests: the producer issues nothing, so consumers time out
   uint64_t timeout_ns;
@@ -983,6 +986,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   if (prefetched) cp_async_wait_all();
   consumer_sync<C>();
   stamp(P, 0, 1);
+  if (P.reset_barriers && !P.has_head && threadIdx.x == 0) {
+    // this CTA is past its last grid barrier; the last one to get here (all others are past
+    // theirs too) zeroes the arrival counter for the next launch
+    __threadfence();
+    if (atomicAdd(&P.ctrl->exit_done, 1u) == gridDim.x - 1) {
+      P.ctrl->arrive = 0u;
+      P.ctrl->exit_done = 0u;
+    }
+  }
 
   if (P.has_head) {  // CTA best per vector, then the last CTA to finish reduces all CTAs
     volatile int& s_last = *reinterpret_cast<volatile int*>(smem + L.abort_flag + 4);
@@ -1031,6 +1043,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       if (threadIdx.x == 0) {
         P.ctrl->head_done = 0u;
         if (P.head_next) *P.head_next = 0u;  // every producer's last grab came before its CTA arrived
+        if (P.reset_barriers) P.ctrl->arrive = 0u;  // every CTA arrived after its last grid barrier
       }
       if (P.verify_emit && !failed) {  // accept the longest agreeing draft prefix on the device
         consumer_sync<C>();
@@ -1304,16 +1317,19 @@ nt_status persist_launch(nt_decode_plan* p, cudaStream_t st) {
   P.head_src = p->head_src;
   int threads = 0;
   const void* kern = kernel_for(p->B, p->mode == NT_STEP_CHAINED, &threads);
+  // a single launch per step resets the barrier counter itself (its parameters are the same
+  // on every call); segmented steps count barriers across their launches on the host
+  P.reset_barriers = p->seg_barriers.empty() ? 1 : 0;
   auto launch = [&](int n_barriers) -> nt_status {
     P.n_barriers = n_barriers;
-    P.barrier_base = p->barrier_count * (uint32_t)p->grid;
+    P.barrier_base = P.reset_barriers ? 0u : p->barrier_count * (uint32_t)p->grid;
     void* args[] = {&P};
     const cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p->grid), dim3(threads), args, p->smem_bytes, st);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return set_error(NT_ERR_CUDA, std::string("persistent launch: ") + cudaGetErrorString(e));
     }
-    p->barrier_count += (uint32_t)n_barriers;
+    if (!P.reset_barriers) p->barrier_count += (uint32_t)n_barriers;
     return NT_OK;
   };
   if (p->seg_barriers.empty()) {

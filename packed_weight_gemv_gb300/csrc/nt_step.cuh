@@ -26,7 +26,8 @@ struct StepCtrl {
   unsigned int arrive;     // grid-barrier arrivals (wraps; compared modulo 2^32)
   unsigned int head_done;  // CTAs finished with the output projection's arg-max
   unsigned int head_next;  // output-table rows handed out so far (dynamic rows; the last CTA resets it)
-  unsigned int pad_[3];
+  unsigned int exit_done;  // CTAs past their last grid barrier (single-launch plans without an output table)
+  unsigned int pad_[2];
 };
 
 // One contiguous run of work for one CTA of the persistent kernel. kItemHeadDyn: the output

@@ -429,6 +429,50 @@ def test_decode_step_inputs_in_pinned_host_memory(launcher):
     plan.close()
 
 
+@pytest.mark.parametrize("mode", [nt.NT_STEP_INDEPENDENT, nt.NT_STEP_ORDERED, nt.NT_STEP_CHAINED])
+@pytest.mark.parametrize("with_head", [True, False])
+def test_persistent_step_replayed_from_cuda_graph(mode, with_head):
+    # One persistent step recorded into a CUDA graph by stream capture, replayed with new
+    # inputs written in place before each replay: every replay matches the oracle (the grid
+    # barriers' counter is reset on the device, so the recorded parameters stay valid).
+    L = 2
+    projs = wl.decoder_projections(L, SMALL, seed=22, workload=22)
+    head = wl.head(V=3001, K=512, seed=22, workload=22) if with_head else None
+    dp, hd = plan_inputs(projs, head)
+    plan = nt.DecodePlan(L, 1, dp, hd, mode, nt.NT_LAUNCH_PERSISTENT)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=side):
+        plan.nt_decode_step()
+    x0 = [p.x.copy() for p in projs]
+    hx0 = head.x.copy() if with_head else None
+    for rep in range(3):
+        scale = np.float32(1.0 + 0.37 * rep)
+        for p, d, x in zip(projs, dp, x0):
+            p.x = (x * scale).astype(np.float32)
+            d["x"].copy_(dev(p.x[:1]))
+        if with_head:
+            head.x = (hx0 * scale).astype(np.float32)
+            hd["x"].copy_(dev(head.x[:1]))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert plan.nt_decode_step_status() == nt.NT_OK
+        if mode != nt.NT_STEP_CHAINED:
+            _check_step(projs, head, dp, hd)
+        else:
+            layers = [[(p.w_plain, p.s_w, p.N, p.K) for p in projs[7 * l:7 * l + 7]] for l in range(L)]
+            want = oracle.decode_chained(layers, projs[0].x[:1],
+                                         (head.T, head.s_T, head.V, head.K) if with_head else None)
+            for i, (p, d) in enumerate(zip(projs, dp)):
+                assert np.array_equal(host(d["q"]), want["q"][i]), p.name
+                assert_close(host(d["y"]), want["y"][i], p.name)
+            if with_head:
+                assert np.array_equal(host(hd["argmax"]), want["argmax"])
+    del graph
+    plan.close()
+
+
 def test_decode_step_prequantized_inputs():
     projs = wl.decoder_projections(1, SMALL, seed=6, workload=12)
     dp, _ = plan_inputs(projs, None, quantize_in_step=False)
