@@ -1061,9 +1061,15 @@ struct Unitset {
 };
 
 // Splits one stage's units into `grid` contiguous byte ranges and appends each CTA's items
-// for the pass starting at vector b0.
+// for the pass starting at vector b0. With `one_item` (stages between grid barriers) every
+// CTA gets units of one set only: the sets get whole CTAs in proportion to their bytes
+// (largest remainder, at least one each while there are CTAs left) and split their units
+// evenly among them (so CTA 0, which records a chained stage's codes, always has an item of
+// the stage). A CTA whose range straddled two sets would run them one after the other
+// -- its warps meet at the switch, since the second set's activations replace the first's --
+// and so hold the whole stage back by a tile's latency.
 void partition_stage(const std::vector<Unitset>& sets, int grid, int b0, bool barrier_before,
-                     std::vector<std::vector<WorkItem>>& per_cta) {
+                     std::vector<std::vector<WorkItem>>& per_cta, bool one_item = false) {
   int64_t total = 0;
   for (const Unitset& s : sets) total += s.units * s.unit_bytes;
   std::vector<bool> flagged(grid, false);
@@ -1072,6 +1078,31 @@ void partition_stage(const std::vector<Unitset>& sets, int grid, int b0, bool ba
     if (barrier_before && !flagged[c]) { x.flags |= kFlagStage; flagged[c] = true; }
     per_cta[c].push_back(x);
   };
+  const int ns = (int)sets.size();
+  if (one_item && ns > 1 && ns <= grid && total > 0) {
+    std::vector<int64_t> n(ns);
+    std::vector<std::pair<int64_t, int>> rem;  // (remainder of share * total, set)
+    int64_t given = 0;
+    for (int i = 0; i < ns; ++i) {
+      const int64_t b = sets[i].units * sets[i].unit_bytes;
+      n[i] = std::max<int64_t>(1, b * grid / total);
+      rem.push_back({b * grid - (b * grid / total) * total, i});
+      given += n[i];
+    }
+    std::sort(rem.begin(), rem.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+    for (size_t r = 0; given < grid; r = (r + 1) % rem.size(), ++given) ++n[rem[r].second];
+    for (int i = ns - 1; given > grid; i = (i + ns - 1) % ns)  // the max(1, .) above overshot
+      if (n[i] > 1) { --n[i]; --given; }
+    int c0 = 0;
+    for (int i = 0; i < ns; ++i) {
+      const Unitset& st = sets[i];
+      for (int64_t j = 0; j < n[i]; ++j) {  // rounded up: the set's first CTA always gets units
+        const int64_t u = (st.units * j + n[i] - 1) / n[i], v = (st.units * (j + 1) + n[i] - 1) / n[i];
+        if (u < v) push(c0 + (int)j, WorkItem{st.kind, st.mat, 0, b0, u, v});
+      }
+      c0 += (int)n[i];
+    }
+  } else {
   int64_t start = 0;  // byte offset of the current unit set within the stage
   for (const Unitset& s : sets) {
     int64_t u = 0;
@@ -1085,6 +1116,7 @@ void partition_stage(const std::vector<Unitset>& sets, int grid, int b0, bool ba
       u = v;
     }
     start += s.units * s.unit_bytes;
+  }
   }
   if (barrier_before)  // every CTA takes part in the barrier, with or without work
     for (int c = 0; c < grid; ++c)
@@ -1208,7 +1240,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
     const int L = p->n_layers;
     auto stage_into = [&](std::vector<std::vector<WorkItem>>& pc, bool& first, int& nbar,
                           const std::vector<Unitset>& sets) {
-      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) partition_stage(sets, grid, b0, !first && b0 == 0, pc);
+      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) partition_stage(sets, grid, b0, !first && b0 == 0, pc, true);
       nbar += first ? 0 : 1;
       first = false;
     };
@@ -1236,7 +1268,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
     bool first = true;
     auto stage = [&](const std::vector<Unitset>& sets) {
       for (int b0 = 0; b0 < p->B; b0 += p->chunk_b)
-        partition_stage(sets, grid, b0, !first && b0 == 0, per_cta);
+        partition_stage(sets, grid, b0, !first && b0 == 0, per_cta, true);
       barriers += first ? 0 : 1;
       first = false;
     };
