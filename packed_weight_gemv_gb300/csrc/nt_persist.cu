@@ -735,8 +735,19 @@ __device__ __forceinline__ void row_piece(const uint8_t* sb, const uint8_t* ab, 
 
 // One tile (4 rows) of a tiled ternary matrix against NB activation vectors. The row scale
 // is loaded before the first chunk so its latency hides behind the chunk work.
-template <int NB, bool CH>
-__device__ __forceinline__ void consume_tile(const PersistParams& P, const MatDesc& m, const float (&sx)[NB], int b0,
+// The fields of a matrix descriptor a tile's consumer needs. Chained steps load them before
+// the stage's grid barrier, so the load's latency overlaps the wait (9 us per token); the
+// other instances load the descriptor after it (doing the same there compiled into slower
+// stage code for ordered steps).
+struct TileDesc {
+  const float* s_w;
+  float* y;
+  const float* res_in;
+  float* res_out;
+  int N, K;
+};
+template <int NB, bool CH, class M>
+__device__ __forceinline__ void consume_tile(const PersistParams& P, const M& m, const float (&sx)[NB], int b0,
                              int64_t tile, const uint8_t* act, Ring& ring, int lane, volatile int* s_abort) {
   const int pieces = (int)(padded_k(m.K) / 512);
   const int64_t n = tile * 4 + (lane >> 3);
@@ -816,7 +827,7 @@ __device__ __forceinline__ void consume_head_row(const PersistParams& P, const f
 template <class C, int NB>
 __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkItem& it, uint32_t seq, const uint8_t* act,
                              Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort,
-                             const float* s_chain, const int* slot_row) {
+                             const float* s_chain, const int* slot_row, const TileDesc& pre) {
   float sx[NB];
   const float* sxp = it.kind == kItemTernary ? P.mats[it.mat].s_x : P.head_sx;
 #pragma unroll
@@ -827,10 +838,16 @@ __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkI
   const int64_t first = first_unit<C>(it, seq, cw);
   // The abort flag is read by lane 0 and broadcast, so the whole warp takes one branch.
   if (it.kind == kItemTernary) {
-    const MatDesc m = P.mats[it.mat];
-    for (int64_t u = first; u < it.end; u += C::CW)
-      if (!__shfl_sync(0xffffffffu, *s_abort, 0))
-        consume_tile<NB, C::CHAINED>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
+    if constexpr (C::CHAINED) {
+      for (int64_t u = first; u < it.end; u += C::CW)
+        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+          consume_tile<NB, C::CHAINED>(P, pre, sx, it.b0, u, act, ring, lane, s_abort);
+    } else {
+      const MatDesc m = P.mats[it.mat];
+      for (int64_t u = first; u < it.end; u += C::CW)
+        if (!__shfl_sync(0xffffffffu, *s_abort, 0))
+          consume_tile<NB, C::CHAINED>(P, m, sx, it.b0, u, act, ring, lane, s_abort);
+    }
   } else if (it.kind == kItemHeadDyn) {
     // rows in the order the producer lane handed them out; the slot of a row's first chunk
     // names it, and a slot naming row -1 ends the stream
@@ -926,6 +943,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   for (int i = 0; i < n_items; ++i) {
     const WorkItem it = get_item(P, i);
     const bool staged = (it.flags & kFlagStage) != 0;
+    TileDesc pre{};
+    if constexpr (C::CHAINED) {
+      if (it.kind == kItemTernary) {
+        const MatDesc* md = P.mats + it.mat;
+        pre = TileDesc{md->s_w, md->y, md->res_in, md->res_out, md->N, md->K};
+      }
+    }
     if (staged) {
       ++barriers;
       grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
@@ -971,13 +995,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       abuf = ab;
     }
     if constexpr (C::NBMAX == 1) {
-      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row);
+      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre);
     } else {
       switch (nb) {
-        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
-        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
-        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
-        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row); break;
+        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
+        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
+        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
+        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
       }
     }
     seq += (uint32_t)(it.end - it.begin);
