@@ -950,6 +950,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
         pre = TileDesc{md->s_w, md->y, md->res_in, md->res_out, md->N, md->K};
       }
     }
+    // supplied inputs: where the next item's activations come from (its work item and matrix
+    // descriptor, two dependent loads), read before this item's barrier so that the prefetch
+    // below is issued as soon as the item starts (ordered steps 847 -> 825 us per token)
+    int K2 = 0, nb2 = 0;
+    const int8_t* q2 = nullptr;
+    if constexpr (!C::CHAINED) {
+      if (i + 1 < n_items) q2 = item_act(P, get_item(P, i + 1), K2, nb2);
+    }
     if (staged) {
       ++barriers;
       grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
@@ -986,9 +994,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       if (staged) stamp(P, (int)barriers, 2);
       prefetched = false;
       if (i + 1 < n_items) {  // supplied inputs were quantized before any stage: prefetch across barriers too
-        const WorkItem nx = get_item(P, i + 1);
-        int K2, nb2;
-        const int8_t* q2 = item_act(P, nx, K2, nb2);
         load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
         prefetched = true;
       }
