@@ -827,12 +827,13 @@ __device__ __forceinline__ void consume_head_row(const PersistParams& P, const f
 template <class C, int NB>
 __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkItem& it, uint32_t seq, const uint8_t* act,
                              Ring& ring, HeadPartial* wbest, int cw, int lane, volatile int* s_abort,
-                             const float* s_chain, const int* slot_row, const TileDesc& pre) {
+                             const float* s_chain, const int* slot_row, const TileDesc& pre, float sx_pre) {
   float sx[NB];
   const float* sxp = it.kind == kItemTernary ? P.mats[it.mat].s_x : P.head_sx;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     if constexpr (C::CHAINED) sx[b] = s_chain[b];
+    else if (C::NBMAX == 1 && it.kind == kItemTernary) sx[b] = sx_pre;
     else sx[b] = __ldcg(sxp + it.b0 + b);
   }
   const int64_t first = first_unit<C>(it, seq, cw);
@@ -952,11 +953,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     }
     // supplied inputs: where the next item's activations come from (its work item and matrix
     // descriptor, two dependent loads), read before this item's barrier so that the prefetch
-    // below is issued as soon as the item starts (ordered steps 847 -> 825 us per token)
+    // below is issued as soon as the item starts (ordered steps 847 -> 825 us per token; the
+    // activation scale read early as well: 829 -> 794)
     int K2 = 0, nb2 = 0;
     const int8_t* q2 = nullptr;
-    if constexpr (!C::CHAINED) {
+    float sx_pre = 0.0f;  // batch 1: this item's activation scale, read before the barrier too
+    if constexpr (!C::CHAINED && C::NBMAX == 1) {  // (the batched instance ran slower with it)
       if (i + 1 < n_items) q2 = item_act(P, get_item(P, i + 1), K2, nb2);
+      if (it.kind == kItemTernary) sx_pre = __ldcg(P.mats[it.mat].s_x + it.b0);
     }
     if (staged) {
       ++barriers;
@@ -994,19 +998,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       if (staged) stamp(P, (int)barriers, 2);
       prefetched = false;
       if (i + 1 < n_items) {  // supplied inputs were quantized before any stage: prefetch across barriers too
+        if constexpr (C::NBMAX != 1) q2 = item_act(P, get_item(P, i + 1), K2, nb2);
         load_act<C>(act + (buf ^ 1) * act_buf, q2, K2, nb2, P.act_k, true);
         prefetched = true;
       }
       abuf = ab;
     }
     if constexpr (C::NBMAX == 1) {
-      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre);
+      consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre, sx_pre);
     } else {
       switch (nb) {
-        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
-        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
-        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
-        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre); break;
+        case 1: consume_item<C, 1>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre, sx_pre); break;
+        case 2: consume_item<C, 2>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre, sx_pre); break;
+        case 3: consume_item<C, 3>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre, sx_pre); break;
+        default: consume_item<C, 4>(P, it, seq, abuf, rg, wbest, cw, lane, s_abort, sc, slot_row, pre, sx_pre); break;
       }
     }
     seq += (uint32_t)(it.end - it.begin);
