@@ -116,7 +116,7 @@ __device__ __forceinline__ void stamp(const PersistParams& P, int b, int i) {
 }
 
 struct SmemLayout {
-  int ring, act, bars, hbest, red, abort_flag, chain_s, slot_row, total;
+  int ring, act, bars, hbest, red, abort_flag, chain_s, slot_row, rec_state, total;
 };
 
 template <class C>
@@ -130,7 +130,9 @@ __host__ __device__ inline SmemLayout smem_layout(int nslots, int chunk_b, int a
   L.abort_flag = L.red + 2 * C::CW * 4 + (C::CHAINED ? 16 : 0);  // chained: the norm factor after the warps' values
   L.chain_s = L.abort_flag + 16;
   L.slot_row = L.chain_s + kStepMaxBatch * 4;   // kItemHeadDyn: the row each ring slot holds
-  L.total = L.slot_row + C::CW * kMaxSlots * 4;
+  // chained: CTA 0's recorded stage input still to be written out (see flush_record)
+  L.rec_state = (L.slot_row + C::CW * kMaxSlots * 4 + 7) & ~7;
+  L.total = L.rec_state + (C::CHAINED ? 32 : 0);
   return L;
 }
 
@@ -867,6 +869,29 @@ __device__ __forceinline__ void consume_item(const PersistParams& P, const WorkI
   }
 }
 
+// Chained steps: CTA 0 writes the codes and scales of a stage input it quantized (still in its
+// activation buffer and s_chain) to the q / s_x of the stage's matrices or of the output
+// projection once its own share of the stage is done, so the writes do not delay the work
+// that every other CTA waits for at the next grid barrier (written in the prologue, they made
+// CTA 0 the last to arrive at most barriers: chained batch-1 steps 1,122 -> 1,103 us per token).
+template <class C>
+__device__ void flush_record(const uint8_t* abuf, const float* s_chain, int act_k, int K, int b0, int nb,
+                             const MatDesc* rec, int n_rec, int8_t* hq, float* hs) {
+  for (int b = 0; b < nb; ++b) {
+    for (int k = 4 * (int)threadIdx.x; k < K; k += 4 * C::CT) {
+      const uint32_t c = *reinterpret_cast<const uint32_t*>(abuf + b * act_k + k);
+      const int64_t o = (int64_t)(b0 + b) * K + k;
+      if (hq) *reinterpret_cast<uint32_t*>(hq + o) = c;
+      for (int rr = 0; rr < n_rec; ++rr) *reinterpret_cast<uint32_t*>(const_cast<int8_t*>(rec[rr].q) + o) = c;
+    }
+    if (threadIdx.x == 0) {
+      const float sv = s_chain[b];
+      if (hs) hs[b0 + b] = sv;
+      for (int rr = 0; rr < n_rec; ++rr) const_cast<float*>(rec[rr].s_x)[b0 + b] = sv;
+    }
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_constant__ PersistParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -941,6 +966,23 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
   bool prefetched = false;
   const float* chain_in0 = nullptr;  // chained: the stage input now in act[buf]
   int chain_b0 = -1;
+  // chained, CTA 0: the recorded stage input waiting to be written out, in shared memory
+  // (K, b0, nb, buffer, matrix count, output projection?; then the first matrix; K = 0: none)
+  volatile int* s_rec = reinterpret_cast<volatile int*>(smem + L.rec_state);
+  const MatDesc** s_rec_mats = reinterpret_cast<const MatDesc**>(smem + L.rec_state + 24);
+  if (C::CHAINED && threadIdx.x == 0) s_rec[0] = 0;
+  auto flush = [&]() {
+    if constexpr (C::CHAINED && C::NBMAX == 1) {  // (the batched instance spilled registers with it)
+      if (blockIdx.x == 0 && s_rec[0] > 0) {
+        const bool hd = s_rec[5] != 0;
+        flush_record<C>(act + s_rec[3] * act_buf, s_chain, P.act_k, s_rec[0], s_rec[1], s_rec[2], *s_rec_mats,
+                        s_rec[4], hd ? const_cast<int8_t*>(P.head_q) : nullptr,
+                        hd ? const_cast<float*>(P.head_sx) : nullptr);
+        consumer_sync<C>();  // every thread has read the state before thread 0 clears it
+        if (threadIdx.x == 0) s_rec[0] = 0;
+      }
+    }
+  };
   for (int i = 0; i < n_items; ++i) {
     const WorkItem it = get_item(P, i);
     const bool staged = (it.flags & kFlagStage) != 0;
@@ -963,6 +1005,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
       if (it.kind == kItemTernary) sx_pre = __ldcg(P.mats[it.mat].s_x + it.b0);
     }
     if (staged) {
+      flush();
       ++barriers;
       grid_barrier<C>(P, barrier_base + barriers * gridDim.x, (int)barriers, s_abort);
     }
@@ -973,15 +1016,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     if constexpr (C::CHAINED) {  // the stage's matrices share one input: quantize it once per stage and pass
       const ChainSrc cs = it.kind == kItemTernary ? P.mats[it.mat].src : P.head_src;
       if ((staged || cs.in0 != chain_in0 || it.b0 != chain_b0) && (it.begin < it.end || blockIdx.x == 0)) {
+        flush();  // this prologue replaces s_chain
         buf ^= 1;
         const bool rec = blockIdx.x == 0;
-        if (it.kind == kItemTernary) {
-          const int rf = P.mats[it.mat].rec_first, rn = P.mats[it.mat].rec_count;
-          chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, P.mats + rf, rn,
-                            nullptr, nullptr);
-        } else {
-          chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, nullptr, 0,
-                            const_cast<int8_t*>(P.head_q), const_cast<float*>(P.head_sx));
+        if constexpr (C::NBMAX != 1) {  // the codes go out from the prologue itself
+          if (it.kind == kItemTernary) {
+            const int rf = P.mats[it.mat].rec_first, rn = P.mats[it.mat].rec_count;
+            chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, P.mats + rf, rn,
+                              nullptr, nullptr);
+          } else {
+            chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, nullptr, 0,
+                              const_cast<int8_t*>(P.head_q), const_cast<float*>(P.head_sx));
+          }
+        } else {  // here only the capture buffer (tests); the codes: flush()
+          chain_prologue<C>(cs, it.b0, nb, P.act_k, act + buf * act_buf, s_chain, red, rec, nullptr, 0, nullptr,
+                            nullptr);
+        }
+        if (C::NBMAX == 1 && rec && threadIdx.x == 0) {
+          const bool hd = it.kind != kItemTernary;
+          s_rec[1] = it.b0;
+          s_rec[2] = nb;
+          s_rec[3] = buf;
+          s_rec[4] = hd ? 0 : P.mats[it.mat].rec_count;
+          s_rec[5] = hd ? 1 : 0;
+          *s_rec_mats = hd ? nullptr : P.mats + P.mats[it.mat].rec_first;
+          s_rec[0] = cs.K;
         }
         chain_in0 = cs.in0;
         chain_b0 = it.b0;
@@ -1018,6 +1077,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) persist_kernel(const __grid_con
     if constexpr (!C::CHAINED) buf ^= 1;
   }
   if (prefetched) cp_async_wait_all();
+  flush();
   consumer_sync<C>();
   stamp(P, 0, 1);
   if (P.reset_barriers && !P.has_head && threadIdx.x == 0) {
@@ -1187,7 +1247,10 @@ int head_fixed_rows(int cw, int nslots, int K, int V, int grid) {
   return std::min(fixed, V / std::max(grid, 1));
 }
 
-bool pick_config(int B, int act_k, int* nslots, int* chunk_b, size_t* smem) {
+bool pick_config(int B, int act_k, int* nslots, int* chunk_b, size_t* smem, bool chained = false) {
+  if (chained)
+    return B == 1 ? pick_config_for<Cfg1C>(B, act_k, nslots, chunk_b, smem)
+                  : pick_config_for<CfgBC>(B, act_k, nslots, chunk_b, smem);
   return B == 1 ? pick_config_for<Cfg1>(B, act_k, nslots, chunk_b, smem)
                 : pick_config_for<CfgB>(B, act_k, nslots, chunk_b, smem);
 }
@@ -1230,7 +1293,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
   int kmax = p->has_head ? p->head_K : 16;
   for (const MatDesc& m : p->mats) kmax = std::max<int>(kmax, (int)padded_k(m.K));
   p->act_stride = (int)padded_k(kmax);
-  if (!pick_config(p->B, p->act_stride, &p->nslots, &p->chunk_b, &p->smem_bytes))
+  if (!pick_config(p->B, p->act_stride, &p->nslots, &p->chunk_b, &p->smem_bytes, p->mode == NT_STEP_CHAINED))
     return set_error(NT_ERR_INVALID_ARG, "persistent launcher: K too large for the shared-memory budget");
   NT_TRY(configure_kernel(p->device));
   int per_sm = 0, threads = 0;
