@@ -1217,6 +1217,17 @@ void partition_stage(const std::vector<Unitset>& sets, int grid, int b0, bool ba
       if (!flagged[c]) push(c, WorkItem{sets.front().kind, sets.front().mat, 0, b0, 0, 0});
 }
 
+// Chained stages: CTA 0 quantizes each stage input like every CTA and also writes its codes
+// out, so it takes no units; the stage is split over CTAs 1 .. grid - 1 and CTA 0 gets an
+// empty item of the stage (its prologue runs for CTA 0 with or without units).
+void partition_stage_chained(const std::vector<Unitset>& sets, int grid, int b0, bool barrier_before,
+                             std::vector<std::vector<WorkItem>>& per_cta) {
+  std::vector<std::vector<WorkItem>> rest(grid - 1);
+  partition_stage(sets, grid - 1, b0, barrier_before, rest, true);
+  for (int c = 1; c < grid; ++c) per_cta[c].insert(per_cta[c].end(), rest[c - 1].begin(), rest[c - 1].end());
+  per_cta[0].push_back(WorkItem{sets.front().kind, sets.front().mat, barrier_before ? kFlagStage : 0, b0, 0, 0});
+}
+
 // Ring depth and vectors per pass that fit the shared-memory budget for activations of
 // act_k bytes: 3 slots when possible (deeper ring), else 2; then fewer vectors per pass.
 template <class C>
@@ -1337,7 +1348,7 @@ nt_status persist_prepare(nt_decode_plan* p) {
     const int L = p->n_layers;
     auto stage_into = [&](std::vector<std::vector<WorkItem>>& pc, bool& first, int& nbar,
                           const std::vector<Unitset>& sets) {
-      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) partition_stage(sets, grid, b0, !first && b0 == 0, pc, true);
+      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) partition_stage_chained(sets, grid, b0, !first && b0 == 0, pc);
       nbar += first ? 0 : 1;
       first = false;
     };
@@ -1364,8 +1375,10 @@ nt_status persist_prepare(nt_decode_plan* p) {
   } else {
     bool first = true;
     auto stage = [&](const std::vector<Unitset>& sets) {
-      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b)
-        partition_stage(sets, grid, b0, !first && b0 == 0, per_cta, true);
+      for (int b0 = 0; b0 < p->B; b0 += p->chunk_b) {
+        if (chained) partition_stage_chained(sets, grid, b0, !first && b0 == 0, per_cta);
+        else partition_stage(sets, grid, b0, !first && b0 == 0, per_cta, true);
+      }
       barriers += first ? 0 : 1;
       first = false;
     };
