@@ -465,7 +465,9 @@ nt_status nt_decode_plan_create(const nt_decode_desc* d, nt_decode_plan** plan);
  * the same launch parameters on every call -- its grid-barrier counter is reset on the device
  * by the CTA that finishes last -- so it can be recorded into a CUDA graph by stream capture
  * and replayed; inputs written in place between replays are read by the next replay. A
- * trace or capture buffer set after recording is not seen by the recorded launch. */
+ * trace or capture buffer set after recording is not seen by the recorded launch. A chained
+ * step with attention (several launches that count grid barriers on the host) returns
+ * NT_ERR_UNSUPPORTED when called while its stream is being recorded. */
 nt_status nt_decode_step(nt_decode_plan* plan, void* stream);
 
 /* After the caller has synchronized with the last step: NT_OK, or NT_ERR_TIMEOUT when a

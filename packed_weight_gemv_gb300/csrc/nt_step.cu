@@ -554,6 +554,14 @@ nt_status nt_decode_step(nt_decode_plan* p, void* stream) {
     case NT_LAUNCH_STREAM:
       return issue_launches(p, st);
     default:
+      if (!p->seg_barriers.empty()) {
+        // a segmented step counts its grid barriers on the host across its launches, so a
+        // recorded copy of it would replay stale counts: refuse to be recorded
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        NT_CUDA_TRY(cudaStreamIsCapturing(st, &cs));
+        if (cs != cudaStreamCaptureStatusNone)
+          return set_error(NT_ERR_UNSUPPORTED, "a chained step with attention cannot be recorded into a CUDA graph");
+      }
       return persist_launch(p, st);
   }
 }

@@ -237,3 +237,31 @@ def test_chained_attention_position_advances(launcher):
     with pytest.raises(nt.NtError):
         plan.nt_decode_plan_set_position(ts)
     plan.close()
+
+
+def test_chained_attention_step_refuses_graph_recording():
+    # A persistent chained step with attention runs as several launches whose grid-barrier
+    # counts live on the host; recording it into a CUDA graph is refused, not silently wrong.
+    L, B, Hkv, ts = 1, 1, 2, 64
+    projs = wl.decoder_projections(L, SHAPES, B=B, seed=45, workload=42)
+    dp, _ = plan_inputs(projs, None, B=B)
+    kc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV) for _ in range(L)]
+    vc = [torch.zeros((Hkv, ts, 128), dtype=torch.int16, device=DEV) for _ in range(L)]
+    att = dict(k_cache=kc, v_cache=vc, t_stride=ts, pos=0)
+    plan = nt.DecodePlan(L, B, dp, None, nt.NT_STEP_CHAINED, nt.NT_LAUNCH_PERSISTENT, attention=att)
+    plan.nt_decode_step()
+    torch.cuda.synchronize()
+    graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        try:
+            with pytest.raises(nt.NtError) as e:
+                plan.nt_decode_step()
+        finally:
+            graph.capture_end()
+    assert e.value.status == nt.NT_ERR_UNSUPPORTED
+    plan.nt_decode_step()  # still usable outside a recording
+    torch.cuda.synchronize()
+    assert plan.nt_decode_step_status() == nt.NT_OK
+    del graph
+    plan.close()
