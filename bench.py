@@ -116,20 +116,63 @@ class ClockSampler:
         time.sleep(0.15)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(out: str) -> dict:
+    """Median SM clock, the maximum clock and every throttle reason seen Active, from
+    nvidia-smi's `--format=csv,noheader,nounits` rows of ClockSampler.FIELDS. Rows that do not
+    parse (a truncated last line, "[N/A]") are skipped."""
+    rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            mx = float(r[2])
+        except ValueError:
+            continue
+        for n, v in zip(names, r[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# Replicas: one process per GPU, each decoding its own tokens; the job's time is the slowest
+# rank's. Collectives here only align the start and take the maximum.
+# ---------------------------------------------------------------------------------------
+
+def max_over_ranks(torch, x: float, world: int, device) -> float:
+    """The largest of every rank's x; x itself on one rank. A collective when world > 1: every
+    rank calls it at the same point."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_token(slowest_us: float, tokens_per_rank: int, world: int) -> float:
+    """Whole-job microseconds per token: `world` replicas each decoded tokens_per_rank tokens in
+    a window as long as the slowest rank's time."""
+    return slowest_us / (tokens_per_rank * world)
+
+
+def host_timed_job(torch, step, n: int, world: int, device, sync=None) -> float:
+    """Whole-job microseconds per token of n calls step(0) ... step(n - 1) on every rank, timed
+    on the host: the ranks start together after a barrier, sync() (if given) ends each rank's
+    window, and the job's window is the slowest rank's."""
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(n):
+        step(i)
+    if sync is not None:
+        sync()
+    us = (time.perf_counter() - t0) * 1e6
+    return job_us_per_token(max_over_ranks(torch, us, world, device), n, world)
 
 
 # ---------------------------------------------------------------------------------------
@@ -397,12 +440,9 @@ def run_ours(args, rank, world):
     clk = clocks.stop()
     if plan.nt_decode_step_status() != nt.NT_OK:
         raise RuntimeError("persistent step reported a timeout in the timed region")
-    if world > 1:
-        t = torch.tensor([us], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us = float(t.item())
+    us = max_over_ranks(torch, us, world, dev)
     per_step_us = us / args.steps
-    value = us / (args.steps * world)
+    value = job_us_per_token(us, args.steps, world)
 
     # Serial end to end through the same public call: every step copies its fp32 inputs from
     # pinned host memory, runs, and reads its token back to the host before the next step
@@ -420,10 +460,7 @@ def run_ours(args, rank, world):
     serial_steps = max(1, min(args.steps, 2000))
     for _ in range(3):
         serial_step()
-    t0 = time.perf_counter()
-    for _ in range(serial_steps):
-        serial_step()
-    e2e_serial_us = (time.perf_counter() - t0) * 1e6 / serial_steps
+    e2e_serial_us = host_timed_job(torch, lambda i: serial_step(), serial_steps, world, dev)
     if int(am_host[0]) != int(hd["argmax"].item()):
         raise RuntimeError("serial end-to-end: the token read back differs from the device's")
 
@@ -444,10 +481,7 @@ def run_ours(args, rank, world):
 
     for _ in range(3):
         graph_step()
-    t0 = time.perf_counter()
-    for _ in range(serial_steps):
-        graph_step()
-    e2e_graph_us = (time.perf_counter() - t0) * 1e6 / serial_steps
+    e2e_graph_us = host_timed_job(torch, lambda i: graph_step(), serial_steps, world, dev)
     if int(am_host[1]) != int(hd["argmax"].item()) or plan.nt_decode_step_status() != nt.NT_OK:
         raise RuntimeError("graph end-to-end: the token read back differs from the device's")
     del graph
@@ -472,10 +506,7 @@ def run_ours(args, rank, world):
 
     for _ in range(3):
         zero_copy_step()
-    t0 = time.perf_counter()
-    for _ in range(serial_steps):
-        zero_copy_step()
-    e2e_zero_copy_us = (time.perf_counter() - t0) * 1e6 / serial_steps
+    e2e_zero_copy_us = host_timed_job(torch, lambda i: zero_copy_step(), serial_steps, world, dev)
     serial_step()  # the device-input plan's outputs for the same inputs
     torch.cuda.synchronize()
     if (plan_zc.nt_decode_step_status() != nt.NT_OK or int(am_host[1]) != int(hd["argmax"].item())
@@ -528,11 +559,7 @@ def run_ours(args, rank, world):
     for i in range(4):
         e2e_step(i)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e2e_us = (time.perf_counter() - t0) * 1e6 / e2e_steps
+    e2e_us = host_timed_job(torch, e2e_step, e2e_steps, world, dev, sync=torch.cuda.synchronize)
     if plans[1].nt_decode_step_status() != nt.NT_OK:
         raise RuntimeError("end-to-end steps reported a timeout")
     plans[1].close()
