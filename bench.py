@@ -253,6 +253,27 @@ def time_steps(torch, plan, steps, stream, nvtx_name=None):
     return ev0.elapsed_time(ev1) * 1e3  # microseconds
 
 
+def step_distribution(torch, plan, steps, stream):
+    """Per-step device times of `steps` consecutive steps: one CUDA event between every two
+    steps on the launching stream (events add no work between the launches). Median, 10th and
+    90th percentile in microseconds."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        plan.nt_decode_step(stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return percentiles_us([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(steps)])
+
+
+def percentiles_us(d) -> dict:
+    d = np.asarray(d, dtype=np.float64)
+    return {"n": int(d.size), "median": round(float(np.median(d)), 2),
+            "p10": round(float(np.percentile(d, 10)), 2), "p90": round(float(np.percentile(d, 90)), 2),
+            "min": round(float(d.min()), 2), "max": round(float(d.max()), 2)}
+
+
 def cpu_baseline(oracle, budget_s=12.0):
     """The oracle on a bounded sample of the same workload, scaled to microseconds per token:
     a whole decoder layer (7 projections, the layer's int8 quantization included) and a
@@ -443,6 +464,10 @@ def run_ours(args, rank, world):
     us = max_over_ranks(torch, us, world, dev)
     per_step_us = us / args.steps
     value = job_us_per_token(us, args.steps, world)
+    # after the timed region: the spread of single steps (at least 50), this rank's
+    dist_steps = step_distribution(torch, plan, max(50, min(args.steps, 2000)), stream)
+    if plan.nt_decode_step_status() != nt.NT_OK:
+        raise RuntimeError("persistent step reported a timeout in the per-step timing")
 
     # Serial end to end through the same public call: every step copies its fp32 inputs from
     # pinned host memory, runs, and reads its token back to the host before the next step
@@ -776,6 +801,8 @@ def run_ours(args, rank, world):
         "e2e_pipelined": {"value": round(e2e_us, 2), "unit": "us/token",
                           "h2d_bytes_per_step": int(x_all.numel() * 4), "d2h_bytes_per_step": 4,
                           "what": "step i+1's input copy overlaps step i (inputs supplied, not produced)"},
+        "step_distribution": dict(dist_steps, unit="us", what="single steps, one event between every two, "
+                                  "after the timed region (this rank)"),
         "gpu_launches": args.steps,
         "clocks": clk,
         "parity": parity if parity_after == "pass" else f"after timing: {parity_after}",

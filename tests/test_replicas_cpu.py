@@ -4,7 +4,9 @@
 no exchange step, so no data-path collective): the ranks start each timed window together, the
 job's window is the slowest rank's, and the whole-job figure counts every rank's tokens. These
 tests run the same helpers as two `gloo` ranks on CPU; the reference arm's other ranks exit
-without work; the clock record is parsed from nvidia-smi's CSV rows.
+without work; the clock record is parsed from nvidia-smi's CSV rows; the per-step spread is
+computed from events recorded between consecutive steps (driven here by stand-ins for the CUDA
+events and the plan).
 """
 import json
 import os
@@ -106,3 +108,51 @@ def test_committed_traffic_profile_matches_the_kernel_sources():
     # the bench reports DRAM traffic only while the capture was taken on these exact sources
     assert bench.read_traffic() is not None, "profile's source hash differs: re-capture the traffic"
     assert abs(bench.read_traffic() / bench.step_bytes() - 1.0) < 0.01
+
+
+class _FakeEvent:
+    clock = [0.0]
+
+    def __init__(self, enable_timing=False):
+        assert enable_timing
+        self.t = None
+
+    def record(self, stream):
+        assert stream == "launch-stream"
+        self.t = _FakeEvent.clock[0]
+
+    def elapsed_time(self, other):  # milliseconds, as CUDA events report
+        return other.t - self.t
+
+
+class _FakeCuda:
+    Event = _FakeEvent
+
+    @staticmethod
+    def synchronize():
+        pass
+
+
+class _FakeTorch:
+    cuda = _FakeCuda
+
+
+class _FakePlan:
+    def __init__(self, step_ms):
+        self.step_ms, self.calls = step_ms, 0
+
+    def nt_decode_step(self, stream):
+        assert stream == "launch-stream"
+        _FakeEvent.clock[0] += self.step_ms[self.calls]
+        self.calls += 1
+
+
+def test_step_distribution_times_each_step_between_its_events():
+    step_ms = [0.330 + 0.001 * (i % 10) for i in range(60)]  # 330 ... 339 us, six times each
+    _FakeEvent.clock[0] = 5.0
+    plan = _FakePlan(step_ms)
+    got = bench.step_distribution(_FakeTorch, plan, 60, "launch-stream")
+    assert plan.calls == 60
+    assert got["n"] == 60 and got["min"] == 330.0 and got["max"] == 339.0
+    assert got["median"] == pytest.approx(334.5, abs=0.01)
+    assert 330.0 <= got["p10"] <= 331.0 and 338.0 <= got["p90"] <= 339.0
