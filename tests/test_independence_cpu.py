@@ -61,7 +61,8 @@ def test_only_tests_entry_and_benchmark_import_the_oracle():
     allowed = {"bench.py", "__graft_entry__.py"}
     for f in _py_files("."):
         rel = os.path.relpath(f, ROOT)
-        top = rel.split(os.sep)[0]
+        parts = rel.split(os.sep)
+        top = parts[0] if len(parts) > 1 else ""
         if top in ("tests", "oracle", "baseline") or top.startswith(("_", ".")) or top.endswith("_out"):
             continue  # the tests, the oracle itself, the reference install, scratch folders
         if "oracle" in _imported_roots(f):
