@@ -339,7 +339,8 @@ nt_status nt_rmsnorm(const float* x, const float* gamma, int B, int D, float eps
  * Decode step: every projection of every layer, then optionally the output projection, in
  * one submission ("A 104 microsecond floor ...": on the instrumented A100 step, roughly
  * 590 of 694 microseconds were spent across about 120 kernel boundaries rather than in
- * DRAM transfers, and a single fused kernel's software barriers brought similar waits back).
+ * DRAM transfers; fusing the step into one kernel moved that cost into its grid-wide
+ * synchronisation instead of removing it).
  */
 enum nt_step_mode {
   NT_STEP_INDEPENDENT = 0, /* every projection has its own supplied input; no ordering */
