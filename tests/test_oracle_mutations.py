@@ -1,10 +1,11 @@
 """Planted mistakes in the oracle are caught by its pins (CPU only).
 
 Each mutation edits a copy of oracle/oracle.c in a temporary directory -- a wrong sign code,
-reversed field order, a dropped term, a dropped scale, the wrong tie rule, truncation instead
-of rounding, a wrong scale divisor, a wrong pair code, a transposed tile offset -- builds it,
-and runs the pin checks against it. Every mutant must fail at least one check; the real
-oracle must pass all of them.
+reversed field order, a dropped term, a dropped scale or one taken from the wrong row or
+vector, a signed maximum, the wrong tie rule, truncation instead of rounding, a wrong scale
+divisor, a wrong pair code or nibble order, a transposed tile offset, an off-by-one in the
+gather's token range or in the acceptance rule -- builds it, and runs the pin checks against
+it. Every mutant must fail at least one check; the real oracle must pass all of them.
 """
 import os
 
@@ -34,6 +35,23 @@ MUTATIONS = {
     "embed_scale_of_row_zero": ("v = (float)T[(int64_t)t * K + k] * s[t];",
                                 "v = (float)T[(int64_t)t * K + k] * s[0];"),
     "verify_compares_next_position": ("draft[j] == argmax[j])", "draft[j] == argmax[j + 1])"),
+    "row_scale_dropped": ("      f = f * s_w[n];\n", ""),
+    "row_scale_of_row_zero": ("f = f * s_w[n];", "f = f * s_w[0];"),
+    "table_scale_dropped": ("      f = f * s_T[v];\n", ""),
+    "absmax_signed": ("float a = fabsf(xb[k]);", "float a = xb[k];"),
+    "every_vector_uses_the_first": (
+        "    const int8_t* qb = q + (int64_t)b * K;\n#pragma omp parallel for schedule(static) reduction(min : status)\n"
+        "    for (int n = 0; n < N; ++n) {",
+        "    const int8_t* qb = q;\n#pragma omp parallel for schedule(static) reduction(min : status)\n"
+        "    for (int n = 0; n < N; ++n) {"),
+    "activation_scale_of_first_vector": ("      f = f * s_x[b];\n      y[o] = f;", "      f = f * s_x[0];\n      y[o] = f;"),
+    "embed_token_zero_rejected": ("if (t >= 0 && t < V) v =", "if (t > 0 && t < V) v ="),
+    "embed_high_tokens_not_counted": ("if (t < 0 || t >= V) ++bad;", "if (t < 0) ++bad;"),
+    "verify_stops_one_early": ("while (j < B - 1 && draft[j] == argmax[j])", "while (j < B - 2 && draft[j] == argmax[j])"),
+    "verify_count_short": ("  return j + 1;\n}", "  return j;\n}"),
+    "tiled_nibbles_reversed": ("word |= (uint32_t)lo << (4 * i);", "word |= (uint32_t)lo << (4 * (3 - i));"),
+    "tiled_pair_halves_swapped": ("pair_code(trit_or_zero(w, N, K, n, k0 + i), trit_or_zero(w, N, K, n, k0 + 4 + i))",
+                                  "pair_code(trit_or_zero(w, N, K, n, k0 + 4 + i), trit_or_zero(w, N, K, n, k0 + i))"),
 }
 
 
@@ -61,6 +79,18 @@ def _check_gemm_matmul(o):
     q = synth.int8_uniform(K, 1, 2)
     acc, _, _ = o.gemv(w, np.ones(N, np.float32), N, K, q, np.float32(1))
     return np.array_equal(acc.astype(np.int64), t @ q.astype(np.int64))
+
+
+def _check_gemm_batched(o):
+    # three vectors with their own power-of-two scales: each row of acc and y is its own vector's
+    N, K, B = 5, 32, 3
+    w = synth.ternary_plain(N, K, 3, 1)
+    t = synth.ternary_dense(N, K, 3, 1).astype(np.int64)
+    q = synth.int8_uniform(B * K, 3, 2).reshape(B, K)
+    s_x = np.array([0.5, 2.0, 0.25], np.float32)
+    acc, y, _ = o.gemm(w, np.ones(N, np.float32), N, K, q, s_x)
+    want = q.astype(np.int64) @ t.T
+    return np.array_equal(acc.astype(np.int64), want) and np.array_equal(y, want * s_x[:, None].astype(np.float64))
 
 
 def _check_quantize(o):
@@ -113,7 +143,7 @@ def _check_verify(o):
                for d, a, e in verifies)
 
 
-CHECKS = [_check_plain, _check_gemv, _check_gemm_matmul, _check_quantize, _check_logits,
+CHECKS = [_check_plain, _check_gemv, _check_gemm_matmul, _check_gemm_batched, _check_quantize, _check_logits,
           _check_tiled, _check_embed, _check_verify]
 
 
