@@ -236,3 +236,113 @@ def test_attention_chain_zero_weights_average_the_cache():
     q, s = oracle.quantize(lo.rmsnorm(x0, g).astype(np.float32))
     _, am, _ = oracle.logits_argmax(T, s_T, V, 128, q, s)
     assert np.array_equal(out["argmax"], am)
+
+
+# ---- the chained step with attention, stage by stage on selection weights ----------------------
+
+def att_selection_model(n_layers, seed):
+    rng = np.random.default_rng(seed)
+    layers, sel = [], []
+    for _ in range(n_layers):
+        mats, s = [], []
+        for N, K in SHAPES_ATT:
+            t, pi, sg = selection(N, K, rng)
+            mats.append((pack_plain(t), np.ones(N, dtype=np.float32), N, K))
+            s.append((pi, sg))
+        layers.append(mats)
+        sel.append(s)
+    return layers, sel
+
+
+def check_selection_attention(decode_chained_attention, n_layers=2, B=3, pos=5, seed=23):
+    """Every stage of a chained step with attention checked against the tensor that must feed it:
+    with selection weights each projection is its own quantized input, permuted and signed
+    (within the quantizer's bound); the cache rows, the attention output, both residual sums,
+    the gated product and the output projection's input are checked exactly against the pinned
+    layer operations applied to the step's own values."""
+    layers, sel = att_selection_model(n_layers, seed)
+    ts, Hq, Hkv = 12, SHAPES_ATT[0][0] // 128, SHAPES_ATT[1][0] // 128
+    x0 = synth.normal(B * 128, seed, 1).reshape(B, 128)
+    kc = [lo.bf16_round(synth.normal(Hkv * ts * 128, seed, 2 + l).reshape(Hkv, ts, 128)) for l in range(n_layers)]
+    vc = [lo.bf16_round(synth.normal(Hkv * ts * 128, seed, 4 + l).reshape(Hkv, ts, 128)) for l in range(n_layers)]
+    k0, v0 = [k.copy() for k in kc], [v.copy() for v in vc]
+    ga = [synth.scales(128, 1.0, seed, 10 + l) for l in range(n_layers)]
+    gf = [synth.scales(128, 1.0, seed, 20 + l) for l in range(n_layers)]
+    gl = synth.scales(128, 1.0, seed, 30)
+    V = 40
+    T = synth.int8_uniform(V * 128, seed, 31).reshape(V, 128)
+    s_T = synth.scales(V, 4096.0, seed, 32)
+    out = decode_chained_attention(oracle.default(), layers, x0, (T, s_T, V, 128), kc, vc, pos,
+                                   norm_attn=ga, norm_ffn=gf, norm_final=gl)
+    posv = pos + np.arange(B)
+    ok = np.array_equal(out["h"][0], x0)
+    for l in range(n_layers):
+        y, s = out["y"][7 * l:7 * l + 7], out["s"][7 * l:7 * l + 7]
+        (pq, sq), (pk, sk), (pv, sv), (po, so), (pg, sg), (pu, su), (pd, sd) = sel[l]
+        h, u, a, g, h1 = out["h"][l], out["u"][l], out["a"][l], out["g"][l], out["h"][l + 1]
+        nh = lo.rmsnorm(h, ga[l]).astype(np.float32)
+        ok &= within_quant_bound(y[0], nh, s[0], pq, sq)
+        ok &= within_quant_bound(y[1], nh, s[1], pk, sk)
+        ok &= within_quant_bound(y[2], nh, s[2], pv, sv)
+        k_new = lo.bf16_round(lo.rope(y[1].reshape(B, Hkv, 128), posv).astype(np.float32)).transpose(1, 0, 2)
+        v_new = lo.bf16_round(y[2].reshape(B, Hkv, 128)).transpose(1, 0, 2)
+        ok &= np.array_equal(kc[l][:, pos:pos + B], k_new) and np.array_equal(vc[l][:, pos:pos + B], v_new)
+        ok &= np.array_equal(kc[l][:, :pos], k0[l][:, :pos]) and np.array_equal(vc[l][:, :pos], v0[l][:, :pos])
+        ok &= np.array_equal(kc[l][:, pos + B:], k0[l][:, pos + B:])
+        ok &= np.array_equal(vc[l][:, pos + B:], v0[l][:, pos + B:])
+        qr = lo.rope(y[0].reshape(B, Hq, 128), posv)
+        u_want = lo.attention_decode(qr, kc[l], vc[l], pos + B).reshape(B, Hq * 128).astype(np.float32)
+        ok &= np.array_equal(u, u_want)
+        ok &= within_quant_bound(y[3], u, s[3], po, so)
+        ok &= np.array_equal(a, fp32_add(h, y[3]))
+        na = lo.rmsnorm(a, gf[l]).astype(np.float32)
+        ok &= within_quant_bound(y[4], na, s[4], pg, sg)
+        ok &= within_quant_bound(y[5], na, s[5], pu, su)
+        ok &= np.array_equal(g, (lo.silu(y[4]) * y[5].astype(np.float64)).astype(np.float32))
+        ok &= within_quant_bound(y[6], g, s[6], pd, sd)
+        ok &= np.array_equal(h1, fp32_add(a, y[6]))
+    qh, sh = oracle.quantize(lo.rmsnorm(out["h"][-1], gl).astype(np.float32))
+    ok &= np.array_equal(out["head_q"], qh) and np.array_equal(out["head_s"], sh)
+    logits, am, _ = oracle.logits_argmax(T, s_T, V, 128, qh, sh)
+    ok &= np.array_equal(out["logits"], logits) and np.array_equal(out["argmax"], am)
+    return bool(ok)
+
+
+def test_attention_chain_selection_weights_stage_by_stage():
+    assert check_selection_attention(chain_mod.decode_chained_attention)
+
+
+ATT_MUTATIONS = {
+    "q_not_rotated": ("qr = lo.rope(y_q.reshape(B, Hq, 128), posv, base)", "qr = y_q.reshape(B, Hq, 128)"),
+    "k_rotated_one_position_late": ("kr = lo.rope(y_k.reshape(B, Hkv, 128), posv, base)",
+                                    "kr = lo.rope(y_k.reshape(B, Hkv, 128), posv + 1, base)"),
+    "k_cached_unrotated": ("lo.bf16_round(kr.astype(np.float32))", "lo.bf16_round(y_k.reshape(B, Hkv, 128))"),
+    "v_cache_from_k": ("v_cache[l][:, pos:pos + B] = lo.bf16_round(y_v.reshape",
+                       "v_cache[l][:, pos:pos + B] = lo.bf16_round(y_k.reshape"),
+    "cache_rows_one_late": ("k_cache[l][:, pos:pos + B] =", "k_cache[l][:, pos + 1:pos + 1 + B] ="),
+    "attention_misses_newest_row": ("lo.attention_decode(qr, k_cache[l], v_cache[l], pos + B)",
+                                    "lo.attention_decode(qr, k_cache[l], v_cache[l], pos + B - 1)"),
+    "attention_residual_dropped": ("a = np.add(h, y_o, dtype=np.float32)", "a = y_o.astype(np.float32)"),
+    "ffn_normalises_h": ("qc, sc = o.quantize(norm(a, None if norm_ffn", "qc, sc = o.quantize(norm(h, None if norm_ffn"),
+    "attention_norm_weights_of_ffn": ("norm(h, None if norm_attn is None else norm_attn[l])",
+                                      "norm(h, None if norm_attn is None else norm_ffn[l])"),
+    "silu_on_up": ("g = (lo.silu(y_gate) * y_up.astype(np.float64))", "g = (lo.silu(y_up) * y_gate.astype(np.float64))"),
+    "ffn_residual_from_h": ("h = np.add(a, y_down, dtype=np.float32)", "h = np.add(h, y_down, dtype=np.float32)"),
+    "final_norm_dropped": ("qh, sh = o.quantize(norm(h, norm_final))", "qh, sh = o.quantize(h)"),
+}
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name", sorted(ATT_MUTATIONS))
+def test_attention_chain_mutant_is_caught(name):
+    old, new = ATT_MUTATIONS[name]
+    src = open(CHAIN_SRC).read()
+    head, sep, tail = src.partition("def decode_chained_attention")  # plant in the attention step only
+    assert tail.count(old) == 1, f"mutation anchor for {name} not unique"
+    ns = {"__name__": "oracle.chain_mutant", "__package__": "oracle"}
+    exec(compile(head + sep + tail.replace(old, new), "chain_mutant.py", "exec"), ns)
+    try:
+        caught = not check_selection_attention(ns["decode_chained_attention"])
+    except Exception:  # the mistake breaks the arithmetic outright
+        caught = True
+    assert caught, f"mutation {name} was not caught"
