@@ -101,8 +101,15 @@ def expand_by_loops(y_v, n_out, hd):
 def check_selection_chain(decode_chained, n_layers=2, B=3, seed=5):
     layers, sel = build_model(n_layers, seed)
     x0 = synth.normal(B * D, seed, 77).reshape(B, D)
-    out = decode_chained(oracle.default(), layers, x0, None, HD)
+    V = 60
+    T = synth.int8_uniform(V * D, seed, 81).reshape(V, D)
+    s_T = synth.scales(V, 4096.0, seed, 82)
+    out = decode_chained(oracle.default(), layers, x0, (T, s_T, V, D), HD)
     ok = np.array_equal(out["h"][0].view(np.uint32), x0.view(np.uint32))
+    qh, sh = oracle.quantize(out["h"][-1])  # the output projection scores the last residual sum
+    ok &= np.array_equal(out["head_q"], qh) and np.array_equal(out["head_s"], sh)
+    logits, am, _ = oracle.logits_argmax(T, s_T, V, D, qh, sh)
+    ok &= np.array_equal(out["logits"], logits) and np.array_equal(out["argmax"], am)
     for l in range(n_layers):
         y = out["y"][7 * l:7 * l + 7]
         s = out["s"][7 * l:7 * l + 7]
@@ -163,6 +170,7 @@ MUTATIONS = {
                           "np.tile(y_v, (1, G))"),
     "o_fed_from_q": ("u = gqa_single_position(y_v, mats[3][3], head_dim)",
                      "u = out['y'][-3][:, :mats[3][3]]"),
+    "head_scores_a": ("        qh, sh = o.quantize(h)\n", "        qh, sh = o.quantize(a)\n"),
 }
 
 
