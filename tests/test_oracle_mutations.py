@@ -50,6 +50,11 @@ MUTATIONS = {
     "verify_stops_one_early": ("while (j < B - 1 && draft[j] == argmax[j])", "while (j < B - 2 && draft[j] == argmax[j])"),
     "verify_count_short": ("  return j + 1;\n}", "  return j;\n}"),
     "tiled_nibbles_reversed": ("word |= (uint32_t)lo << (4 * i);", "word |= (uint32_t)lo << (4 * (3 - i));"),
+    "invalid_field_not_reported": ("default: *bad = 1; return 0;", "default: return 0;"),
+    "invalid_count_of_minus_code": ("if (((w[i] >> (2 * j)) & 3u) == 2u) ++bad;", "if (((w[i] >> (2 * j)) & 3u) == 3u) ++bad;"),
+    "tiled_readback_second_half_wrong": ("int second = (e >= 4 && e < 8) || e >= 12;", "int second = e >= 8;"),
+    "tiled_readback_row_stride_wrong": ("memcpy(&word, tiled + tile * Kp + j * 16 + 4 * r, 4);",
+                                        "memcpy(&word, tiled + tile * Kp + j * 16 + 4 * (r ^ 1), 4);"),
     "tiled_pair_halves_swapped": ("pair_code(trit_or_zero(w, N, K, n, k0 + i), trit_or_zero(w, N, K, n, k0 + 4 + i))",
                                   "pair_code(trit_or_zero(w, N, K, n, k0 + 4 + i), trit_or_zero(w, N, K, n, k0 + i))"),
 }
@@ -126,6 +131,32 @@ def _check_tiled(o):
     return True
 
 
+def _check_invalid(o):
+    # the invalid field code 10 is counted and refused; 00 / 01 / 11 are not
+    for word, trits in _golden.plain_format():
+        w = np.array([[word]], dtype=np.uint32)
+        if trits is None:
+            if o.count_invalid(w) < 1:
+                return False
+            try:
+                o.unpack_plain(w, 1, 16)
+                return False
+            except oracle.OracleError:
+                pass
+        elif o.count_invalid(w) != 0:
+            return False
+    return all(o.count_invalid(np.array([[2 << (2 * j)]], dtype=np.uint32)) == 1 for j in range(16))
+
+
+def _check_tiled_readback(o):
+    for N, K in [(7, 48), (9, 1040)]:
+        w = synth.ternary_plain(N, K, 4, N + K)
+        back = o.unpack_tiled(o.repack_tiled(w, N, K), N, K)
+        if not np.array_equal(back, synth.ternary_dense(N, K, 4, N + K)):
+            return False
+    return True
+
+
 def _check_embed(o):
     T = np.array([[1, -2, 3, -4], [127, -127, 0, 64], [0, 0, 0, 1]], dtype=np.int8)
     s = np.array([0.5, 0.25, 8.0], dtype=np.float32)
@@ -144,7 +175,7 @@ def _check_verify(o):
 
 
 CHECKS = [_check_plain, _check_gemv, _check_gemm_matmul, _check_gemm_batched, _check_quantize, _check_logits,
-          _check_tiled, _check_embed, _check_verify]
+          _check_tiled, _check_tiled_readback, _check_invalid, _check_embed, _check_verify]
 
 
 def _failures(o):
