@@ -34,3 +34,27 @@ def test_scales_normal_int8_ranges():
     assert abs(x.mean()) < 0.01 and abs(x.std() - 1) < 0.01
     t = synth.int8_uniform(1000000, 0, 4)
     assert t.min() == -127 and t.max() == 127
+
+
+def _splitmix64(state, n):
+    """SplitMix64 (Steele, Lea & Flood 2014; Vigna's reference version): the state advances by
+    the golden-ratio increment and each output is the state through the 64-bit finaliser."""
+    M = (1 << 64) - 1
+    out = []
+    for _ in range(n):
+        state = (state + 0x9E3779B97F4A7C15) & M
+        z = state
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M
+        out.append(z ^ (z >> 31))
+    return out
+
+
+def test_generator_is_splitmix64():
+    # the reference sequence for state 0, as published with the algorithm's reference code
+    assert _splitmix64(0, 3) == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    # draw i of the stream (seed, tag) is output i of SplitMix64 started from the stream's key
+    for seed, tag in [(0, 1), (7, 99), (2**63 + 5, 123456789)]:
+        key = int(synth._load().synth_key(seed, tag))
+        assert synth.draws(seed, tag, 0, 8).tolist() == _splitmix64(key, 8)
+        assert synth.draws(seed, tag, 1000, 3).tolist() == _splitmix64(key, 1003)[1000:]
