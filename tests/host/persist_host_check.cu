@@ -1,8 +1,16 @@
-// Host-side check of the persistent launcher's stage partition (no GPU needed: only host
-// functions run). The partition source is compiled into this program as it is; the test
-// prints "ok <cases>" or the first broken property and exits non-zero.
+// Host-side checks of the persistent launcher's stage partition and shared-memory layout (no
+// GPU needed: only host functions run). The kernel's source is compiled into this program as
+// it is; the test prints "ok <cases>" or the first broken property and exits non-zero.
 //
-// Properties, for random stages of 1-3 unit sets on grids of 1 to 160 CTAs:
+// Shared-memory layout, for every kernel instance, ring depth, vectors per pass and
+// activation length (multiples of 512 up to 65,536): the activation buffers start on 16 bytes
+// (bulk and 16-byte copies), the mbarriers on 8, the head partials, reductions, flags, stage
+// scales and slot rows on their element size, the chained record state on 8 (it holds a
+// pointer); regions follow one another without overlap; every configuration pick_config
+// returns fits the 227 KB budget, and it returns one whenever the shallowest ring with one
+// vector per pass fits.
+//
+// Stage partition, for random stages of 1-3 unit sets on grids of 1 to 160 CTAs:
 //   * every unit of every set is owned by exactly one item (no gap, no overlap);
 //   * an item holds a non-empty unit range, except the empty item a CTA without work gets so
 //     that it still takes part in a stage's grid barrier;
@@ -79,6 +87,47 @@ int check(const std::vector<nt::Unitset>& sets, int grid, bool one_item, bool ba
   return 0;
 }
 
+template <class C>
+int check_layouts(bool chained) {
+  int cases = 0;
+  for (int act_k = 512; act_k <= 65536; act_k += 512) {
+    for (int ns = 2; ns <= nt::kMaxSlots; ++ns)
+      for (int cb = 1; cb <= C::NBMAX; ++cb) {
+        const nt::SmemLayout L = nt::smem_layout<C>(ns, cb, act_k);
+        const int at[] = {L.ring, L.act, L.bars, L.hbest, L.red, L.abort_flag, L.chain_s, L.slot_row,
+                          L.rec_state, L.total};
+        for (int i = 0; i + 1 < 10; ++i)
+          if (at[i + 1] < at[i]) { std::printf("FAIL layout regions out of order\n"); return -1; }
+        if (L.ring != 0 || L.act % 16 || L.bars % 8 || L.hbest % (int)alignof(nt::HeadPartial) || L.red % 4 ||
+            L.abort_flag % 4 || L.chain_s % 4 || L.slot_row % 4 || L.rec_state % 8) {
+          std::printf("FAIL misaligned layout (ns %d, cb %d, act_k %d)\n", ns, cb, act_k);
+          return -1;
+        }
+        if (L.act - L.ring != C::CW * ns * nt::kSlotBytes || L.bars - L.act != 2 * cb * act_k ||
+            L.slot_row + C::CW * nt::kMaxSlots * 4 > L.rec_state || L.total - L.rec_state != (chained ? 32 : 0)) {
+          std::printf("FAIL layout region sizes (ns %d, cb %d, act_k %d)\n", ns, cb, act_k);
+          return -1;
+        }
+        ++cases;
+      }
+    for (int B = 1; B <= nt::kStepMaxBatch; ++B) {
+      if ((B == 1) != (C::NBMAX == 1)) continue;
+      int nslots = 0, chunk_b = 0;
+      size_t smem = 0;
+      const bool ok = nt::pick_config(B, act_k, &nslots, &chunk_b, &smem, chained);
+      const bool any = nt::smem_layout<C>(2, 1, act_k).total <= nt::kMaxSmem;
+      if (ok != any) { std::printf("FAIL pick_config at B %d, act_k %d\n", B, act_k); return -1; }
+      if (ok && (smem > (size_t)nt::kMaxSmem || nslots < 2 || nslots > nt::kMaxSlots || chunk_b < 1 ||
+                 chunk_b > std::min(B, C::NBMAX) || smem != (size_t)nt::smem_layout<C>(nslots, chunk_b, act_k).total)) {
+        std::printf("FAIL picked configuration at B %d, act_k %d\n", B, act_k);
+        return -1;
+      }
+      ++cases;
+    }
+  }
+  return cases;
+}
+
 }  // namespace
 
 int main() {
@@ -86,6 +135,12 @@ int main() {
   const int grids[] = {1, 2, 3, 7, 64, 148, 152, 160};
   const int64_t unit_bytes[] = {512, 1024, 4096, 12288, 4096 + 16};
   int cases = 0;
+  for (int i = 0; i < 4; ++i) {
+    const int n = i == 0 ? check_layouts<nt::Cfg1>(false) : i == 1 ? check_layouts<nt::CfgB>(false)
+                : i == 2 ? check_layouts<nt::Cfg1C>(true) : check_layouts<nt::CfgBC>(true);
+    if (n < 0) return 1;
+    cases += n;
+  }
   for (int rep = 0; rep < 300; ++rep)
     for (int grid : grids)
       for (int ns = 1; ns <= 3; ++ns) {
