@@ -661,7 +661,7 @@ nt_status nt_rope_append(const float* q, const float* k_new, const float* v_new,
   clear_error();
   if (!q || !k_new || !v_new || !q_out || !k_cache || !v_cache) return set_error(NT_ERR_INVALID_ARG, "NULL pointer");
   if (D != kAttnD) return set_error(NT_ERR_UNSUPPORTED, "head dimension must be 128");
-  if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || pos0 < 0 || pos0 + B > t_stride || !(base > 1.0f))
+  if (B < 1 || B > 65535 || Hq < 1 || Hkv < 1 || pos0 < 0 || (int64_t)pos0 + B > t_stride || !(base > 1.0f))
     return set_error(NT_ERR_INVALID_ARG,
                      "need 1 <= B <= 65535, Hq, Hkv >= 1, 0 <= pos0, pos0 + B <= t_stride and base > 1");
   if (!aligned(q, 4) || !aligned(k_new, 4) || !aligned(v_new, 4) || !aligned(q_out, 4) || !aligned(k_cache, 2) ||

@@ -51,7 +51,7 @@ nt_status validate_chain(const nt_decode_desc* d) {
     const int G = Hq / Hkv;
     if (G != 1 && G != 2 && G != 4 && G != 8) return set_error(NT_ERR_UNSUPPORTED, "attention: Hq / Hkv must be 1, 2, 4 or 8");
     if (!d->attn_v_cache) return set_error(NT_ERR_INVALID_ARG, "attention: attn_v_cache is NULL");
-    if (d->attn_pos < 0 || d->attn_pos + d->batch > d->attn_t_stride)
+    if (d->attn_pos < 0 || (int64_t)d->attn_pos + d->batch > d->attn_t_stride)
       return set_error(NT_ERR_INVALID_ARG, "attention: need 0 <= attn_pos and attn_pos + batch <= attn_t_stride");
     for (int l = 0; l < d->n_layers; ++l) {
       if (d->proj[l * kProjPerLayer].N != Hq * 128 || d->proj[l * kProjPerLayer + 1].N != Hkv * 128)
@@ -570,7 +570,7 @@ nt_status nt_decode_plan_set_position(nt_decode_plan* p, int pos, void* stream) 
   clear_error();
   if (!p) return set_error(NT_ERR_INVALID_ARG, "NULL plan");
   if (!p->attn) return set_error(NT_ERR_INVALID_ARG, "the plan has no attention side");
-  if (pos < 0 || pos + p->B > p->t_stride) return set_error(NT_ERR_INVALID_ARG, "need 0 <= pos and pos + batch <= attn_t_stride");
+  if (pos < 0 || (int64_t)pos + p->B > p->t_stride) return set_error(NT_ERR_INVALID_ARG, "need 0 <= pos and pos + batch <= attn_t_stride");
   set_position_kernel<<<1, 1, 0, as_stream(stream)>>>(p->d_pos, pos, p->B);
   return check_launch("set_position_kernel");
 }
