@@ -174,6 +174,8 @@ nt_status nt_repack_ternary(const uint32_t* w_plain, int N, int K, void* w_tiled
  *   s_w      [N] fp32 row scales            q  [K] int8      s_x  [1] fp32
  *   y        [N] fp32 (output)              acc_opt [N] int32 (output) or NULL
  *   K % 16 == 0, N >= 1.
+ * The int32 sums are exact while they fit: |acc| <= 127 K, so for any K up to 16,909,320.
+ * Past that, an input whose sum leaves the int32 range gets no exact result.
  */
 nt_status nt_ternary_gemv(const void* w, int layout, const float* s_w, int N, int K,
                           const int8_t* q, const float* s_x, float* y, int32_t* acc_opt,
@@ -218,6 +220,9 @@ nt_status nt_ternary_gemm(const void* w, int layout, const float* s_w, int N, in
  *       before its first use; every call returns it to that state (unless a wait ran out:
  *       see nt_workspace_status). Calls that share one workspace must not overlap on the
  *       device.
+ * The int32 sums are exact while they fit: |acc| <= 127 * 127 K, so for any K up to 133,144
+ * (the 8B-shaped table has K = 4,096). Past that, a sum that leaves the int32 range gets no
+ * exact result.
  * B = 1 streams T through the persistent dp4a kernel; 2 <= B <= 16 reads T once on the
  * tensor cores (f16 MMA of exactly converted int8 with exact int32 sums); larger B takes
  * several passes of 16. Logits and arg-max are the same in every case.
